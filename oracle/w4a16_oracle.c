@@ -1,0 +1,303 @@
+/*
+ * W4A16 GEMM oracle: a plain, slow, fp64 CPU statement of what the GPU path computes.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline
+ * leg may load or run this code. The product path (libw4a16 and its Python binding) never
+ * touches it, and this file shares no code, header or table with the CUDA sources.
+ *
+ * What is computed (each function below cites the passage it follows):
+ *
+ *   W4A16 ("weights stored in 4-bit, activations remain 16-bit"):
+ *     "RTX 3090 Tested: Qwen's 381 tok/s Myth Busted" (kongchang.com), section
+ *     "What Exactly Is This Stack".
+ *   One weight read shared by B activation rows (y = x . W with x of B rows):
+ *     "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s" (ai.satyajit.si), section
+ *     "One weight read, shared by every stream".
+ *   Canonical packed format of the workload (the pages are silent on it; this is the plainest
+ *   reading the workload definition gives):
+ *     qweight int32 [K/8][N]: nibble j (bits 4j..4j+3, read as an unsigned 32-bit word) of
+ *       qweight[k/8][n] is q[k][n] with j = k mod 8 (low nibble first);
+ *     scales fp16 [K/G][N];
+ *     w[k][n] = fp16_rne((q[k][n] - 8) * scales[k/G][n]);
+ *     y[m][n] = sum_k x[m][k] * w[k][n], summed here in fp64 in ascending k.
+ *
+ * The fp16 codec is written out bit by bit (sign, exponent, mantissa, subnormals, overflow to
+ * infinity, round-to-nearest-even); no compiler half type is used.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- fp16 codec (IEEE binary16) */
+
+/* binary16 bits -> exact double. Subnormal: m * 2^-24; normal: (1024 + m) * 2^(e - 25). */
+double w4o_half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+/* double -> binary16 bits, one rounding to nearest, ties to even. NaN -> 0x7e00 (quiet). */
+uint16_t w4o_double_to_half(double v) {
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    if (isnan(v)) return 0x7e00;
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7c00);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);           /* a = f * 2^e2, f in [0.5, 1)  =>  a in [2^(e2-1), 2^e2) */
+    int ex = e2 - 1;         /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -14) ex = -14;  /* below the normal range the spacing stays 2^-24 */
+    /* the spacing of binary16 values around a is 2^(ex-10); a / spacing is exact in double */
+    double n = ldexp(a, 10 - ex);
+    /* round n to an integer, ties to even, without relying on the FP rounding mode */
+    double fl = floor(n);
+    double diff = n - fl;
+    double r;
+    if (diff > 0.5)
+        r = fl + 1.0;
+    else if (diff < 0.5)
+        r = fl;
+    else
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    /* r * 2^(ex-10) is the rounded magnitude; r in [0, 2048] */
+    if (r >= 2048.0) { /* carried into the next binade */
+        r = 1024.0;
+        ex += 1;
+    }
+    if (r < 1024.0) {
+        /* only possible when ex == -14: subnormal (or zero), mantissa = r */
+        return (uint16_t)(sign | (uint16_t)r);
+    }
+    int field = ex + 15;
+    if (field >= 31) return (uint16_t)(sign | 0x7c00); /* overflow */
+    return (uint16_t)(sign | (uint16_t)(field << 10) | (uint16_t)((int)r - 1024));
+}
+
+void w4o_half_to_double_array(const uint16_t* h, double* out, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) out[i] = w4o_half_to_double(h[i]);
+}
+
+void w4o_double_to_half_array(const double* v, uint16_t* out, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) out[i] = w4o_double_to_half(v[i]);
+}
+
+/* ---------------------------------------------------------------- canonical format */
+
+/* q[k][n]: nibble (k mod 8) of qweight[k/8][n], the word taken as unsigned. */
+int w4o_nibble(const int32_t* qweight, int N, int k, int n) {
+    uint32_t word = (uint32_t)qweight[(size_t)(k / 8) * (size_t)N + (size_t)n];
+    return (int)((word >> (4 * (k % 8))) & 0xFu);
+}
+
+/* w[k][n] = fp16_rne((q - 8) * s). (q - 8) * s has at most 4 + 11 significant bits, so the
+ * double product is exact and w4o_double_to_half applies the only rounding. */
+double w4o_weight(const int32_t* qweight, const uint16_t* scales, int N, int G, int k, int n) {
+    int q = w4o_nibble(qweight, N, k, n);
+    double s = w4o_half_to_double(scales[(size_t)(k / G) * (size_t)N + (size_t)n]);
+    double prod = (double)(q - 8) * s;
+    return w4o_half_to_double(w4o_double_to_half(prod));
+}
+
+void w4o_unpack(const int32_t* qweight, int K, int N, uint8_t* q_out) {
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) q_out[(size_t)k * N + n] = (uint8_t)w4o_nibble(qweight, N, k, n);
+}
+
+void w4o_dequant(const int32_t* qweight, const uint16_t* scales, int K, int N, int G, double* w_out) {
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) w_out[(size_t)k * N + n] = w4o_weight(qweight, scales, N, G, k, n);
+}
+
+static int shape_ok(int M, int N, int K, int G) {
+    if (M < 0 || N <= 0 || K <= 0 || G <= 0) return 0;
+    if (K % 8 != 0 || G % 8 != 0 || K % G != 0) return 0;
+    return 1;
+}
+
+/* ---------------------------------------------------------------- the GEMM */
+
+/* One output column n: w[:, n] is dequantised into col (K doubles), then every requested row m
+ * is summed in ascending k. y and absy receive sum_k x*w and sum_k |x*w|. */
+static void column_dot(const double* xrow, int K, const double* col, double* y, double* absy) {
+    double acc = 0.0, aacc = 0.0;
+    for (int k = 0; k < K; ++k) {
+        double p = xrow[k] * col[k];
+        acc += p;
+        aacc += fabs(p);
+    }
+    *y = acc;
+    *absy = aacc;
+}
+
+static void dequant_column(const int32_t* qweight, const uint16_t* scales, int N, int K, int G, int n,
+                           double* col) {
+    for (int k = 0; k < K; ++k) col[k] = w4o_weight(qweight, scales, N, G, k, n);
+}
+
+/* y[m][n] (fp64) for x given as double [M][K]. Rows of x are used as given. */
+int w4o_gemm_xf64(const double* x, const int32_t* qweight, const uint16_t* scales, int M, int N, int K,
+                  int G, double* y, double* absy, int nthreads) {
+    if (!shape_ok(M, N, K, G)) return 1;
+    if (nthreads < 1) nthreads = 1;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double* col = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!col) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 8)
+#endif
+            for (int n = 0; n < N; ++n) {
+                dequant_column(qweight, scales, N, K, G, n, col);
+                for (int m = 0; m < M; ++m)
+                    column_dot(x + (size_t)m * K, K, col, &y[(size_t)m * N + n], &absy[(size_t)m * N + n]);
+            }
+            free(col);
+        }
+    }
+    return failed ? 2 : 0;
+}
+
+/* y[m][n] for x given as fp16 bits [M][K]: x is decoded exactly to double, then as above. */
+int w4o_gemm(const uint16_t* x, const int32_t* qweight, const uint16_t* scales, int M, int N, int K, int G,
+             double* y, double* absy, int nthreads) {
+    if (!shape_ok(M, N, K, G)) return 1;
+    double* xd = (double*)malloc(sizeof(double) * ((size_t)M * K + 1));
+    if (!xd) return 2;
+    w4o_half_to_double_array(x, xd, (int64_t)M * K);
+    int rc = w4o_gemm_xf64(xd, qweight, scales, M, N, K, G, y, absy, nthreads);
+    free(xd);
+    return rc;
+}
+
+/* The same sum for a list of (m, n) pairs only: used where the full product is too large. */
+int w4o_gemm_sampled(const uint16_t* x, const int32_t* qweight, const uint16_t* scales, int M, int N, int K,
+                     int G, const int64_t* ms, const int64_t* ns, int64_t count, double* y, double* absy,
+                     int nthreads) {
+    if (!shape_ok(M, N, K, G)) return 1;
+    for (int64_t i = 0; i < count; ++i)
+        if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N) return 1;
+    if (nthreads < 1) nthreads = 1;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double* col = (double*)malloc(sizeof(double) * (size_t)K);
+        double* xr = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!col || !xr) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t i = 0; i < count; ++i) {
+                int m = (int)ms[i], n = (int)ns[i];
+                dequant_column(qweight, scales, N, K, G, n, col);
+                for (int k = 0; k < K; ++k) xr[k] = w4o_half_to_double(x[(size_t)m * K + k]);
+                column_dot(xr, K, col, &y[i], &absy[i]);
+            }
+        }
+        free(col);
+        free(xr);
+    }
+    return failed ? 2 : 0;
+}
+
+/* ---------------------------------------------------------------- the device layout
+ *
+ * The one-time re-layout the GPU path streams from (a bijection of the canonical bytes). This is
+ * the library's own format, stated here independently of the CUDA code:
+ *
+ *   weights: uint32 Wr[N/32][K/32][32][4]. For column n (tile t = n/32, lane l = n mod 32) and
+ *            k (block b = k/32, word w = (k mod 32)/8, j = k mod 8), q[k][n] sits in nibble
+ *            position p of Wr[t][b][l][w], where p = 0,4,1,5,2,6,3,7 for j = 0..7
+ *            (positions 0..3 hold the even k of the word, positions 4..7 the odd k).
+ *   scales:  uint16 Sr[N/32][K/G][32], Sr[t][g][l] = scales[g][32t + l].
+ */
+static const int kPosOfJ[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+
+static int layout_ok(int N, int K, int G) {
+    return N > 0 && K > 0 && G > 0 && N % 32 == 0 && K % 32 == 0 && K % G == 0 && G % 8 == 0;
+}
+
+int w4o_repack(const int32_t* qweight, const uint16_t* scales, int K, int N, int G, uint32_t* wr, uint16_t* sr) {
+    if (!layout_ok(N, K, G)) return 1;
+    size_t nwords = (size_t)N * K / 8;
+    memset(wr, 0, nwords * sizeof(uint32_t));
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < N; ++n) {
+            uint32_t q = (uint32_t)w4o_nibble(qweight, N, k, n);
+            int t = n / 32, l = n % 32, b = k / 32, w = (k % 32) / 8, j = k % 8;
+            size_t idx = (((size_t)t * (K / 32) + b) * 32 + l) * 4 + w;
+            wr[idx] |= q << (4 * kPosOfJ[j]);
+        }
+    }
+    for (int g = 0; g < K / G; ++g)
+        for (int n = 0; n < N; ++n) {
+            int t = n / 32, l = n % 32;
+            sr[((size_t)t * (K / G) + g) * 32 + l] = scales[(size_t)g * N + n];
+        }
+    return 0;
+}
+
+int w4o_unrepack(const uint32_t* wr, const uint16_t* sr, int K, int N, int G, int32_t* qweight, uint16_t* scales) {
+    if (!layout_ok(N, K, G)) return 1;
+    size_t nwords = (size_t)N * K / 8;
+    memset(qweight, 0, nwords * sizeof(int32_t));
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < N; ++n) {
+            int t = n / 32, l = n % 32, b = k / 32, w = (k % 32) / 8, j = k % 8;
+            size_t idx = (((size_t)t * (K / 32) + b) * 32 + l) * 4 + w;
+            uint32_t q = (wr[idx] >> (4 * kPosOfJ[j])) & 0xFu;
+            uint32_t* dst = (uint32_t*)&qweight[(size_t)(k / 8) * N + n];
+            *dst |= q << (4 * (k % 8));
+        }
+    }
+    for (int g = 0; g < K / G; ++g)
+        for (int n = 0; n < N; ++n) {
+            int t = n / 32, l = n % 32;
+            scales[(size_t)g * N + n] = sr[((size_t)t * (K / G) + g) * 32 + l];
+        }
+    return 0;
+}
+
+int w4o_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int w4o_has_openmp(void) {
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}

@@ -1,0 +1,349 @@
+"""Pins for the CPU oracle: each checks the oracle against something other than itself.
+
+Sources of truth used here (none of them is the oracle's own code):
+  * numpy's binary16 conversions and float16 arithmetic (library routines);
+  * torch's CPU float16 multiply, which rounds the exact fp32 product once (library routine);
+  * exact rational arithmetic (``fractions.Fraction``) on tiny inputs;
+  * closed forms: one-hot rows, all-ones rows, zero scales, constant weights, linearity;
+  * handcrafted packed words whose nibble order is known by construction.
+
+The W4A16 definition (4-bit weights, 16-bit activations) follows "RTX 3090 Tested: Qwen's 381
+tok/s Myth Busted" (kongchang.com), section "What Exactly Is This Stack"; the product of one
+weight read with several activation rows follows "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s"
+(ai.satyajit.si), section "One weight read, shared by every stream". The canonical format
+(low nibble first, offset 8, fp16 group scales) is the workload's, not the pages'.
+
+``test_planted_mistake_is_caught`` compiles altered copies of the oracle's C source (a dropped
+term, a wrong sign, a wrong index, a transposed operand, a wrong rounding ...) and checks that
+at least one pin fails for every one of them.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a16_inputs as inputs
+
+RNG_SEED = 1234
+
+
+# ------------------------------------------------------------------------------ helpers (numpy)
+def np_unpack(qweight: np.ndarray) -> np.ndarray:
+    """Independent numpy reading of the canonical words: q[k, n] (uint8)."""
+    words = np.asarray(qweight).view(np.uint32)
+    K8, N = words.shape
+    out = np.empty((K8 * 8, N), np.uint8)
+    for j in range(8):
+        out[j::8, :] = ((words >> np.uint32(4 * j)) & np.uint32(0xF)).astype(np.uint8)
+    return out
+
+
+def np_dequant(qweight: np.ndarray, scales_bits: np.ndarray, group: int) -> np.ndarray:
+    """w = float16((q - 8) * s) with numpy float16 arithmetic (one rounding of an exact product)."""
+    q = np_unpack(qweight).astype(np.int16) - 8
+    s = np.asarray(scales_bits).view(np.float16)
+    s_full = np.repeat(s, group, axis=0)
+    with np.errstate(all="ignore"):
+        return (q.astype(np.float16) * s_full).astype(np.float64)
+
+
+def f16_bits(values) -> np.ndarray:
+    return np.asarray(values, np.float64).astype(np.float16).view(np.uint16)
+
+
+def random_case(rng, M, K, N, G, scale_kind="mixed"):
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    flat = q.reshape(-1)
+    if flat.size >= 16:
+        flat[:16] = rng.permutation(16)  # every nibble value present
+    if scale_kind == "workload":
+        s = 0.002 * (1.0 + rng.random((K // G, N)))
+    else:  # varied exponents, signs and a few subnormal scales
+        s = rng.choice([-1.0, 1.0], size=(K // G, N)) * np.exp2(rng.uniform(-12, 3, size=(K // G, N)))
+        s.reshape(-1)[::7] = 3.0e-6  # subnormal in binary16
+    x = rng.standard_normal((M, K)) * np.exp2(rng.integers(-3, 3, size=(M, K)))
+    return f16_bits(x), inputs.pack_nibbles(q), f16_bits(s)
+
+
+def same_float(a: np.ndarray, b: np.ndarray) -> bool:
+    """Bit-level equality of float arrays, NaN == NaN, +0 != -0."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    both_nan = np.isnan(a) & np.isnan(b)
+    eq = (a == b) & (np.signbit(a) == np.signbit(b))
+    return bool(np.all(both_nan | eq))
+
+
+# ------------------------------------------------------------------------------ pins
+def pin_half_decode_all(o):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    assert same_float(o.half_to_double(bits), ref)
+
+
+def pin_half_encode(o):
+    rng = np.random.default_rng(RNG_SEED)
+    fin = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    vals = fin.view(np.float16).astype(np.float64)
+    mids = (vals[:-1] + vals[1:]) / 2.0  # exact ties in double
+    rand = rng.choice([-1, 1], 20000) * np.exp2(rng.uniform(-30, 17, 20000))
+    special = np.array([65504.0, 65519.99, 65520.0, 65536.0, 1e10, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                        2.0 ** -14 - 2.0 ** -25, 2.0 ** -14 - 2.0 ** -26, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11,
+                        0.0, -0.0, np.inf, -np.inf, 1e-300, -1e-300])
+    allv = np.concatenate([vals, -vals, mids, -mids, rand, special])
+    with np.errstate(over="ignore"):
+        ref = allv.astype(np.float16).view(np.uint16)
+    got = o.double_to_half(allv)
+    assert np.array_equal(got, ref)
+    assert o.double_to_half(np.array([np.nan]))[0] & 0x7FFF > 0x7C00
+
+
+def pin_dequant_exhaustive(o):
+    """All 16 nibble values x all 65,536 fp16 scale patterns against torch's fp16 multiply."""
+    N = 65536
+    words = np.empty((2, N), np.uint32)
+    words[0, :] = 0x76543210
+    words[1, :] = 0xFEDCBA98
+    scales = np.arange(N, dtype=np.uint32).astype(np.uint16).reshape(1, N)
+    got = o.dequant(words.view(np.int32), scales, 16)
+    qm8 = (torch.arange(16) - 8).to(torch.float16).reshape(16, 1)
+    s = torch.from_numpy(scales.view(np.int16)).view(torch.float16)
+    ref = (qm8 * s).to(torch.float64).numpy()
+    assert same_float(got, ref)
+
+
+def pin_nibble_order(o):
+    w = np.array([[0x76543210, 0xFEDCBA98]], np.uint32).view(np.int32)
+    q = o.unpack(w)
+    assert q[:, 0].tolist() == list(range(8))
+    assert q[:, 1].tolist() == list(range(8, 16))
+
+
+def pin_pack_roundtrip(o):
+    rng = np.random.default_rng(RNG_SEED + 1)
+    words = rng.integers(0, 2 ** 32, size=(6, 5), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    assert np.array_equal(inputs.pack_nibbles(o.unpack(words)), words)
+    q = rng.integers(0, 16, size=(48, 7), dtype=np.uint8)
+    assert np.array_equal(o.unpack(inputs.pack_nibbles(q)), q)
+
+
+def pin_bruteforce_fraction(o):
+    rng = np.random.default_rng(RNG_SEED + 2)
+    for (M, K, N, G) in [(1, 8, 1, 8), (2, 16, 3, 8), (3, 128, 4, 8), (2, 256, 3, 128), (3, 128, 2, 128)]:
+        x, qw, sc = random_case(rng, M, K, N, G)
+        y, a = o.gemm(x, qw, sc, G, nthreads=1)
+        q = np_unpack(qw).astype(np.int64)
+        s = sc.view(np.float16).astype(np.float64)
+        w = np.empty((K, N), object)
+        for k in range(K):
+            for n in range(N):
+                prod = float(q[k, n] - 8) * s[k // G, n]  # exact in double
+                w[k, n] = Fraction(float(np.float64(prod).astype(np.float16)))
+        # Fraction has no signed zero, so compare values (0 == -0) here; signs are pinned elsewhere
+        assert np.array_equal(o.dequant(qw, sc, G), np.array(w, dtype=np.float64))
+        xf = x.view(np.float16).astype(np.float64)
+        for m in range(M):
+            for n in range(N):
+                terms = [Fraction(float(xf[m, k])) * w[k, n] for k in range(K)]
+                exact = sum(terms, Fraction(0))
+                exact_abs = sum((abs(t) for t in terms), Fraction(0))
+                bound = Fraction(K) * Fraction(2) ** -53 * exact_abs
+                assert abs(Fraction(float(y[m, n])) - exact) <= bound
+                assert abs(Fraction(float(a[m, n])) - exact_abs) <= bound
+
+
+def pin_exact_dyadic(o):
+    """Small integers x and power-of-two scales: every partial sum is exact, so y is bit-exact."""
+    rng = np.random.default_rng(RNG_SEED + 3)
+    M, K, N, G = 3, 128, 5, 32
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    xi = rng.integers(-8, 9, size=(M, K))
+    s = np.exp2(rng.integers(-6, 2, size=(K // G, N)).astype(np.float64))
+    y, a = o.gemm(f16_bits(xi), inputs.pack_nibbles(q), f16_bits(s), G, nthreads=1)
+    ref = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            ref[m, n] = sum(int(xi[m, k]) * (int(q[k, n]) - 8) * s[k // G, n] for k in range(K))
+    assert np.array_equal(y, ref)
+
+
+def _workload_matrix(K=256, N=64, G=128, seed=7):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    s = 0.002 * (1.0 + rng.random((K // G, N)))
+    return inputs.pack_nibbles(q), f16_bits(s)
+
+
+def pin_one_hot(o):
+    K, N, G = 256, 64, 128
+    qw, sc = _workload_matrix(K, N, G)
+    w = np_dequant(qw, sc, G)
+    ks = [0, 7, 8, 127, 128, K - 1]
+    x = np.zeros((2 * len(ks), K))
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+        x[len(ks) + i, k] = -2.0
+    y, _ = o.gemm(f16_bits(x), qw, sc, G, nthreads=1)
+    for i, k in enumerate(ks):
+        assert np.array_equal(y[i], w[k])
+        assert np.array_equal(y[len(ks) + i], -2.0 * w[k])
+
+
+def pin_all_ones(o):
+    K, N, G = 256, 64, 128
+    qw, sc = _workload_matrix(K, N, G, seed=8)
+    w = np_dequant(qw, sc, G)
+    y, a = o.gemm(f16_bits(np.ones((1, K))), qw, sc, G, nthreads=1)
+    ref = np.sum(w, axis=0)
+    assert np.all(np.abs(y[0] - ref) <= 1e-12 * np.sum(np.abs(w), axis=0))
+    assert np.allclose(a[0], np.sum(np.abs(w), axis=0), rtol=1e-12, atol=0)
+
+
+def pin_zero_scales(o):
+    rng = np.random.default_rng(RNG_SEED + 4)
+    K, N, G = 256, 32, 128
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    s = np.zeros((K // G, N))
+    s[0, ::2] = -0.0
+    x = f16_bits(rng.standard_normal((3, K)))
+    y, a = o.gemm(x, inputs.pack_nibbles(q), f16_bits(s), G, nthreads=1)
+    assert np.all(y == 0.0) and np.all(a == 0.0)
+
+
+def pin_constant_weights(o):
+    rng = np.random.default_rng(RNG_SEED + 5)
+    K, N, G, M = 256, 32, 128, 3
+    x = f16_bits(rng.standard_normal((M, K)))
+    xs = x.view(np.float16).astype(np.float64)
+    sigma = np.float16(0.0031)
+    for c in (0, 3, 8, 9, 15):
+        q = np.full((K, N), c, np.uint8)
+        s = np.full((K // G, N), float(sigma))
+        y, _ = o.gemm(x, inputs.pack_nibbles(q), f16_bits(s), G, nthreads=1)
+        wc = float(np.float16(c - 8) * sigma)
+        ref = wc * xs.sum(axis=1)
+        if c == 8:
+            assert np.all(y == 0.0)
+        assert np.all(np.abs(y - ref[:, None]) <= 1e-12 * abs(wc) * np.abs(xs).sum(axis=1)[:, None])
+
+
+def pin_linearity(o):
+    rng = np.random.default_rng(RNG_SEED + 6)
+    K, N, G = 384, 32, 128
+    qw, sc = _workload_matrix(K, N, G, seed=9)
+    x1 = rng.standard_normal((2, K))
+    x2 = rng.standard_normal((2, K))
+    al, be = 1.5, -0.75
+    y1, a1 = o.gemm_xf64(x1, qw, sc, G, nthreads=1)
+    y2, a2 = o.gemm_xf64(x2, qw, sc, G, nthreads=1)
+    y3, _ = o.gemm_xf64(al * x1 + be * x2, qw, sc, G, nthreads=1)
+    assert np.all(np.abs(y3 - (al * y1 + be * y2)) <= 1e-12 * (abs(al) * a1 + abs(be) * a2))
+
+
+def pin_sampled_matches_full(o):
+    rng = np.random.default_rng(RNG_SEED + 7)
+    M, K, N, G = 5, 256, 96, 128
+    x, qw, sc = random_case(rng, M, K, N, G, "workload")
+    y, a = o.gemm(x, qw, sc, G, nthreads=2)
+    ms = rng.integers(0, M, 40)
+    ns = rng.integers(0, N, 40)
+    ys, as_ = o.gemm_sampled(x, qw, sc, G, ms, ns, nthreads=2)
+    assert np.array_equal(ys, y[ms, ns]) and np.array_equal(as_, a[ms, ns])
+
+
+def pin_threads_deterministic(o):
+    rng = np.random.default_rng(RNG_SEED + 8)
+    x, qw, sc = random_case(rng, 4, 512, 64, 128, "workload")
+    y1, a1 = o.gemm(x, qw, sc, 128, nthreads=1)
+    y4, a4 = o.gemm(x, qw, sc, 128, nthreads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(a1, a4)
+
+
+def pin_repack_positions(o):
+    """Single-nibble matrices land where the layout statement says (p = 0,4,1,5,2,6,3,7)."""
+    K, N, G = 96, 64, 32
+    pos_of_j = [0, 4, 1, 5, 2, 6, 3, 7]
+    for (k, n) in [(0, 0), (1, 0), (2, 5), (7, 31), (8, 32), (33, 1), (95, 63), (61, 40)]:
+        q = np.zeros((K, N), np.uint8)
+        q[k, n] = 0xA
+        wr, _ = o.repack(inputs.pack_nibbles(q), np.zeros((K // G, N), np.uint16), G)
+        flat = wr.reshape(-1)
+        idx = (((n // 32) * (K // 32) + k // 32) * 32 + n % 32) * 4 + (k % 32) // 8
+        assert np.count_nonzero(flat) == 1
+        assert flat[idx] == np.uint32(0xA << (4 * pos_of_j[k % 8]))
+    sc = np.arange(K // G * N, dtype=np.uint16).reshape(K // G, N)
+    _, sr = o.repack(np.zeros((K // 8, N), np.int32), sc, G)
+    for (g, n) in [(0, 0), (1, 33), (2, 63)]:
+        assert sr[n // 32, g, n % 32] == sc[g, n]
+
+
+def pin_repack_roundtrip(o):
+    rng = np.random.default_rng(RNG_SEED + 9)
+    K, N, G = 256, 96, 64
+    words = rng.integers(0, 2 ** 32, size=(K // 8, N), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    sc = rng.integers(0, 2 ** 16, size=(K // G, N), dtype=np.uint32).astype(np.uint16)
+    wr, sr = o.repack(words, sc, G)
+    qw2, sc2 = o.unrepack(wr, sr, K, N, G)
+    assert np.array_equal(qw2, words) and np.array_equal(sc2, sc)
+
+
+PINS = [pin_half_decode_all, pin_half_encode, pin_dequant_exhaustive, pin_nibble_order, pin_pack_roundtrip,
+        pin_bruteforce_fraction, pin_exact_dyadic, pin_one_hot, pin_all_ones, pin_zero_scales,
+        pin_constant_weights, pin_linearity, pin_sampled_matches_full, pin_threads_deterministic,
+        pin_repack_positions, pin_repack_roundtrip]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pin(pin, oracle_mod):
+    pin(oracle_mod.load())
+
+
+# ------------------------------------------------------------------------------ planted mistakes
+MUTANTS = {
+    "dropped_term": ("for (int k = 0; k < K; ++k) {\n        double p = xrow[k] * col[k];",
+                     "for (int k = 1; k < K; ++k) {\n        double p = xrow[k] * col[k];"),
+    "wrong_sign": ("double prod = (double)(q - 8) * s;", "double prod = (double)(8 - q) * s;"),
+    "wrong_zero_point": ("double prod = (double)(q - 8) * s;", "double prod = (double)(q - 7) * s;"),
+    "wrong_group_index": ("scales[(size_t)(k / G) * (size_t)N", "scales[(size_t)(k / (2 * G)) * (size_t)N"),
+    "nibble_high_first": ("(word >> (4 * (k % 8)))", "(word >> (28 - 4 * (k % 8)))"),
+    "ties_away_from_zero": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
+    "unrounded_weight": ("return w4o_half_to_double(w4o_double_to_half(prod));", "return prod;"),
+    "subnormal_flush_decode": ("v = ldexp((double)m, -24);", "v = 0.0;"),
+    "subnormal_encode": ("if (ex < -14) ex = -14;", ""),
+    "transposed_output": ("&y[(size_t)m * N + n], &absy[(size_t)m * N + n]",
+                          "&y[(size_t)n * M + m], &absy[(size_t)n * M + m]"),
+    "shifted_x_row": ("column_dot(x + (size_t)m * K,", "column_dot(x + (size_t)m,"),
+    "abs_not_abs": ("aacc += fabs(p);", "aacc += p;"),
+    "layout_positions": ("kPosOfJ[8] = {0, 4, 1, 5, 2, 6, 3, 7};", "kPosOfJ[8] = {0, 1, 2, 3, 4, 5, 6, 7};"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path, oracle_mod):
+    old, new = MUTANTS[name]
+    src = oracle_mod.source_text()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    bad = oracle_mod.load_from_source(src.replace(old, new), str(tmp_path))
+    caught = []
+    for pin in PINS:
+        try:
+            pin(bad)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {name}"
+
+
+def test_tolerance_helper_flags_errors(oracle_mod):
+    y_ref = np.array([1.0, -2.0, 0.0, 3.0])
+    a_ref = np.array([2.0, 2.0, 1.0, 4.0])
+    bound = 2.0 ** -10 * (np.abs(y_ref) + a_ref)
+    ok, worst, nbad = oracle_mod.within_tolerance(y_ref + 0.99 * bound, y_ref, a_ref)
+    assert ok and worst < 1.0 and nbad == 0
+    ok, worst, nbad = oracle_mod.within_tolerance(y_ref + 1.01 * bound, y_ref, a_ref)
+    assert not ok and nbad == 4
+    ok, _, nbad = oracle_mod.within_tolerance(np.array([np.nan, -2.0, 0.0, 3.0]), y_ref, a_ref)
+    assert not ok and nbad == 1
