@@ -1,0 +1,140 @@
+/*
+ * libw4a16: the W4A16 weight-streaming GEMM on one GB300 (sm_103a).
+ *
+ *   y[M,N] = x[M,K] . W[K,N]      W stored as 4-bit integers with fp16 group scales,
+ *                                 w[k][n] = fp16_rne((q[k][n] - 8) * s[k/G][n]),
+ *                                 fp16 x, fp32 accumulation, fp16 y (round to nearest even).
+ *
+ * The operation: a weight matrix stored in 4 bits multiplied by 16-bit activations ("RTX 3090
+ * Tested: Qwen's 381 tok/s Myth Busted", kongchang.com, section "What Exactly Is This Stack"),
+ * with one read of the weights shared by all M activation rows of a decode or verify step
+ * ("Qwen3.8-27B at 764, 1,035 and 1,623 tok/s", ai.satyajit.si, sections "One weight read,
+ * shared by every stream" and "Speculation spends the same arithmetic": M = streams x verified
+ * positions). The canonical packed format is the workload's (the pages do not print one):
+ *
+ *   qweight int32 [K/8][N]   nibble j (bits 4j..4j+3 of the word taken as unsigned) of
+ *                            qweight[k/8][n] is q[k][n] with j = k mod 8 (low nibble first)
+ *   scales  fp16  [K/G][N]   (passed as uint16_t bit patterns)
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the library never frees or
+ *     keeps it. Host pointers are rejected where the CUDA runtime can tell (see each call).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls that
+ *     launch work are asynchronous on it and return once the work is queued.
+ *   - The library allocates no device or host memory on any call. Its only device state is one
+ *     status word per device (see w4a16_device_status).
+ *   - Every call returns a w4a16_status. Argument checks happen before any launch; a rejected
+ *     call launches nothing and leaves every buffer untouched.
+ *   - Supported shapes: N % 32 == 0, K % 64 == 0, group % 32 == 0, K % group == 0,
+ *     1 <= M <= 2^20, N <= 2^23, K <= 2^22. x, y, qweight and scales 16-byte aligned.
+ *     x and y must not overlap.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, overlap, host pointer */
+    W4A16_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
+    W4A16_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+    W4A16_ERR_CUDA = 4,              /* the CUDA runtime refused a launch or query */
+    W4A16_ERR_DEVICE_TIMEOUT = 5     /* a kernel gave up a bounded wait (reported by w4a16_device_status) */
+} w4a16_status;
+
+/* Which kernel family runs a GEMM. */
+typedef enum {
+    W4A16_PATH_AUTO = 0, /* the dispatcher decides from (M, N, K) */
+    W4A16_PATH_GEMV = 1, /* CUDA-core split-K GEMV, M <= 8 */
+    W4A16_PATH_TC = 2    /* tcgen05 tensor-core tiles, any M */
+} w4a16_path;
+
+/* A launch plan. Zero fields mean "choose automatically". */
+typedef struct {
+    int path;    /* w4a16_path */
+    int split_k; /* CTAs of one thread-block cluster splitting K (1..16) */
+    int m_tile;  /* TC: activation rows per tile, one of 16, 32, 64, 128, 256 */
+    int k_chunk; /* TC: K per pipeline stage, 64 or 128 */
+    int stages;  /* TC: pipeline depth, 2..8 */
+} w4a16_plan;
+
+/* Library version: major*10000 + minor*100 + patch. */
+int w4a16_version(void);
+
+/* Human-readable name of a w4a16_status value (static string; never NULL). */
+const char* w4a16_status_string(int code);
+
+/* Bytes of the repacked weight / scale buffers for an N x K matrix with group size `group`;
+ * 0 when the shape is unsupported. They equal the canonical sizes, K*N/2 and (K/group)*N*2. */
+size_t w4a16_repacked_qweight_bytes(int N, int K, int group);
+size_t w4a16_repacked_scales_bytes(int N, int K, int group);
+
+/*
+ * One-time re-layout of a canonical matrix into the device layout the GEMM streams
+ * (a bijection of the bytes; not part of the timed step):
+ *   qweight_r: uint32 [N/32][K/32][32][4]  - for column n (tile n/32, lane n mod 32) and k
+ *              (block k/32, word (k mod 32)/8), q[k][n] sits in nibble position
+ *              p = 0,4,1,5,2,6,3,7 for k mod 8 = 0..7. One 16-byte vector holds 32 consecutive
+ *              k of one column; 32 lanes make 512 contiguous bytes per (tile, k-block).
+ *   scales_r:  uint16 [N/32][K/group][32]  - scales_r[t][g][l] = scales[g][32t + l].
+ * In: qweight int32 [K/8][N], scales uint16 [K/group][N] (device). Out: qweight_r
+ * (w4a16_repacked_qweight_bytes), scales_r (w4a16_repacked_scales_bytes) (device, caller
+ * allocated, must not overlap the inputs). Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED,
+ * CUDA.
+ */
+int w4a16_repack(const int32_t* qweight, const uint16_t* scales, void* qweight_r, void* scales_r, int N, int K,
+                 int group, void* stream);
+
+/* Exact inverse of w4a16_repack (used to check the round trip bit for bit). */
+int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight, uint16_t* scales, int N, int K,
+                   int group, void* stream);
+
+/*
+ * y[M][N] = x[M][K] . dequant(W), the hot path of a decode or speculative-verify step.
+ *   x:         fp16 [M][K] row-major (uint16_t bit patterns), device
+ *   qweight_r: repacked weights from w4a16_repack, device
+ *   scales_r:  repacked scales from w4a16_repack, device
+ *   y:         fp16 [M][N] row-major, device, written in full (every element)
+ * The dispatcher picks the kernel family and launch plan from (M, N, K); w4a16_last_dispatch
+ * reports what ran. Accuracy: every element is within 2^-10*|y_exact| + 2^-10*sum_k|x*w| of the
+ * exact result (fp32 accumulation chains are kept short enough for that bound).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA (launch refused).
+ */
+int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
+               int group, void* stream);
+
+/* As w4a16_gemm with an explicit plan (NULL or zero fields = automatic). An invalid plan
+ * (e.g. GEMV with M > 8, split_k larger than the K chunks) returns UNSUPPORTED_SHAPE. */
+int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
+                  int group, const w4a16_plan* plan, void* stream);
+
+/* The plan w4a16_gemm would use for this shape (host only; launches nothing). */
+int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
+
+/* Describes the last GEMM this process launched (path, tile, split, grid) into buf (NUL
+ * terminated, truncated to len). Host only. Returns W4A16_OK or INVALID_ARG. */
+int w4a16_last_dispatch(char* buf, size_t len);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word. Kernels set it
+ * when a bounded wait runs out (W4A16_ERR_DEVICE_TIMEOUT) instead of hanging; the CUDA context
+ * stays usable. Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT, or W4A16_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int w4a16_device_status(void* stream);
+
+/* Limit for every bounded wait inside the kernels, in nanoseconds (default 2e9; minimum 1e5).
+ * Host-side setting applied to launches made after the call. */
+int w4a16_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

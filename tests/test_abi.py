@@ -1,0 +1,105 @@
+"""The C-ABI library loads, exports every entry point include/w4a16.h declares, and rejects bad
+arguments on the host before any launch (no GPU needed: these calls return before touching CUDA)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def W():
+    import __graft_entry__
+
+    __graft_entry__.build_library()
+    import w4a16_weight_streaming_gb300 as W
+
+    return W
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(w4a16_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_gemm_and_repack_calls():
+    names = declared_functions()
+    for n in ("w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(W):
+    lib = ctypes.CDLL(W.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in w4a16.h but not exported"
+    assert sorted(W.EXPORTED) == declared_functions()
+
+
+def test_version_and_status_strings(W):
+    assert W.w4a16_version() >= 100
+    for code in range(6):
+        assert W.status_string(code).startswith("W4A16_")
+    assert W.status_string(99) == "W4A16_ERR_UNKNOWN"
+
+
+def test_repacked_sizes_equal_canonical_sizes(W):
+    for (N, K, G) in [(1024, 1024, 128), (5120, 17408, 128), (34816, 5120, 128), (96, 256, 32)]:
+        assert W.w4a16_repacked_qweight_bytes(N, K, G) == K * N // 2
+        assert W.w4a16_repacked_scales_bytes(N, K, G) == (K // G) * N * 2
+    assert W.w4a16_repacked_qweight_bytes(100, 1024, 128) == 0  # N % 32
+    assert W.w4a16_repacked_scales_bytes(1024, 1000, 128) == 0  # K % 64
+
+
+FAKE = 1 << 40  # never dereferenced: every call below is rejected before any launch
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, FAKE, FAKE, 4, 1024, 1024, 128), 1),          # null x
+    ((FAKE, 0, FAKE, FAKE, 4, 1024, 1024, 128), 1),          # null qweight
+    ((FAKE, FAKE, FAKE, 0, 4, 1024, 1024, 128), 1),          # null y
+    ((FAKE, FAKE, FAKE, FAKE * 2, 0, 1024, 1024, 128), 1),   # M = 0
+    ((FAKE, FAKE, FAKE, FAKE * 2, -3, 1024, 1024, 128), 1),  # M < 0
+    ((FAKE, FAKE, FAKE, FAKE * 2, 4, 1000, 1024, 128), 2),   # N % 32
+    ((FAKE, FAKE, FAKE, FAKE * 2, 4, 1024, 1000, 128), 2),   # K % 64
+    ((FAKE, FAKE, FAKE, FAKE * 2, 4, 1024, 1024, 48), 2),    # group % 32
+    ((FAKE, FAKE, FAKE, FAKE * 2, 4, 1024, 640, 256), 2),    # K % group
+    ((FAKE, FAKE, FAKE, FAKE * 2, (1 << 20) + 1, 1024, 1024, 128), 2),  # M too large
+    ((FAKE + 8, FAKE, FAKE, FAKE * 2, 4, 1024, 1024, 128), 3),          # misaligned x
+    ((FAKE, FAKE, FAKE + 4, FAKE * 2, 4, 1024, 1024, 128), 3),          # misaligned scales
+    ((FAKE, FAKE * 4, FAKE * 4, FAKE + 1024, 4, 1024, 1024, 128), 1),   # y overlaps x
+])
+def test_gemm_rejects_bad_arguments_on_host(W, args, code):
+    assert W.w4a16_gemm(*args, None) == code
+
+
+def test_repack_rejects_bad_arguments_on_host(W):
+    assert W.w4a16_repack(0, FAKE, FAKE * 2, FAKE * 3, 1024, 1024, 128, None) == 1
+    assert W.w4a16_repack(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 1000, 1024, 128, None) == 2
+    assert W.w4a16_repack(FAKE + 2, FAKE * 2, FAKE * 3, FAKE * 4, 1024, 1024, 128, None) == 3
+    # output overlapping the input
+    assert W.w4a16_repack(FAKE, FAKE * 2, FAKE + 64, FAKE * 4, 1024, 1024, 128, None) == 1
+    assert W.w4a16_unrepack(FAKE, FAKE * 2, FAKE * 3, 0, 1024, 1024, 128, None) == 1
+
+
+def test_plan_for_host_only(W):
+    p = W.w4a16_plan_for(1, 5120, 5120, 128)
+    assert p.path in (W.PATH_GEMV, W.PATH_TC)
+    for M in (1, 16, 256, 1024):
+        p = W.w4a16_plan_for(M, 34816, 5120, 128)
+        if p.path == W.PATH_TC:
+            assert p.m_tile in (16, 32, 64, 128, 256) and p.m_tile >= min(M, 16)
+            assert p.k_chunk in (64, 128) and 2 <= p.stages <= 8 and 1 <= p.split_k <= 16
+    with pytest.raises(W.W4A16Error):
+        W.w4a16_plan_for(0, 5120, 5120, 128)
+
+
+def test_wait_timeout_setting(W):
+    assert W.w4a16_set_wait_timeout_ns(10) == 1
+    assert W.w4a16_set_wait_timeout_ns(2_000_000_000) == 0

@@ -1,0 +1,229 @@
+"""W4A16 GEMM on the GPU against the CPU oracle, element by element.
+
+Bound (every element): |y - y_ref| <= 2^-10 |y_ref| + 2^-10 sum_k |x w|, y finite. One-hot rows
+and zero scales are bit-exact. Small shapes span several column tiles, K chunks, cluster splits
+and a ragged last tile; the workload shapes run at full size with sampled oracle elements."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a16_inputs as inputs
+from gpu_util import assert_parity, lib, run_gemm, to_dev, x_to_dev, y_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def W():
+    return lib()
+
+
+def _case(M, K, N, G, seed):
+    d = inputs.generate(M, K, N, G, seed=seed)
+    y_ref, abs_ref = oracle.gemm(d["x"], d["qweight"], d["scales"], G)
+    return d, y_ref, abs_ref
+
+
+def _repacked(W, d, G):
+    x, qw, sc = to_dev(d)
+    qw_r, sc_r = W.repack(qw, sc, G)
+    return x, qw_r, sc_r
+
+
+# ------------------------------------------------------------------------------ oracle-scale workload
+ORACLE_SCALE_PLANS = [
+    None,
+    dict(path=1), dict(path=1, split_k=1), dict(path=1, split_k=2), dict(path=1, split_k=5), dict(path=1, split_k=16),
+    dict(path=2), dict(path=2, m_tile=16, k_chunk=128, stages=3, split_k=1),
+    dict(path=2, m_tile=16, k_chunk=64, stages=4, split_k=2), dict(path=2, m_tile=16, k_chunk=128, stages=2, split_k=3),
+    dict(path=2, m_tile=16, k_chunk=128, stages=3, split_k=8), dict(path=2, m_tile=32, k_chunk=64, stages=6, split_k=16),
+]
+
+
+def plan_id(p):
+    if p is None:
+        return "auto"
+    name = {1: "gemv", 2: "tc"}.get(p.get("path", 0), "auto")
+    return name + "".join(f"-{k[0]}{v}" for k, v in p.items() if k != "path")
+
+
+@pytest.mark.parametrize("plan", ORACLE_SCALE_PLANS, ids=plan_id)
+def test_oracle_scale_workload(W, plan):
+    M, K, N, G = 4, 1024, 1024, 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=0)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+    assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+# ------------------------------------------------------------------------------ ragged / edge shapes
+EDGE_M = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 33, 63, 65, 127, 129, 200, 257, 513]
+
+
+@pytest.fixture(scope="module")
+def edge_matrix(W):
+    K, N, G = 640, 352, 128  # 5 chunks of 128 (uneven splits), 3 column tiles, the last one 96 wide
+    d = inputs.generate(max(EDGE_M), K, N, G, seed=11)
+    x_all, qw_r, sc_r = _repacked(W, d, G)
+    return d, x_all, qw_r, sc_r, K, N, G
+
+
+@pytest.mark.parametrize("M", EDGE_M)
+def test_edge_rows_tc(W, edge_matrix, M):
+    d, x_all, qw_r, sc_r, K, N, G = edge_matrix
+    y_ref, abs_ref = oracle.gemm(d["x"][:M], d["qweight"], d["scales"], G)
+    x = x_all[:M].contiguous()
+    for plan in (None, dict(path=2, split_k=1), dict(path=2, split_k=5)):
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+        assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+@pytest.mark.parametrize("M", [m for m in EDGE_M if m <= 8])
+def test_edge_rows_gemv(W, edge_matrix, M):
+    d, x_all, qw_r, sc_r, K, N, G = edge_matrix
+    y_ref, abs_ref = oracle.gemm(d["x"][:M], d["qweight"], d["scales"], G)
+    x = x_all[:M].contiguous()
+    for split in (1, 3, 16):
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=1, split_k=split))
+        assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+TC_TILES = [(mt, kc) for mt in (16, 32, 64, 128, 256) for kc in (64, 128)]
+
+
+@pytest.mark.parametrize("mt,kc", TC_TILES)
+def test_every_tc_tile(W, mt, kc):
+    M, K, N, G = mt - 3, 1024, 256, 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=mt + kc)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    for split in (1, 3):
+        stages = 4 if kc == 64 else 3
+        if stages * kc // 2 + mt > 512:
+            stages = 2
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=mt, k_chunk=kc, stages=stages, split_k=split))
+        assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+@pytest.mark.parametrize("G", [32, 64, 256])
+def test_group_sizes(W, G):
+    M, K, N = 5, 1024, 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=G)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    plans = [dict(path=1), dict(path=2, k_chunk=64, stages=4), dict(path=2, k_chunk=128, stages=3, split_k=2)]
+    for plan in plans:
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+        assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+# ------------------------------------------------------------------------------ exact cases
+def test_one_hot_rows_are_exact(W):
+    K, N, G = 512, 256, 128
+    d = inputs.generate(1, K, N, G, seed=21)
+    ks = [0, 7, 8, 127, 128, 255, 256, K - 1]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    d["x"] = x.view(np.uint16)
+    w = oracle.dequant(d["qweight"], d["scales"], G)
+    expect = np.stack([w[k] for k in ks]).astype(np.float16)  # every w is an fp16 value
+    xd, qw_r, sc_r = _repacked(W, d, G)
+    plans = [dict(path=1, split_k=1), dict(path=1, split_k=4), dict(path=2, split_k=1), dict(path=2, split_k=4),
+             dict(path=2, m_tile=16, k_chunk=64, stages=4, split_k=8)]
+    for plan in plans:
+        y = run_gemm(W, xd, qw_r, sc_r, N, K, G, plan=plan).cpu().numpy()
+        assert np.array_equal(y.view(np.uint16), expect.view(np.uint16)), W.w4a16_last_dispatch()
+
+
+def test_zero_scales_give_zero(W):
+    M, K, N, G = 9, 512, 128, 128
+    d = inputs.generate(M, K, N, G, seed=22)
+    d["scales"] = np.zeros_like(d["scales"])
+    x, qw_r, sc_r = _repacked(W, d, G)
+    for plan in (dict(path=1), dict(path=2), dict(path=2, split_k=4)):
+        if plan["path"] == 1:
+            y = run_gemm(W, x[:8].contiguous(), qw_r, sc_r, N, K, G, plan=plan)
+        else:
+            y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+        assert torch.count_nonzero(y.float()).item() == 0
+
+
+@pytest.mark.parametrize("qv", [0, 15])
+def test_extreme_nibbles_and_large_x(W, qv):
+    M, K, N, G = 6, 512, 128, 128
+    d = inputs.generate(M, K, N, G, seed=23)
+    q = np.full((K, N), qv, np.uint8)
+    d["qweight"] = inputs.pack_nibbles(q)
+    rng = np.random.default_rng(qv)
+    d["x"] = (rng.choice([-8.0, 8.0], size=(M, K))).astype(np.float16).view(np.uint16)
+    y_ref, abs_ref = oracle.gemm(d["x"], d["qweight"], d["scales"], G)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    for plan in (dict(path=1), dict(path=2), dict(path=2, split_k=4)):
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+        assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+def test_deterministic_and_stream_ordered(W):
+    M, K, N, G = 16, 2048, 512, 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=24)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        y1 = W.gemm(x, qw_r, sc_r, N, K, G, plan=dict(path=2, split_k=4), stream=s)
+        y2 = W.gemm(x, qw_r, sc_r, N, K, G, plan=dict(path=2, split_k=4), stream=s)
+    s.synchronize()
+    assert W.w4a16_device_status(s.cuda_stream) == W.OK
+    assert torch.equal(y1, y2)
+    assert_parity(y_f64(y1), y_ref, abs_ref, "non-default stream")
+
+
+# ------------------------------------------------------------------------------ full-size workloads
+FULL = [(M, K, N, seed) for name in ("decode_gemv", "spec_verify", "batched_verify")
+        for (M, K, N, seed) in inputs.WORKLOADS[name]]
+
+
+@pytest.mark.parametrize("M,K,N,seed", FULL)
+def test_full_size_workloads(W, M, K, N, seed):
+    """The bench's workloads at full size, in the auto launch plan the bench times. M = 1 shapes
+    are compared on every element; larger ones on sampled elements (oracle cost) plus a full
+    finiteness check."""
+    G = inputs.GROUP
+    d = inputs.generate(M, K, N, G, seed=seed)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    y = y_f64(run_gemm(W, x, qw_r, sc_r, N, K, G))
+    assert np.all(np.isfinite(y))
+    if M == 1:
+        y_ref, abs_ref = oracle.gemm(d["x"], d["qweight"], d["scales"], G)
+        assert_parity(y, y_ref, abs_ref, W.w4a16_last_dispatch())
+        return
+    rng = np.random.default_rng(seed)
+    ms = np.concatenate([[0, M - 1, 0, M - 1], rng.integers(0, M, 3000)])
+    ns = np.concatenate([[0, 0, N - 1, N - 1], rng.integers(0, N, 3000)])
+    y_ref, abs_ref = oracle.gemm_sampled(d["x"], d["qweight"], d["scales"], G, ms, ns)
+    assert_parity(y[ms, ns], y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+def test_layer_sweep_all_rows(W):
+    """Every matrix of the dense-layer sweep at every M, auto plan, sampled elements."""
+    G = inputs.GROUP
+    rng = np.random.default_rng(4)
+    for name, K, N in inputs.SWEEP_MATRICES:
+        qweight, scales = inputs.generate_weights(K, N, G, seed=inputs.SWEEP_SEED)
+        qw = torch.from_numpy(qweight).cuda()
+        sc = torch.from_numpy(scales.view(np.int16)).cuda()
+        qw_r, sc_r = W.repack(qw, sc, G)
+        for M in inputs.SWEEP_M:
+            xb = inputs.generate_x(M, K, seed=1000 + M)
+            y = y_f64(run_gemm(W, x_to_dev(xb), qw_r, sc_r, N, K, G))
+            assert np.all(np.isfinite(y)), f"{name} M={M}"
+            ms = rng.integers(0, M, 400)
+            ns = rng.integers(0, N, 400)
+            y_ref, abs_ref = oracle.gemm_sampled(xb, qweight, scales, G, ms, ns)
+            assert_parity(y[ms, ns], y_ref, abs_ref, f"{name} M={M}: {W.w4a16_last_dispatch()}")
+
+
+def test_status_word_clean(W):
+    assert W.w4a16_device_status() == W.OK

@@ -1,0 +1,189 @@
+"""Python binding of libw4a16 (the W4A16 weight-streaming GEMM for GB300, sm_103a).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA kernels of
+``libw4a16.so`` (built in-tree by ``_build.build()``), reached through the C ABI declared in
+``include/w4a16.h``. PyTorch provides device memory and streams. There is no fallback: if the
+library is missing or fails to load, importing this package raises.
+
+Function names mirror the C entry points (``w4a16_repack``, ``w4a16_gemm`` ...), plus two
+conveniences (``repack``, ``gemm``) that allocate the outputs with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+LIB_PATH = _build.LIB_PATH
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED_SHAPE = 2
+ERR_MISALIGNED = 3
+ERR_CUDA = 4
+ERR_DEVICE_TIMEOUT = 5
+
+PATH_AUTO = 0
+PATH_GEMV = 1
+PATH_TC = 2
+
+# every symbol include/w4a16.h declares
+EXPORTED = [
+    "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
+    "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
+    "w4a16_device_status", "w4a16_set_wait_timeout_ns",
+]
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``w4a16_plan``; zero fields mean automatic."""
+
+    _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("m_tile", ctypes.c_int),
+                ("k_chunk", ctypes.c_int), ("stages", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libw4a16.so is not built ({LIB_PATH}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.w4a16_version.restype = I
+    lib.w4a16_status_string.restype = ctypes.c_char_p
+    lib.w4a16_status_string.argtypes = [I]
+    for n in ("w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes"):
+        getattr(lib, n).restype = S
+        getattr(lib, n).argtypes = [I, I, I]
+    for n in ("w4a16_repack", "w4a16_unrepack"):
+        getattr(lib, n).restype = I
+        getattr(lib, n).argtypes = [P, P, P, P, I, I, I, P]
+    lib.w4a16_gemm.restype = I
+    lib.w4a16_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
+    lib.w4a16_gemm_ex.restype = I
+    lib.w4a16_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
+    lib.w4a16_plan_for.restype = I
+    lib.w4a16_plan_for.argtypes = [I, I, I, I, ctypes.POINTER(Plan)]
+    lib.w4a16_last_dispatch.restype = I
+    lib.w4a16_last_dispatch.argtypes = [ctypes.c_char_p, S]
+    lib.w4a16_device_status.restype = I
+    lib.w4a16_device_status.argtypes = [P]
+    lib.w4a16_set_wait_timeout_ns.restype = I
+    lib.w4a16_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    return lib
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------------------------ raw C ABI
+def status_string(code: int) -> str:
+    return lib.w4a16_status_string(int(code)).decode()
+
+
+def w4a16_version() -> int:
+    return lib.w4a16_version()
+
+
+def w4a16_repacked_qweight_bytes(N: int, K: int, group: int) -> int:
+    return lib.w4a16_repacked_qweight_bytes(N, K, group)
+
+
+def w4a16_repacked_scales_bytes(N: int, K: int, group: int) -> int:
+    return lib.w4a16_repacked_scales_bytes(N, K, group)
+
+
+def w4a16_repack(qweight: int, scales: int, qweight_r: int, scales_r: int, N: int, K: int, group: int,
+                 stream: int | None) -> int:
+    return lib.w4a16_repack(qweight, scales, qweight_r, scales_r, N, K, group, stream)
+
+
+def w4a16_unrepack(qweight_r: int, scales_r: int, qweight: int, scales: int, N: int, K: int, group: int,
+                   stream: int | None) -> int:
+    return lib.w4a16_unrepack(qweight_r, scales_r, qweight, scales, N, K, group, stream)
+
+
+def w4a16_gemm(x: int, qweight_r: int, scales_r: int, y: int, M: int, N: int, K: int, group: int,
+               stream: int | None) -> int:
+    return lib.w4a16_gemm(x, qweight_r, scales_r, y, M, N, K, group, stream)
+
+
+def w4a16_gemm_ex(x: int, qweight_r: int, scales_r: int, y: int, M: int, N: int, K: int, group: int,
+                  plan: Plan | None, stream: int | None) -> int:
+    return lib.w4a16_gemm_ex(x, qweight_r, scales_r, y, M, N, K, group,
+                             ctypes.byref(plan) if plan is not None else None, stream)
+
+
+def w4a16_plan_for(M: int, N: int, K: int, group: int) -> Plan:
+    p = Plan()
+    rc = lib.w4a16_plan_for(M, N, K, group, ctypes.byref(p))
+    if rc != OK:
+        raise W4A16Error(rc, "w4a16_plan_for")
+    return p
+
+
+def w4a16_last_dispatch() -> str:
+    buf = ctypes.create_string_buffer(512)
+    lib.w4a16_last_dispatch(buf, len(buf))
+    return buf.value.decode()
+
+
+def w4a16_device_status(stream: int | None = None) -> int:
+    return lib.w4a16_device_status(stream)
+
+
+def w4a16_set_wait_timeout_ns(ns: int) -> int:
+    return lib.w4a16_set_wait_timeout_ns(int(ns))
+
+
+# ------------------------------------------------------------------------------ torch conveniences
+def _stream_handle(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise W4A16Error(rc, where)
+
+
+def repack(qweight: torch.Tensor, scales: torch.Tensor, group: int = 128, stream=None):
+    """Device layout from canonical device tensors (int32 [K/8, N], float16/int16 [K/G, N])."""
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    qw_r = torch.empty(w4a16_repacked_qweight_bytes(N, K, group) // 4, dtype=torch.int32, device=qweight.device)
+    sc_r = torch.empty(max(w4a16_repacked_scales_bytes(N, K, group) // 2, 1), dtype=torch.int16,
+                       device=qweight.device)
+    _check(w4a16_repack(qweight.data_ptr(), scales.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), N, K, group,
+                        _stream_handle(stream)), "w4a16_repack")
+    return qw_r, sc_r
+
+
+def unrepack(qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, group: int = 128, stream=None):
+    qw = torch.empty((K // 8, N), dtype=torch.int32, device=qweight_r.device)
+    sc = torch.empty((K // group, N), dtype=torch.int16, device=qweight_r.device)
+    _check(w4a16_unrepack(qweight_r.data_ptr(), scales_r.data_ptr(), qw.data_ptr(), sc.data_ptr(), N, K, group,
+                          _stream_handle(stream)), "w4a16_unrepack")
+    return qw, sc
+
+
+def gemm(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, group: int = 128,
+         y: torch.Tensor | None = None, plan: Plan | dict | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] (float16) = x[M, K] (float16, CUDA) . dequant(W) through w4a16_gemm / w4a16_gemm_ex."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if isinstance(plan, dict):
+        plan = Plan(**plan)
+    _check(w4a16_gemm_ex(x.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K, group, plan,
+                         _stream_handle(stream)), "w4a16_gemm")
+    return y

@@ -1,0 +1,214 @@
+// CUDA-core split-K GEMV for the smallest decode batches (M <= 8).
+//
+// One CTA = 4 warps on one 32-column tile of W and one K-slice. Lane l owns column 32t + l and
+// streams its 16-byte vectors (32 k each); the 4 warps interleave over the K-slice's 32-k blocks
+// and combine through shared memory. The K-slices of one column tile form a thread-block
+// cluster and are summed through distributed shared memory, in a fixed rank order, by the CTA
+// that owns each output element. Activations of the K-slice are staged once in shared memory as
+// fp16 and read as broadcasts; products are fp16 x fp16 rounded once into fp32 accumulators.
+//
+// Per weight: ~1.6 instructions of exact dequantisation (common.cuh) + M fused multiply-adds.
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kUnroll = 4;  // 32-k blocks in flight per warp
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+struct GemvSlice {
+    int kb_begin, kb_end, klen;  // 32-k blocks [kb_begin, kb_end), klen = K elements in slice
+};
+
+__device__ __forceinline__ GemvSlice slice_of(int rank, int split, int KB) {
+    GemvSlice s;
+    s.kb_begin = static_cast<int>((static_cast<int64_t>(rank) * KB) / split);
+    s.kb_end = static_cast<int>((static_cast<int64_t>(rank + 1) * KB) / split);
+    s.klen = (s.kb_end - s.kb_begin) * 32;
+    return s;
+}
+
+// acc[c][m][h]: chain c (word parity), row m, half h (even / odd k of a pair).
+template <int MR>
+__device__ __forceinline__ void gemv_block(const uint4 v, uint16_t sbits, const __half* xs_blk, int klen,
+                                           float (&acc)[2][MR][2]) {
+    const uint32_t s2 = static_cast<uint32_t>(sbits) | (static_cast<uint32_t>(sbits) << 16);
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w2[4];
+        dequant8(words[i], s2, w2);
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs_blk + m * klen + 8 * i);
+            fma2_mixed(acc[i & 1][m][0], acc[i & 1][m][1], w2[0], xv.x);
+            fma2_mixed(acc[i & 1][m][0], acc[i & 1][m][1], w2[1], xv.y);
+            fma2_mixed(acc[i & 1][m][0], acc[i & 1][m][1], w2[2], xv.z);
+            fma2_mixed(acc[i & 1][m][0], acc[i & 1][m][1], w2[3], xv.w);
+        }
+    }
+}
+
+template <int MR>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restrict__ x,
+                                                        const uint4* __restrict__ wr,
+                                                        const uint16_t* __restrict__ sr, uint16_t* __restrict__ y,
+                                                        int N, int K, int G, int split) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int KB = K / 32;
+    const int NG = K / G;
+    const int rank = blockIdx.x;
+    const int t = blockIdx.y;
+    const GemvSlice sl = slice_of(rank, split, KB);
+    const int klen_max = ((KB + split - 1) / split) * 32;
+
+    __half* xs = reinterpret_cast<__half*>(smem);
+    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(MR) * klen_max * 2);  // [kWarps][MR][32]
+    float* part = red + kWarps * MR * 32;                                                  // [MR][32]
+
+    // Stage x[0:MR][slice] as fp16 (16-byte copies).
+    {
+        const int vec_per_row = sl.klen / 8;
+        for (int i = threadIdx.x; i < MR * vec_per_row; i += kThreads) {
+            const int m = i / vec_per_row;
+            const int c = i % vec_per_row;
+            const uint4 v = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(m) * K + sl.kb_begin * 32 + 8 * c);
+            *reinterpret_cast<uint4*>(xs + m * sl.klen + 8 * c) = v;
+        }
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    float acc[2][MR][2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[c][m][0] = acc[c][m][1] = 0.f;
+
+    const uint4* wcol = wr + static_cast<int64_t>(t) * KB * 32 + lane;  // + kb * 32
+    const uint16_t* scol = sr + static_cast<int64_t>(t) * NG * 32 + lane;  // + g * 32
+
+    int kb = sl.kb_begin + warp;
+    for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
+        uint4 v[kUnroll];
+        uint16_t sb[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = kb + kWarps * u;
+            v[u] = ldg_stream(wcol + static_cast<int64_t>(b) * 32);
+            sb[u] = ldg_u16(scol + static_cast<int64_t>((b * 32) / G) * 32);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = kb + kWarps * u;
+            gemv_block<MR>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
+        }
+    }
+    for (; kb < sl.kb_end; kb += kWarps) {
+        const uint4 v = ldg_stream(wcol + static_cast<int64_t>(kb) * 32);
+        const uint16_t sb = ldg_u16(scol + static_cast<int64_t>((kb * 32) / G) * 32);
+        gemv_block<MR>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
+    }
+
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+        red[(warp * MR + m) * 32 + lane] = (acc[0][m][0] + acc[0][m][1]) + (acc[1][m][0] + acc[1][m][1]);
+    __syncthreads();
+
+    const int e = threadIdx.x;  // element (m, lane) = (e / 32, e % 32)
+    if (split == 1) {
+        if (e < MR * 32) {
+            const int m = e / 32, l = e % 32;
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += red[(w * MR + m) * 32 + l];
+            y[static_cast<int64_t>(m) * N + 32 * t + l] = __half_as_ushort(__float2half_rn(s));
+        }
+        return;
+    }
+    if (e < MR * 32) {
+        const int m = e / 32, l = e % 32;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += red[(w * MR + m) * 32 + l];
+        part[e] = s;
+    }
+    cluster_sync_all();
+    if (e < MR * 32 && (e % split) == rank) {
+        const uint32_t local = smem_u32(part + e);
+        float s = 0.f;
+        for (int p = 0; p < split; ++p) s += ld_dsmem_f1(map_peer(local, p));
+        const int m = e / 32, l = e % 32;
+        y[static_cast<int64_t>(m) * N + 32 * t + l] = __half_as_ushort(__float2half_rn(s));
+    }
+    cluster_sync_all();
+}
+
+template <int MR>
+cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
+                          int N, int K, int G, int split, size_t smem, cudaStream_t s) {
+    auto kern = gemv_kernel<MR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (split > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(split, N / 32, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, x, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, N, K, G, split);
+}
+
+}  // namespace
+
+size_t gemv_smem_bytes(int M, int N, int K, int split) {
+    (void)N;
+    const int KB = K / 32;
+    const size_t klen_max = static_cast<size_t>((KB + split - 1) / split) * 32;
+    return static_cast<size_t>(M) * klen_max * 2 + static_cast<size_t>(kWarps + 1) * M * 32 * 4;
+}
+
+cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
+                        int N, int K, int G, int split, const LaunchCtx& ctx) {
+    const size_t smem = gemv_smem_bytes(M, N, K, split);
+    switch (M) {
+        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace w4a16

@@ -1,0 +1,44 @@
+// Host-side interface between the C-ABI layer (w4a16_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace w4a16 {
+
+// Everything a kernel launch needs besides its data pointers.
+struct LaunchCtx {
+    cudaStream_t stream;
+    unsigned* status;     // device address of this device's status word
+    uint64_t timeout_ns;  // limit of every bounded wait
+    int sm_count;
+};
+
+// ---- repack.cu
+cudaError_t launch_repack(const int32_t* qweight, const uint16_t* scales, uint32_t* qweight_r, uint16_t* scales_r,
+                          int N, int K, int G, cudaStream_t s);
+cudaError_t launch_unrepack(const uint32_t* qweight_r, const uint16_t* scales_r, int32_t* qweight, uint16_t* scales,
+                            int N, int K, int G, cudaStream_t s);
+
+// ---- gemv.cu: CUDA-core split-K GEMV, M <= 8.
+constexpr int kGemvMaxM = 8;
+size_t gemv_smem_bytes(int M, int N, int K, int split);
+cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
+                        int N, int K, int G, int split, const LaunchCtx& ctx);
+
+// ---- tc_gemm.cu: tcgen05 tensor-core path.
+struct TcConfig {
+    int m_tile;   // 16, 32, 64, 128, 256
+    int k_chunk;  // 64 or 128
+    int stages;   // 2..8
+    int split;    // CTAs per cluster along K, 1..16
+};
+bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G);
+size_t tc_smem_bytes(const TcConfig& c, int G);
+int tc_tmem_cols(const TcConfig& c);
+cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
+                      int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
+
+}  // namespace w4a16

@@ -1,0 +1,324 @@
+// C-ABI entry points of libw4a16 (declared in include/w4a16.h): argument checks, the per-shape
+// dispatcher, and the per-device status word. Allocates nothing.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "w4a16.h"
+
+namespace w4a16 {
+
+// The one piece of device state: a status word per device, set by kernels whose bounded waits
+// ran out, read and cleared by w4a16_device_status.
+__device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    unsigned* status = nullptr;
+    int sm_count = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+char g_last[320] = "none";
+
+// Resolves (once per device, with that device current) the status word's device address and
+// the SM count. Returns false if the runtime refuses.
+bool device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        d.status = static_cast<unsigned*>(p);
+        d.sm_count = sms;
+        d.ready = true;
+    }
+    *out = d;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rejects pointers the runtime knows to be host memory (pageable host pointers are unknown to
+// it and are reported as unregistered; those cannot be told apart from device pointers of
+// another runtime and pass).
+bool is_host_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_matrix_shape(int N, int K, int G) {
+    if (N <= 0 || K <= 0 || G <= 0) return W4A16_ERR_INVALID_ARG;
+    if (N % 32 != 0 || K % 64 != 0 || G % 32 != 0 || K % G != 0) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (N > (1 << 23) || K > (1 << 22)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    return W4A16_OK;
+}
+
+// ----------------------------------------------------------------------------- dispatcher
+struct Choice {
+    int path;
+    TcConfig tc;
+    int gemv_split;
+};
+
+int gemv_pick_split(int M, int N, int K, int sm_count) {
+    const int KB = K / 32;
+    const int tiles = N / 32;
+    int split = 1;
+    while (split < 16 && split * 2 <= KB &&
+           (tiles * split < 4 * sm_count || gemv_smem_bytes(M, N, K, split) > 96 * 1024))
+        split *= 2;
+    return split;
+}
+
+TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
+    TcConfig c;
+    c.m_tile = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    c.k_chunk = (c.m_tile <= 64 && K % 128 == 0 && (128 % G == 0 || G % 128 == 0)) ? 128 : 64;
+    c.stages = c.m_tile <= 64 ? (c.k_chunk == 128 ? 3 : 6) : 4;
+    while (c.stages > 2 && c.stages * (c.k_chunk / 2) + c.m_tile > 256 && c.m_tile <= 128) --c.stages;
+    c.split = 1;
+    const int per_sm = 512 / tc_tmem_cols(c);
+    const int slots = sm_count * per_sm;
+    const int tiles = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
+    const int C = K / c.k_chunk;
+    // Minimise (waves) x (stages of work per CTA) + a small cost per extra cluster rank.
+    double best = 1e30;
+    for (int s = 1; s <= 16 && s <= C; ++s) {
+        const int ctas = tiles * s;
+        const int waves = (ctas + slots - 1) / slots;
+        const int per_cta = (C + s - 1) / s;
+        const double cost = static_cast<double>(waves) * (per_cta + 2.0) + 0.25 * s;
+        if (cost < best - 1e-9) {
+            best = cost;
+            c.split = s;
+        }
+    }
+    (void)G;
+    return c;
+}
+
+int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, Choice* out) {
+    w4a16_plan p = {};
+    if (plan) p = *plan;
+    if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
+    int path = p.path;
+    if (path == W4A16_PATH_AUTO) path = W4A16_PATH_TC;
+    out->path = path;
+    if (path == W4A16_PATH_GEMV) {
+        if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        int split = p.split_k > 0 ? p.split_k : gemv_pick_split(M, N, K, sm_count);
+        if (split < 1 || split > 16 || split > K / 32) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        if (gemv_smem_bytes(M, N, K, split) > 200 * 1024) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        out->gemv_split = split;
+        return W4A16_OK;
+    }
+    TcConfig c = tc_default(M, N, K, G, sm_count);
+    const bool custom = p.m_tile > 0 || p.k_chunk > 0 || p.stages > 0 || p.split_k > 0;
+    if (p.m_tile > 0) c.m_tile = p.m_tile;
+    if (p.k_chunk > 0) c.k_chunk = p.k_chunk;
+    if (p.stages > 0) c.stages = p.stages;
+    if (p.split_k > 0) c.split = p.split_k;
+    if (custom && p.split_k <= 0) c.split = std::min(c.split, K / c.k_chunk);
+    if (!tc_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    out->tc = c;
+    return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+int w4a16_version(void) { return 100; }
+
+const char* w4a16_status_string(int code) {
+    switch (code) {
+        case W4A16_OK: return "W4A16_OK";
+        case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG: null pointer, bad size, overlap or host pointer";
+        case W4A16_ERR_UNSUPPORTED_SHAPE: return "W4A16_ERR_UNSUPPORTED_SHAPE: shape or plan outside the supported set";
+        case W4A16_ERR_MISALIGNED: return "W4A16_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA: the CUDA runtime refused the call";
+        case W4A16_ERR_DEVICE_TIMEOUT: return "W4A16_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
+        default: return "W4A16_ERR_UNKNOWN";
+    }
+}
+
+size_t w4a16_repacked_qweight_bytes(int N, int K, int group) {
+    if (check_matrix_shape(N, K, group) != W4A16_OK) return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>(K) / 2;
+}
+
+size_t w4a16_repacked_scales_bytes(int N, int K, int group) {
+    if (check_matrix_shape(N, K, group) != W4A16_OK) return 0;
+    return static_cast<size_t>(K / group) * static_cast<size_t>(N) * 2;
+}
+
+static int repack_common_checks(const void* a, const void* b, const void* c, const void* d, int N, int K, int group) {
+    if (!a || !b || !c || !d) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d)) return W4A16_ERR_MISALIGNED;
+    const size_t qb = static_cast<size_t>(N) * K / 2, sb = static_cast<size_t>(K / group) * N * 2;
+    if (overlaps(a, qb, c, qb) || overlaps(a, qb, d, sb) || overlaps(b, sb, c, qb) || overlaps(b, sb, d, sb) ||
+        overlaps(c, qb, d, sb))
+        return W4A16_ERR_INVALID_ARG;
+    if (is_host_pointer(a) || is_host_pointer(b) || is_host_pointer(c) || is_host_pointer(d))
+        return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+int w4a16_repack(const int32_t* qweight, const uint16_t* scales, void* qweight_r, void* scales_r, int N, int K,
+                 int group, void* stream) {
+    const int rc = repack_common_checks(qweight, scales, qweight_r, scales_r, N, K, group);
+    if (rc != W4A16_OK) return rc;
+    const cudaError_t e = launch_repack(qweight, scales, static_cast<uint32_t*>(qweight_r),
+                                        static_cast<uint16_t*>(scales_r), N, K, group,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight, uint16_t* scales, int N, int K,
+                   int group, void* stream) {
+    const int rc = repack_common_checks(qweight_r, scales_r, qweight, scales, N, K, group);
+    if (rc != W4A16_OK) return rc;
+    const cudaError_t e = launch_unrepack(static_cast<const uint32_t*>(qweight_r),
+                                          static_cast<const uint16_t*>(scales_r), qweight, scales, N, K, group,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
+    if (!out) return W4A16_ERR_INVALID_ARG;
+    if (M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo d;
+    const int sms = device_info(&d) ? d.sm_count : 152;
+    Choice ch;
+    const int rc = resolve_plan(M, N, K, group, nullptr, sms, &ch);
+    if (rc != W4A16_OK) return rc;
+    out->path = ch.path;
+    if (ch.path == W4A16_PATH_GEMV) {
+        out->split_k = ch.gemv_split;
+        out->m_tile = out->k_chunk = out->stages = 0;
+    } else {
+        out->split_k = ch.tc.split;
+        out->m_tile = ch.tc.m_tile;
+        out->k_chunk = ch.tc.k_chunk;
+        out->stages = ch.tc.stages;
+    }
+    return W4A16_OK;
+}
+
+int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
+                  int group, const w4a16_plan* plan, void* stream) {
+    if (!x || !qweight_r || !scales_r || !y) return W4A16_ERR_INVALID_ARG;
+    if (M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(qweight_r) || !aligned16(scales_r) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+    const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
+    const size_t qb = static_cast<size_t>(N) * K / 2, sb = static_cast<size_t>(K / group) * N * 2;
+    if (overlaps(x, xb, y, yb) || overlaps(qweight_r, qb, y, yb) || overlaps(scales_r, sb, y, yb))
+        return W4A16_ERR_INVALID_ARG;
+    if (is_host_pointer(x) || is_host_pointer(qweight_r) || is_host_pointer(scales_r) || is_host_pointer(y))
+        return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    Choice ch;
+    const int rc = resolve_plan(M, N, K, group, plan, d.sm_count, &ch);
+    if (rc != W4A16_OK) return rc;
+    LaunchCtx ctx;
+    ctx.stream = static_cast<cudaStream_t>(stream);
+    ctx.status = d.status;
+    ctx.timeout_ns = g_timeout_ns.load();
+    ctx.sm_count = d.sm_count;
+    cudaError_t e;
+    char desc[256];
+    if (ch.path == W4A16_PATH_GEMV) {
+        e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
+                        group, ch.gemv_split, ctx);
+        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%d,%d,1) block=128", M, N, K,
+                 group, ch.gemv_split, ch.gemv_split, N / 32);
+    } else {
+        e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
+                      group, ch.tc, ctx);
+        snprintf(desc, sizeof(desc),
+                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d split_k=%d grid=(%d,%d,%d) "
+                 "block=320 tmem_cols=%d",
+                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.split, ch.tc.split, (N + 127) / 128,
+                 (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc));
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        snprintf(g_last, sizeof(g_last), "%s%s", desc, e == cudaSuccess ? "" : " (launch failed)");
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+}
+
+int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
+               int group, void* stream) {
+    return w4a16_gemm_ex(x, qweight_r, scales_r, y, M, N, K, group, nullptr, stream);
+}
+
+int w4a16_last_dispatch(char* buf, size_t len) {
+    if (!buf || len == 0) return W4A16_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    snprintf(buf, len, "%s", g_last);
+    return W4A16_OK;
+}
+
+int w4a16_device_status(void* stream) {
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, d.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(d.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return W4A16_ERR_CUDA;
+    }
+    return v == 0 ? W4A16_OK : static_cast<int>(v);
+}
+
+int w4a16_set_wait_timeout_ns(uint64_t ns) {
+    if (ns < 100000ull) return W4A16_ERR_INVALID_ARG;
+    g_timeout_ns.store(ns);
+    return W4A16_OK;
+}
+
+}  // extern "C"
