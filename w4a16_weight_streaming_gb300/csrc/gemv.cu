@@ -132,9 +132,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         red[(warp * MR + m) * 32 + lane] = (acc[0][m][0] + acc[0][m][1]) + (acc[1][m][0] + acc[1][m][1]);
     __syncthreads();
 
-    const int e = threadIdx.x;  // element (m, lane) = (e / 32, e % 32)
+    // element e = (m, lane) = (e / 32, e % 32); MR * 32 may exceed the CTA's 128 threads
     if (split == 1) {
-        if (e < MR * 32) {
+        for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
             const int m = e / 32, l = e % 32;
             float s = 0.f;
 #pragma unroll
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         }
         return;
     }
-    if (e < MR * 32) {
+    for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
         const int m = e / 32, l = e % 32;
         float s = 0.f;
 #pragma unroll
@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         part[e] = s;
     }
     cluster_sync_all();
-    if (e < MR * 32 && (e % split) == rank) {
+    for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
+        if ((e % split) != rank) continue;
         const uint32_t local = smem_u32(part + e);
         float s = 0.f;
         for (int p = 0; p < split; ++p) s += ld_dsmem_f1(map_peer(local, p));
