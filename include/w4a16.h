@@ -57,11 +57,12 @@ typedef enum {
 
 /* A launch plan. Zero fields mean "choose automatically". */
 typedef struct {
-    int path;    /* w4a16_path */
-    int split_k; /* CTAs of one thread-block cluster splitting K (1..16) */
-    int m_tile;  /* TC: activation rows per tile, one of 16, 32, 64, 128, 256 */
-    int k_chunk; /* TC: K per pipeline stage, 64 or 128 */
-    int stages;  /* TC: pipeline depth, 2..8 */
+    int path;        /* w4a16_path */
+    int split_k;     /* CTAs of one thread-block cluster splitting K (1..16) */
+    int m_tile;      /* TC: activation rows per tile, one of 16, 32, 64, 128, 256 */
+    int k_chunk;     /* TC: K per pipeline stage, 64, 128 or 256 */
+    int stages;      /* TC: shared-memory pipeline depth, 2..16 */
+    int tmem_stages; /* TC: tensor-memory (dequantised A) pipeline depth, 2..8 */
 } w4a16_plan;
 
 /* Library version: major*10000 + minor*100 + patch. */
@@ -78,11 +79,12 @@ size_t w4a16_repacked_scales_bytes(int N, int K, int group);
 /*
  * One-time re-layout of a canonical matrix into the device layout the GEMM streams
  * (a bijection of the bytes; not part of the timed step):
- *   qweight_r: uint32 [N/32][K/32][32][4]  - for column n (tile n/32, lane n mod 32) and k
- *              (block k/32, word (k mod 32)/8), q[k][n] sits in nibble position
- *              p = 0,4,1,5,2,6,3,7 for k mod 8 = 0..7. One 16-byte vector holds 32 consecutive
- *              k of one column; 32 lanes make 512 contiguous bytes per (tile, k-block).
- *   scales_r:  uint16 [N/32][K/group][32]  - scales_r[t][g][l] = scales[g][32t + l].
+ *   Columns are grouped in tiles of 128 (the last one w_t = N - 128t wide, t = n / 128).
+ *   qweight_r: tile t occupies bytes [64*t*K, 64*t*K + w_t*K/2), laid out [K/32][w_t] of
+ *              16-byte vectors; a vector holds 32 consecutive k of one column as 4 words of 8 k,
+ *              and inside a word q[k][n] sits in nibble position p = 0,4,1,5,2,6,3,7 for
+ *              k mod 8 = 0..7. One tile's rows k0..k0+KC are therefore one contiguous block.
+ *   scales_r:  tile t occupies elements [128*t*(K/group), ...), laid out [K/group][w_t].
  * In: qweight int32 [K/8][N], scales uint16 [K/group][N] (device). Out: qweight_r
  * (w4a16_repacked_qweight_bytes), scales_r (w4a16_repacked_scales_bytes) (device, caller
  * allocated, must not overlap the inputs). Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED,

@@ -183,12 +183,12 @@ class Oracle:
 
     # ---------------------------------------------------------------------------- layout
     def repack(self, qweight, scales, group: int):
-        """(wr uint32 [N/32, K/32, 32, 4], sr uint16 [N/32, K/G, 32]): the device layout."""
+        """(wr uint32 [N*K/8], sr uint16 [N*K/G]): the device layout (flat; see w4a16_oracle.c)."""
         qw = _c(qweight, np.int32)
         sc = _c(scales, np.uint16)
         K, N = qw.shape[0] * 8, qw.shape[1]
-        wr = np.empty((N // 32, K // 32, 32, 4), np.uint32)
-        sr = np.empty((N // 32, K // group, 32), np.uint16)
+        wr = np.empty(N * K // 8, np.uint32)
+        sr = np.empty(N * (K // group), np.uint16)
         rc = self.lib.w4o_repack(_ptr(qw), _ptr(sc), K, N, group, _ptr(wr), _ptr(sr))
         if rc != 0:
             raise ValueError(f"oracle repack rejected the shape (rc={rc})")

@@ -231,18 +231,36 @@ int w4o_gemm_sampled(const uint16_t* x, const int32_t* qweight, const uint16_t* 
 /* ---------------------------------------------------------------- the device layout
  *
  * The one-time re-layout the GPU path streams from (a bijection of the canonical bytes). This is
- * the library's own format, stated here independently of the CUDA code:
+ * the library's own format, stated here independently of the CUDA code.
  *
- *   weights: uint32 Wr[N/32][K/32][32][4]. For column n (tile t = n/32, lane l = n mod 32) and
- *            k (block b = k/32, word w = (k mod 32)/8, j = k mod 8), q[k][n] sits in nibble
- *            position p of Wr[t][b][l][w], where p = 0,4,1,5,2,6,3,7 for j = 0..7
- *            (positions 0..3 hold the even k of the word, positions 4..7 the odd k).
- *   scales:  uint16 Sr[N/32][K/G][32], Sr[t][g][l] = scales[g][32t + l].
+ * Columns are grouped in tiles of 128: tile t holds columns [128t, 128t + w_t) with
+ * w_t = min(128, N - 128t) (N is a multiple of 32, so w_t is 32, 64, 96 or 128).
+ *
+ *   weights: tile t occupies the 4-byte words [16t*K, 16t*K + w_t*K/8) (a column holds K/8
+ *            words; all earlier tiles are full). Inside it, column n (c = n - 128t) and k
+ *            (block b = k/32, word w = (k mod 32)/8, j = k mod 8) address the word
+ *            16t*K + (b*w_t + c)*4 + w, and q[k][n] sits in nibble position p of that word with
+ *            p = 0,4,1,5,2,6,3,7 for j = 0..7 (positions 0..3 hold the even k, 4..7 the odd k).
+ *   scales:  tile t occupies the elements [128t*(K/G), ...), laid out [K/G][w_t]:
+ *            scales[g][n] sits at 128t*(K/G) + g*w_t + c.
  */
 static const int kPosOfJ[8] = {0, 4, 1, 5, 2, 6, 3, 7};
 
 static int layout_ok(int N, int K, int G) {
     return N > 0 && K > 0 && G > 0 && N % 32 == 0 && K % 32 == 0 && K % G == 0 && G % 8 == 0;
+}
+
+static size_t weight_word_index(int K, int N, int k, int n) {
+    int t = n / 128, c = n % 128;
+    int wt = N - 128 * t < 128 ? N - 128 * t : 128;
+    int b = k / 32, w = (k % 32) / 8;
+    return (size_t)16 * t * K + ((size_t)b * wt + c) * 4 + w;
+}
+
+static size_t scale_index(int K, int N, int G, int g, int n) {
+    int t = n / 128, c = n % 128;
+    int wt = N - 128 * t < 128 ? N - 128 * t : 128;
+    return (size_t)128 * t * (K / G) + (size_t)g * wt + c;
 }
 
 int w4o_repack(const int32_t* qweight, const uint16_t* scales, int K, int N, int G, uint32_t* wr, uint16_t* sr) {
@@ -252,16 +270,11 @@ int w4o_repack(const int32_t* qweight, const uint16_t* scales, int K, int N, int
     for (int k = 0; k < K; ++k) {
         for (int n = 0; n < N; ++n) {
             uint32_t q = (uint32_t)w4o_nibble(qweight, N, k, n);
-            int t = n / 32, l = n % 32, b = k / 32, w = (k % 32) / 8, j = k % 8;
-            size_t idx = (((size_t)t * (K / 32) + b) * 32 + l) * 4 + w;
-            wr[idx] |= q << (4 * kPosOfJ[j]);
+            wr[weight_word_index(K, N, k, n)] |= q << (4 * kPosOfJ[k % 8]);
         }
     }
     for (int g = 0; g < K / G; ++g)
-        for (int n = 0; n < N; ++n) {
-            int t = n / 32, l = n % 32;
-            sr[((size_t)t * (K / G) + g) * 32 + l] = scales[(size_t)g * N + n];
-        }
+        for (int n = 0; n < N; ++n) sr[scale_index(K, N, G, g, n)] = scales[(size_t)g * N + n];
     return 0;
 }
 
@@ -271,18 +284,13 @@ int w4o_unrepack(const uint32_t* wr, const uint16_t* sr, int K, int N, int G, in
     memset(qweight, 0, nwords * sizeof(int32_t));
     for (int k = 0; k < K; ++k) {
         for (int n = 0; n < N; ++n) {
-            int t = n / 32, l = n % 32, b = k / 32, w = (k % 32) / 8, j = k % 8;
-            size_t idx = (((size_t)t * (K / 32) + b) * 32 + l) * 4 + w;
-            uint32_t q = (wr[idx] >> (4 * kPosOfJ[j])) & 0xFu;
+            uint32_t q = (wr[weight_word_index(K, N, k, n)] >> (4 * kPosOfJ[k % 8])) & 0xFu;
             uint32_t* dst = (uint32_t*)&qweight[(size_t)(k / 8) * N + n];
             *dst |= q << (4 * (k % 8));
         }
     }
     for (int g = 0; g < K / G; ++g)
-        for (int n = 0; n < N; ++n) {
-            int t = n / 32, l = n % 32;
-            scales[(size_t)g * N + n] = sr[((size_t)t * (K / G) + g) * 32 + l];
-        }
+        for (int n = 0; n < N; ++n) scales[(size_t)g * N + n] = sr[scale_index(K, N, G, g, n)];
     return 0;
 }
 

@@ -95,7 +95,8 @@ def test_plan_for_host_only(W):
         p = W.w4a16_plan_for(M, 34816, 5120, 128)
         if p.path == W.PATH_TC:
             assert p.m_tile in (16, 32, 64, 128, 256) and p.m_tile >= min(M, 16)
-            assert p.k_chunk in (64, 128) and 2 <= p.stages <= 8 and 1 <= p.split_k <= 16
+            assert p.k_chunk in (64, 128, 256) and 2 <= p.stages <= 16 and 1 <= p.split_k <= 16
+            assert 2 <= p.tmem_stages <= 8
     with pytest.raises(W.W4A16Error):
         W.w4a16_plan_for(0, 5120, 5120, 128)
 

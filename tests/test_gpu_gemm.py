@@ -91,19 +91,31 @@ def test_edge_rows_gemv(W, edge_matrix, M):
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
-TC_TILES = [(mt, kc) for mt in (16, 32, 64, 128, 256) for kc in (64, 128)]
+TC_TILES = [(16, 64), (16, 128), (16, 256), (32, 64), (32, 128), (32, 256), (64, 64), (64, 128), (64, 256),
+            (128, 64), (128, 128), (256, 64), (256, 128)]
 
 
 @pytest.mark.parametrize("mt,kc", TC_TILES)
 def test_every_tc_tile(W, mt, kc):
-    M, K, N, G = mt - 3, 1024, 256, 128
+    M, K, N, G = mt - 3, 1024, 352, 128  # ragged last column tile (96 wide)
     d, y_ref, abs_ref = _case(M, K, N, G, seed=mt + kc)
     x, qw_r, sc_r = _repacked(W, d, G)
     for split in (1, 3):
-        stages = 4 if kc == 64 else 3
-        if stages * kc // 2 + mt > 512:
-            stages = 2
-        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=mt, k_chunk=kc, stages=stages, split_k=split))
+        for ts in (2, 3):
+            if ts * kc // 2 + mt > 512:
+                continue
+            plan = dict(path=2, m_tile=mt, k_chunk=kc, split_k=split, tmem_stages=ts)
+            y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+            assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+def test_shallow_and_deep_rings(W):
+    M, K, N, G = 16, 2048, 256, 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=31)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    for (kc, st, ts) in [(64, 2, 2), (64, 16, 8), (128, 2, 2), (128, 7, 3), (256, 2, 2), (256, 5, 2)]:
+        plan = dict(path=2, m_tile=16, k_chunk=kc, stages=st, tmem_stages=ts, split_k=1)
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
@@ -112,7 +124,8 @@ def test_group_sizes(W, G):
     M, K, N = 5, 1024, 128
     d, y_ref, abs_ref = _case(M, K, N, G, seed=G)
     x, qw_r, sc_r = _repacked(W, d, G)
-    plans = [dict(path=1), dict(path=2, k_chunk=64, stages=4), dict(path=2, k_chunk=128, stages=3, split_k=2)]
+    plans = [dict(path=1), dict(path=2, k_chunk=64, stages=4), dict(path=2, k_chunk=128, stages=3, split_k=2),
+             dict(path=2, k_chunk=256, split_k=2)]
     for plan in plans:
         y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())

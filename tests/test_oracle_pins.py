@@ -264,26 +264,31 @@ def pin_threads_deterministic(o):
 
 
 def pin_repack_positions(o):
-    """Single-nibble matrices land where the layout statement says (p = 0,4,1,5,2,6,3,7)."""
-    K, N, G = 96, 64, 32
+    """Single-nibble matrices land where the layout statement says: 128-column tiles (the last
+    one w_t = N - 128t wide), word 16t*K + (b*w_t + c)*4 + w, nibble p = 0,4,1,5,2,6,3,7."""
+    K, N, G = 96, 224, 32  # tiles of 128 and 96 columns
     pos_of_j = [0, 4, 1, 5, 2, 6, 3, 7]
-    for (k, n) in [(0, 0), (1, 0), (2, 5), (7, 31), (8, 32), (33, 1), (95, 63), (61, 40)]:
+    for (k, n) in [(0, 0), (1, 0), (2, 5), (7, 31), (8, 32), (33, 1), (95, 127), (61, 40), (0, 128), (95, 223),
+                   (37, 150)]:
         q = np.zeros((K, N), np.uint8)
         q[k, n] = 0xA
         wr, _ = o.repack(inputs.pack_nibbles(q), np.zeros((K // G, N), np.uint16), G)
-        flat = wr.reshape(-1)
-        idx = (((n // 32) * (K // 32) + k // 32) * 32 + n % 32) * 4 + (k % 32) // 8
-        assert np.count_nonzero(flat) == 1
-        assert flat[idx] == np.uint32(0xA << (4 * pos_of_j[k % 8]))
+        t, c = n // 128, n % 128
+        wt = min(128, N - 128 * t)
+        idx = 16 * t * K + ((k // 32) * wt + c) * 4 + (k % 32) // 8
+        assert np.count_nonzero(wr) == 1
+        assert wr[idx] == np.uint32(0xA << (4 * pos_of_j[k % 8]))
     sc = np.arange(K // G * N, dtype=np.uint16).reshape(K // G, N)
     _, sr = o.repack(np.zeros((K // 8, N), np.int32), sc, G)
-    for (g, n) in [(0, 0), (1, 33), (2, 63)]:
-        assert sr[n // 32, g, n % 32] == sc[g, n]
+    for (g, n) in [(0, 0), (1, 33), (2, 127), (0, 128), (2, 223)]:
+        t, c = n // 128, n % 128
+        wt = min(128, N - 128 * t)
+        assert sr[128 * t * (K // G) + g * wt + c] == sc[g, n]
 
 
 def pin_repack_roundtrip(o):
     rng = np.random.default_rng(RNG_SEED + 9)
-    K, N, G = 256, 96, 64
+    K, N, G = 256, 352, 64
     words = rng.integers(0, 2 ** 32, size=(K // 8, N), dtype=np.uint64).astype(np.uint32).view(np.int32)
     sc = rng.integers(0, 2 ** 16, size=(K // G, N), dtype=np.uint32).astype(np.uint16)
     wr, sr = o.repack(words, sc, G)
@@ -319,6 +324,7 @@ MUTANTS = {
     "shifted_x_row": ("column_dot(x + (size_t)m * K,", "column_dot(x + (size_t)m,"),
     "abs_not_abs": ("aacc += fabs(p);", "aacc += p;"),
     "layout_positions": ("kPosOfJ[8] = {0, 4, 1, 5, 2, 6, 3, 7};", "kPosOfJ[8] = {0, 1, 2, 3, 4, 5, 6, 7};"),
+    "layout_transposed_tile": ("((size_t)b * wt + c) * 4 + w;", "((size_t)c * (K / 32) + b) * 4 + w;"),
 }
 
 

@@ -82,6 +82,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Warp-wide wait: lane 0 polls (so a warp puts one poller, not 32, on the barrier), the warp
+// reconverges, then every lane performs its own (now immediate) acquiring test of the phase.
+// Returns the same verdict in all lanes. Must be called by all 32 lanes.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t timeout_ns, unsigned* status) {
+    int ok = 1;
+    if ((threadIdx.x & 31u) == 0u) ok = mbar_wait(bar, parity, abort_flag, timeout_ns, status) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
 // ------------------------------------------------------------------------------------ TMA
 // 1-D bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.

@@ -1,7 +1,8 @@
 // CUDA-core split-K GEMV for the smallest decode batches (M <= 8).
 //
-// One CTA = 4 warps on one 32-column tile of W and one K-slice. Lane l owns column 32t + l and
-// streams its 16-byte vectors (32 k each); the 4 warps interleave over the K-slice's 32-k blocks
+// One CTA = 4 warps on one 32-column slice of W and one K-slice. Lane l owns one column and
+// streams its 16-byte vectors (32 k each, 512 contiguous bytes per warp per 32-k block in the
+// 128-column-tile layout); the 4 warps interleave over the K-slice's 32-k blocks
 // and combine through shared memory. The K-slices of one column tile form a thread-block
 // cluster and are summed through distributed shared memory, in a fixed rank order, by the CTA
 // that owns each output element. Activations of the K-slice are staged once in shared memory as
@@ -74,7 +75,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     const int KB = K / 32;
     const int NG = K / G;
     const int rank = blockIdx.x;
-    const int t = blockIdx.y;
+    const int t = blockIdx.y;           // 32-column slice: columns 32t .. 32t + 31
+    const int tile = t / 4;             // 128-column tile of the streaming layout
+    const int wt = min(128, N - 128 * tile);
+    const int cofs = 32 * (t % 4);      // slice offset inside the tile
     const GemvSlice sl = slice_of(rank, split, KB);
     const int klen_max = ((KB + split - 1) / split) * 32;
 
@@ -102,8 +106,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 #pragma unroll
         for (int m = 0; m < MR; ++m) acc[c][m][0] = acc[c][m][1] = 0.f;
 
-    const uint4* wcol = wr + static_cast<int64_t>(t) * KB * 32 + lane;  // + kb * 32
-    const uint16_t* scol = sr + static_cast<int64_t>(t) * NG * 32 + lane;  // + g * 32
+    const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;      // + kb * wt
+    const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;  // + g * wt
 
     int kb = sl.kb_begin + warp;
     for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
@@ -112,8 +116,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int b = kb + kWarps * u;
-            v[u] = ldg_stream(wcol + static_cast<int64_t>(b) * 32);
-            sb[u] = ldg_u16(scol + static_cast<int64_t>((b * 32) / G) * 32);
+            v[u] = ldg_stream(wcol + static_cast<int64_t>(b) * wt);
+            sb[u] = ldg_u16(scol + static_cast<int64_t>((b * 32) / G) * wt);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -122,8 +126,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         }
     }
     for (; kb < sl.kb_end; kb += kWarps) {
-        const uint4 v = ldg_stream(wcol + static_cast<int64_t>(kb) * 32);
-        const uint16_t sb = ldg_u16(scol + static_cast<int64_t>((kb * 32) / G) * 32);
+        const uint4 v = ldg_stream(wcol + static_cast<int64_t>(kb) * wt);
+        const uint16_t sb = ldg_u16(scol + static_cast<int64_t>((kb * 32) / G) * wt);
         gemv_block<MR>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
     }
 

@@ -30,10 +30,11 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint
 
 // ---- tc_gemm.cu: tcgen05 tensor-core path.
 struct TcConfig {
-    int m_tile;   // 16, 32, 64, 128, 256
-    int k_chunk;  // 64 or 128
-    int stages;   // 2..8
-    int split;    // CTAs per cluster along K, 1..16
+    int m_tile;       // 16, 32, 64, 128, 256
+    int k_chunk;      // K per stage: 64, 128 or 256
+    int stages;       // shared-memory ring depth, 2..16
+    int split;        // CTAs per cluster along K, 1..16
+    int tmem_stages;  // TMEM A ring depth, 2..8
 };
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G);
 size_t tc_smem_bytes(const TcConfig& c, int G);

@@ -29,62 +29,57 @@ __device__ __forceinline__ uint32_t deinterleave_word(uint32_t w) {
     return out;
 }
 
-// One thread per 16-byte output vector (tile t, k-block b, lane l): reads the four canonical
-// words qweight[4b + i][32t + l] (consecutive l -> consecutive addresses) and writes the vector.
+// Tile geometry of the streaming layout: 128-column tiles, the last one w_t = N - 128t wide.
+__device__ __forceinline__ int tile_width(int N, int t) { return min(128, N - 128 * t); }
+
+// One thread per 16-byte vector (k-block b, column n), v = b * N + n: reads the four canonical
+// words qweight[4b + i][n] (consecutive n -> consecutive addresses) and writes the vector at
+// tile t = n / 128, position b * w_t + (n - 128t) of that tile's [K/32][w_t] block.
 __global__ void repack_weights_kernel(const uint32_t* __restrict__ qw, uint4* __restrict__ out, int N, int K) {
     const int64_t total = static_cast<int64_t>(N) * (K / 32);
-    const int KB = K / 32;
     for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
          v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int l = static_cast<int>(v % 32);
-        const int64_t tb = v / 32;
-        const int b = static_cast<int>(tb % KB);
-        const int t = static_cast<int>(tb / KB);
-        const int n = 32 * t + l;
+        const int n = static_cast<int>(v % N);
+        const int b = static_cast<int>(v / N);
+        const int t = n / 128;
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) w[i] = interleave_word(qw[static_cast<int64_t>(4 * b + i) * N + n]);
-        out[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        out[static_cast<int64_t>(t) * 128 * (K / 32) + static_cast<int64_t>(b) * tile_width(N, t) + (n - 128 * t)] =
+            make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 __global__ void unrepack_weights_kernel(const uint4* __restrict__ in, uint32_t* __restrict__ qw, int N, int K) {
     const int64_t total = static_cast<int64_t>(N) * (K / 32);
-    const int KB = K / 32;
     for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
          v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int l = static_cast<int>(v % 32);
-        const int64_t tb = v / 32;
-        const int b = static_cast<int>(tb % KB);
-        const int t = static_cast<int>(tb / KB);
-        const int n = 32 * t + l;
-        const uint4 x = in[v];
+        const int n = static_cast<int>(v % N);
+        const int b = static_cast<int>(v / N);
+        const int t = n / 128;
+        const uint4 x =
+            in[static_cast<int64_t>(t) * 128 * (K / 32) + static_cast<int64_t>(b) * tile_width(N, t) + (n - 128 * t)];
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) qw[static_cast<int64_t>(4 * b + i) * N + n] = deinterleave_word(w[i]);
     }
 }
 
-// scales [K/G][N] <-> scales_r [N/32][K/G][32]; one thread per element, indexed by the
-// canonical position when `to_tiles`, by the tiled position otherwise (so writes coalesce).
+// scales [K/G][N] <-> scales_r (tile t: [K/G][w_t] at element 128t * K/G); one thread per
+// canonical element i = g * N + n.
 __global__ void scales_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int N, int NG,
                               bool to_tiles) {
     const int64_t total = static_cast<int64_t>(N) * NG;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        if (to_tiles) {
-            // i = (t * NG + g) * 32 + l  (output order)
-            const int l = static_cast<int>(i % 32);
-            const int64_t tg = i / 32;
-            const int g = static_cast<int>(tg % NG);
-            const int t = static_cast<int>(tg / NG);
-            out[i] = in[static_cast<int64_t>(g) * N + 32 * t + l];
-        } else {
-            // i = g * N + n  (output order)
-            const int n = static_cast<int>(i % N);
-            const int g = static_cast<int>(i / N);
-            out[i] = in[(static_cast<int64_t>(n / 32) * NG + g) * 32 + (n % 32)];
-        }
+        const int n = static_cast<int>(i % N);
+        const int g = static_cast<int>(i / N);
+        const int t = n / 128;
+        const int64_t tiled = static_cast<int64_t>(t) * 128 * NG + static_cast<int64_t>(g) * tile_width(N, t) + (n - 128 * t);
+        if (to_tiles)
+            out[tiled] = in[i];
+        else
+            out[i] = in[tiled];
     }
 }
 

@@ -6,27 +6,31 @@
 //
 // A never touches shared memory in fp16: dequantisation warps read the packed nibbles that TMA
 // streamed into shared memory, dequantise in registers (exact fp16, common.cuh) and write the
-// fp16 pairs straight into TMEM with tcgen05.st; the MMA reads A from TMEM ("A in tensor memory"
-// form of tcgen05.mma). Shared memory therefore carries 0.5 B per weight instead of 2.
+// fp16 pairs straight into TMEM with tcgen05.st; the MMA reads A from TMEM (the "A in tensor
+// memory" form of tcgen05.mma). Shared memory carries 0.5 B per weight instead of 2.
+//
+// Two rings:
+//   shared-memory stages (s_stages): per stage ONE bulk copy of the 128-column tile's packed
+//     weights for KC rows of K (contiguous in the streaming layout), ONE bulk copy of its scales,
+//     ONE 3-D tensor copy of the x tile (KC/64 blocks of 64 k x MT rows, 128-byte swizzle, rows
+//     beyond M zero-filled). Three copy instructions per stage keep the single producer thread
+//     far from its issue limit.
+//   TMEM A stages (a_stages): KC/2 columns each (fp16 pairs).
 //
 // Warp roles (320 threads):
-//   warps 0-7  dequantise (warp w owns TMEM lanes 32*(w%4).., i.e. column sub-tile w%4, and
-//              half w/4 of every stage's 32-k blocks), then run the epilogue;
-//   warp 8     TMA producer: per stage, 1-D bulk copies of the packed weights and scales of the
-//              4 column sub-tiles (L2 evict-first) and 2-D tensor copies of the x tile
-//              (128-byte swizzle, rows beyond M zero-filled);
-//   warp 9     allocates TMEM and issues tcgen05.mma from one thread.
-// Pipeline: full[s] (TMA bytes landed) -> afull[s] (A stage written to TMEM) -> MMA ->
-// tcgen05.commit -> empty[s] (shared stage and TMEM A stage free) -> producer refills.
-// Every wait is bounded (common.cuh: mbar_wait).
+//   warps 0-7  dequantise. Warp w owns TMEM lanes 32*(w%4).. (column slice w%4) and belongs to
+//              group w/4; the two groups take alternate stages, so two stages are in
+//              dequantisation at once. Then both groups run the epilogue.
+//   warp 8     TMA producer (one thread).
+//   warp 9     allocates TMEM and issues tcgen05.mma (one thread).
+// Barriers: full[s] (TMA bytes landed) -> afull[a] (A stage written) -> MMA -> tcgen05.commit ->
+// empty[s] (shared stage free) and aempty[a] (TMEM A stage free). Every wait is bounded.
 //
 // Split-K: the `split` CTAs of a thread-block cluster cover disjoint K ranges of the same
 // 128 x MT output tile; after the mainloop each CTA writes its fp32 partial tile to shared
 // memory and the cluster sums them through distributed shared memory in rank order, each CTA
 // finishing 1/split of the tile. No global scratch memory is used.
 #include <cudaTypedefs.h>
-
-#include <cstdio>
 
 #include "common.cuh"
 #include "internal.h"
@@ -35,90 +39,102 @@ namespace w4a16 {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kDequantWarps = 8;
+constexpr int kGroupWarps = 4;  // dequant warps per group (one per TMEM lane quadrant)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTileN = 128;  // output columns per CTA (= TMEM lanes)
 
 struct SmemPlan {
-    uint32_t x_off, x_stage;  // x tiles: stages x (MT * KC * 2)
-    uint32_t w_off, w_stage;  // packed weights: stages x (4 * KC/32 * 512)
-    uint32_t s_off, s_stage;  // scales: stages x (4 * ngs * 64)
+    uint32_t x_off, x_stage;  // x tiles: s_stages x (MT * KC * 2)
+    uint32_t w_off, w_stage;  // packed weights: s_stages x (128 * KC / 2)
+    uint32_t s_off, s_stage;  // scales: s_stages x (ngs * 128 * 2)
     uint32_t red_off;         // split-K partial tile, MT * 128 * 4 (may overlap the x tiles)
-    uint32_t bar_off;         // 3 * stages + 1 mbarriers
+    uint32_t bar_off;         // 2 * s_stages + 2 * a_stages + 1 mbarriers
     uint32_t misc_off;        // tmem address slot, abort flag
     uint32_t total;           // bytes from the 1024-aligned base
 };
 
 __host__ __device__ inline int groups_per_stage(int KC, int G) { return KC >= G ? KC / G : 1; }
 
-__host__ __device__ inline SmemPlan make_plan(int MT, int KC, int stages, int G, int split) {
+__host__ __device__ inline SmemPlan make_plan(int MT, int KC, int s_stages, int a_stages, int G, int split) {
     SmemPlan p;
     p.x_stage = static_cast<uint32_t>(MT * KC * 2);
-    p.w_stage = static_cast<uint32_t>(4 * (KC / 32) * 512);
-    p.s_stage = static_cast<uint32_t>(4 * groups_per_stage(KC, G) * 64);
+    p.w_stage = static_cast<uint32_t>(kTileN * KC / 2);
+    p.s_stage = static_cast<uint32_t>(groups_per_stage(KC, G) * kTileN * 2);
     p.x_off = 0;
-    p.w_off = p.x_off + stages * p.x_stage;
-    p.s_off = p.w_off + stages * p.w_stage;
-    uint32_t end = p.s_off + stages * p.s_stage;
+    p.w_off = p.x_off + s_stages * p.x_stage;
+    p.s_off = p.w_off + s_stages * p.w_stage;
+    uint32_t end = p.s_off + s_stages * p.s_stage;
     const uint32_t red_bytes = static_cast<uint32_t>(MT * kTileN * 4);
-    if (split > 1 && red_bytes > stages * p.x_stage) {
+    if (split > 1 && red_bytes > s_stages * p.x_stage) {
         p.red_off = (end + 15u) & ~15u;
         end = p.red_off + red_bytes;
     } else {
         p.red_off = 0;
     }
     p.bar_off = (end + 7u) & ~7u;
-    p.misc_off = p.bar_off + (3 * stages + 1) * 8;
+    p.misc_off = p.bar_off + (2 * s_stages + 2 * a_stages + 1) * 8;
     p.total = p.misc_off + 16;
     return p;
 }
 
-__host__ __device__ inline int tmem_cols_needed(int MT, int KC, int stages) { return stages * (KC / 2) + MT; }
+__host__ __device__ inline int tmem_cols_needed(int MT, int KC, int a_stages) { return a_stages * (KC / 2) + MT; }
 
-__host__ __device__ inline uint32_t tmem_alloc_cols(int MT, int KC, int stages) {
-    const int need = tmem_cols_needed(MT, KC, stages);
+__host__ __device__ inline uint32_t tmem_alloc_cols(int MT, int KC, int a_stages) {
+    const int need = tmem_cols_needed(MT, KC, a_stages);
     uint32_t c = 32;
     while (static_cast<int>(c) < need) c <<= 1;
     return c;
+}
+
+template <int KC>
+__device__ __forceinline__ void tma_load_x(uint32_t dst, const void* tmap, int k0, int m0, uint32_t bar, bool three_d) {
+    if (three_d) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+                dst),
+            "l"(tmap), "r"(0), "r"(m0), "r"(k0 / 64), "r"(bar)
+            : "memory");
+    }
 }
 
 template <int MT, int KC, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
-                   int stages, unsigned* status, uint64_t timeout_ns) {
+                   int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
-    static_assert(KC == 64 || KC == 128, "stage K must be 64 or 128");
-    constexpr int kKB = KC / 32;      // 32-k blocks per stage
-    constexpr int kHalfKB = kKB / 2;  // blocks per dequant half
-    constexpr int kACols = KC / 2;    // TMEM columns of one A stage (fp16 pairs)
+    static_assert(KC == 64 || KC == 128 || KC == 256, "stage K must be 64, 128 or 256");
+    constexpr int kKB = KC / 32;    // 32-k blocks per stage
+    constexpr int kACols = KC / 2;  // TMEM columns of one A stage (fp16 pairs)
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     const int split = gridDim.x;
-    const SmemPlan P = make_plan(MT, KC, stages, G, split);
+    const SmemPlan P = make_plan(MT, KC, s_stages, a_stages, G, split);
     const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);
     const uint32_t bar0 = sbase + P.bar_off;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto afull_bar = [&](int s) { return bar0 + 8u * (stages + s); };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * stages + s); };
-    const uint32_t dfull_bar = bar0 + 8u * (3 * stages);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (s_stages + s); };
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a_stages + a); };
+    const uint32_t dfull_bar = bar0 + 8u * (2 * s_stages + 2 * a_stages);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.misc_off + 4);
-    (void)bars;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t ncols = tmem_alloc_cols(MT, KC, stages);
+    const uint32_t ncols = tmem_alloc_cols(MT, KC, a_stages);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < s_stages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(afull_bar(s), kDequantWarps * 32);
             mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < a_stages; ++a) {
+            mbar_init(afull_bar(a), kGroupWarps);  // one elected arrival per warp of the group
+            mbar_init(aempty_bar(a), 1);
         }
         mbar_init(dfull_bar, 1);
         *abort_flag = 0;
@@ -133,12 +149,12 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t d_tmem = tmem + static_cast<uint32_t>(stages * kACols);
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(a_stages * kACols);
 
     const int rank = blockIdx.x;
-    const int n0 = blockIdx.y * kTileN;
-    const int t0 = n0 / 32;
-    const int nsub = min(4, N / 32 - t0);
+    const int tile = blockIdx.y;
+    const int n0 = tile * kTileN;
+    const int wt = min(kTileN, N - n0);  // columns of this tile (32, 64, 96 or 128)
     const int m0 = blockIdx.z * MT;
     const int KB = K / 32;
     const int NG = K / G;
@@ -147,35 +163,40 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
     const int c_begin = static_cast<int>((static_cast<int64_t>(rank) * C) / split);
     const int c_end = static_cast<int>((static_cast<int64_t>(rank + 1) * C) / split);
     const int niter = c_end - c_begin;
+    const uint4* w_tile = wr + static_cast<int64_t>(tile) * kTileN * KB;       // [K/32][wt] vectors
+    const uint16_t* s_tile = sr + static_cast<int64_t>(tile) * kTileN * NG;    // [K/G][wt]
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            const uint32_t bytes = static_cast<uint32_t>(nsub * (kKB * 512 + ngs * 64) + (KC / 64) * MT * 128);
+            const uint32_t wbytes = static_cast<uint32_t>(kKB * wt * 16);
+            const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
+            const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
             int issued = 0;
             for (int i = 0; i < niter; ++i) {
-                const int s = i % stages;
-                const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
-                if (i >= stages && !mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, timeout_ns, status)) break;
+                const int s = i % s_stages;
+                if (i >= s_stages &&
+                    !mbar_wait(empty_bar(s), static_cast<uint32_t>(i / s_stages - 1) & 1u, abort_flag, timeout_ns,
+                               status))
+                    break;
                 const int k0 = (c_begin + i) * KC;
-                const int g0 = k0 / G;
-                mbar_arrive_expect_tx(full_bar(s), bytes);
-                for (int q = 0; q < nsub; ++q) {
-                    bulk_g2s(sbase + P.w_off + s * P.w_stage + q * kKB * 512,
-                             wr + (static_cast<int64_t>(t0 + q) * KB + k0 / 32) * 32, kKB * 512, full_bar(s), pol);
-                    bulk_g2s(sbase + P.s_off + s * P.s_stage + q * ngs * 64,
-                             sr + (static_cast<int64_t>(t0 + q) * NG + g0) * 32, ngs * 64, full_bar(s), pol);
-                }
+                const uint32_t fb = full_bar(s);
+                mbar_arrive_expect_tx(fb, bytes);
+                bulk_g2s(sbase + P.w_off + s * P.w_stage, w_tile + static_cast<int64_t>(k0 / 32) * wt, wbytes, fb, pol);
+                bulk_g2s(sbase + P.s_off + s * P.s_stage, s_tile + static_cast<int64_t>(k0 / G) * wt, sbytes, fb, pol);
+                const uint32_t xs = sbase + P.x_off + s * P.x_stage;
+                if (x_3d) {
+                    tma_load_x<KC>(xs, &tmap_x, k0, m0, fb, true);
+                } else {
 #pragma unroll
-                for (int a = 0; a < KC / 64; ++a)
-                    tma_load_2d(sbase + P.x_off + s * P.x_stage + a * MT * 128, &tmap_x, k0 + 64 * a, m0,
-                                full_bar(s));
+                    for (int a = 0; a < KC / 64; ++a) tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, fb);
+                }
                 issued = i + 1;
             }
             // Let the copies still in flight land before shared memory can be released.
             int dummy_abort = 0;
-            for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
-                mbar_wait(full_bar(i % stages), static_cast<uint32_t>(i / stages) & 1u, &dummy_abort, timeout_ns,
+            for (int i = issued > s_stages ? issued - s_stages : 0; i < issued; ++i)
+                mbar_wait(full_bar(i % s_stages), static_cast<uint32_t>(i / s_stages) & 1u, &dummy_abort, timeout_ns,
                           status);
         }
         __syncwarp();
@@ -183,12 +204,14 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, MT);
             for (int i = 0; i < niter; ++i) {
-                const int s = i % stages;
-                const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
-                if (!mbar_wait(afull_bar(s), ph, abort_flag, timeout_ns, status)) break;
-                if (!mbar_wait(full_bar(s), ph, abort_flag, timeout_ns, status)) break;
+                const int s = i % s_stages;
+                const int a = i % a_stages;
+                if (!mbar_wait(afull_bar(a), static_cast<uint32_t>(i / a_stages) & 1u, abort_flag, timeout_ns, status))
+                    break;
+                if (!mbar_wait(full_bar(s), static_cast<uint32_t>(i / s_stages) & 1u, abort_flag, timeout_ns, status))
+                    break;
                 tc_fence_after();
-                const uint32_t a_tmem = tmem + static_cast<uint32_t>(s * kACols);
+                const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
                 const uint32_t x_stage = sbase + P.x_off + s * P.x_stage;
 #pragma unroll
                 for (int kk = 0; kk < KC / 16; ++kk) {
@@ -196,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
                     umma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (i > 0) || (kk > 0));
                 }
                 umma_commit(empty_bar(s));
+                umma_commit(aempty_bar(a));
             }
             umma_commit(dfull_bar);
         }
@@ -203,48 +227,57 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
     } else {
         // ---------------- dequantisation warps
         const int q = warp & 3;
-        const int h = warp >> 2;
-        const bool valid = q < nsub;
+        const int grp = warp >> 2;
+        const bool valid = 32 * q < wt;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        for (int i = 0; i < niter; ++i) {
-            const int s = i % stages;
-            const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
-            if (!mbar_wait(full_bar(s), ph, abort_flag, timeout_ns, status)) break;
+        for (int i = grp; i < niter; i += 2) {
+            const int s = i % s_stages;
+            const int a = i % a_stages;
+            if (!warp_wait(full_bar(s), static_cast<uint32_t>(i / s_stages) & 1u, abort_flag, timeout_ns, status))
+                break;
+            if (i >= a_stages &&
+                !warp_wait(aempty_bar(a), static_cast<uint32_t>(i / a_stages - 1) & 1u, abort_flag, timeout_ns, status))
+                break;
             if (valid) {
                 const int k0 = (c_begin + i) * KC;
                 const int g0 = k0 / G;
-                const uint4* wst = reinterpret_cast<const uint4*>(smem + P.w_off + s * P.w_stage) + q * kKB * 32;
-                const uint16_t* sst = reinterpret_cast<const uint16_t*>(smem + P.s_off + s * P.s_stage) + q * ngs * 32;
-                uint32_t regs[kHalfKB * 16];
+                const uint4* wst = reinterpret_cast<const uint4*>(smem + P.w_off + s * P.w_stage) + 32 * q + lane;
+                const uint16_t* sst = reinterpret_cast<const uint16_t*>(smem + P.s_off + s * P.s_stage) + 32 * q + lane;
+                const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(a * kACols);
 #pragma unroll
-                for (int bb = 0; bb < kHalfKB; ++bb) {
-                    const int b = h * kHalfKB + bb;
-                    const uint4 v = wst[b * 32 + lane];
-                    const uint32_t sb = sst[((k0 + 32 * b) / G - g0) * 32 + lane];
-                    const uint32_t s2 = sb | (sb << 16);
-                    dequant8(v.x, s2, &regs[bb * 16 + 0]);
-                    dequant8(v.y, s2, &regs[bb * 16 + 4]);
-                    dequant8(v.z, s2, &regs[bb * 16 + 8]);
-                    dequant8(v.w, s2, &regs[bb * 16 + 12]);
+                for (int bp = 0; bp < kKB; bp += 2) {
+                    uint32_t regs[32];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int b = bp + u;
+                        const uint4 v = wst[b * wt];
+                        const uint32_t sb = sst[((k0 + 32 * b) / G - g0) * wt];
+                        const uint32_t s2 = sb | (sb << 16);
+                        dequant8(v.x, s2, &regs[u * 16 + 0]);
+                        dequant8(v.y, s2, &regs[u * 16 + 4]);
+                        dequant8(v.z, s2, &regs[u * 16 + 8]);
+                        dequant8(v.w, s2, &regs[u * 16 + 12]);
+                    }
+                    tmem_st<32>(a_col + static_cast<uint32_t>(bp * 16), regs);
                 }
-                tmem_st<kHalfKB * 16>(tmem + lane_base + static_cast<uint32_t>(s * kACols + h * kHalfKB * 16), regs);
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(afull_bar(s));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull_bar(a));
         }
 
         // ---------------- epilogue: TMEM -> registers -> y (or the split-K partial tile)
-        const bool have_d = mbar_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
+        const bool have_d = warp_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
         tc_fence_after();
         if (have_d) {
-            const int mbase = h * (MT / 2);
+            const int mbase = grp * (MT / 2);
             float* red = reinterpret_cast<float*>(smem + P.red_off);
             const int n = n0 + 32 * q + lane;
 #pragma unroll 1
             for (int c = 0; c < MT / 2; c += 8) {
                 uint32_t r[8];
-                tmem_ld8(tmem + lane_base + static_cast<uint32_t>(stages * kACols + mbase + c), r);
+                tmem_ld8(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
                 tmem_wait_ld();
                 if (split == 1) {
                     if (valid) {
@@ -284,13 +317,13 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
             }
             const int e = 4 * e4;
             const int m = m0 + e / kTileN;
-            const int n = n0 + e % kTileN;
-            if (m < M && n < N) {
+            const int c = e % kTileN;
+            if (m < M && c < wt) {
                 const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
                                     (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
                 const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |
                                     (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.w))) << 16);
-                *reinterpret_cast<uint2*>(y + static_cast<int64_t>(m) * N + n) = make_uint2(lo, hi);
+                *reinterpret_cast<uint2*>(y + static_cast<int64_t>(m) * N + n0 + c) = make_uint2(lo, hi);
             }
         }
         __syncwarp();
@@ -319,15 +352,43 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// x viewed as [K/64 blocks][M rows][64 k] (strides 128 B and 2K B): one box = the whole stage
+// tile [KC/64][MT][64], laid out in shared memory exactly as the MMA's 128-byte-swizzle K-major
+// operand atoms expect. Falls back to a 2-D map ([M][K], box 64 x MT, KC/64 copies per stage)
+// if the driver refuses the 3-D one.
+bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int KC, bool* three_d) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    {
+        const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128u};
+        const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MT), static_cast<cuuint32_t>(KC / 64)};
+        if (encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            *three_d = true;
+            return true;
+        }
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(MT)};
+    *three_d = false;
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MT, int KC, int MIN_BLOCKS>
-cudaError_t launch_tc_t(const CUtensorMap& tmap, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
-                        int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
+cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
+                        uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
     auto kern = tc_gemm_kernel<MT, KC, MIN_BLOCKS>;
-    const SmemPlan P = make_plan(MT, KC, c.stages, G, c.split);
+    const SmemPlan P = make_plan(MT, KC, c.stages, c.tmem_stages, G, c.split);
     size_t smem = P.total + 1024;  // + alignment slack for the 1024-byte base
     // Keep the number of co-resident CTAs within what TMEM can hold, so that no CTA ever waits
     // in tcgen05.alloc for a CTA of another cluster.
-    const int per_sm_tmem = 512 / static_cast<int>(tmem_alloc_cols(MT, KC, c.stages));
+    const int per_sm_tmem = 512 / static_cast<int>(tmem_alloc_cols(MT, KC, c.tmem_stages));
     const size_t min_smem = 233472 / (per_sm_tmem + 1) - 1024 + 16;
     if (smem < min_smem) smem = min_smem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -349,7 +410,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, const uint32_t* qweight_r, cons
     cfg.attrs = attr;
     cfg.numAttrs = c.split > 1 ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
-                              c.stages, ctx.status, ctx.timeout_ns);
+                              c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
 }
 
 }  // namespace
@@ -358,48 +419,46 @@ bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
     (void)M;
     (void)N;
     if (c.m_tile != 16 && c.m_tile != 32 && c.m_tile != 64 && c.m_tile != 128 && c.m_tile != 256) return false;
-    if (c.k_chunk != 64 && c.k_chunk != 128) return false;
+    if (c.k_chunk != 64 && c.k_chunk != 128 && c.k_chunk != 256) return false;
     if (K % c.k_chunk != 0) return false;
-    if (c.stages < 2 || c.stages > 8) return false;
+    if (c.stages < 2 || c.stages > 16) return false;
+    if (c.tmem_stages < 2 || c.tmem_stages > 8) return false;
     if (c.split < 1 || c.split > 16 || c.split > K / c.k_chunk) return false;
-    if (tmem_cols_needed(c.m_tile, c.k_chunk, c.stages) > 512) return false;
+    if (tmem_cols_needed(c.m_tile, c.k_chunk, c.tmem_stages) > 512) return false;
     if (c.k_chunk < G && G % c.k_chunk != 0) return false;
     if (c.k_chunk >= G && c.k_chunk % G != 0) return false;
-    const SmemPlan P = make_plan(c.m_tile, c.k_chunk, c.stages, G, c.split);
+    const SmemPlan P = make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.split);
     if (P.total + 1024 > 232448) return false;
     return true;
 }
 
-size_t tc_smem_bytes(const TcConfig& c, int G) { return make_plan(c.m_tile, c.k_chunk, c.stages, G, c.split).total + 1024; }
+size_t tc_smem_bytes(const TcConfig& c, int G) {
+    return make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.split).total + 1024;
+}
 
-int tc_tmem_cols(const TcConfig& c) { return static_cast<int>(tmem_alloc_cols(c.m_tile, c.k_chunk, c.stages)); }
+int tc_tmem_cols(const TcConfig& c) { return static_cast<int>(tmem_alloc_cols(c.m_tile, c.k_chunk, c.tmem_stages)); }
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr) return cudaErrorNotSupported;
     CUtensorMap tmap;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(c.m_tile)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-#define W4A16_TC_CASE(MT_, KC_, MB_)                                                                     \
-    if (c.m_tile == MT_ && c.k_chunk == KC_)                                                             \
-        return launch_tc_t<MT_, KC_, MB_>(tmap, qweight_r, scales_r, y, M, N, K, G, c, ctx);
-    W4A16_TC_CASE(16, 128, 2)
+    bool three_d = false;
+    if (!encode_x_map(&tmap, x, M, K, c.m_tile, c.k_chunk, &three_d)) return cudaErrorInvalidValue;
+#define W4A16_TC_CASE(MT_, KC_, MB_)                                                                          \
+    if (c.m_tile == MT_ && c.k_chunk == KC_)                                                                  \
+        return launch_tc_t<MT_, KC_, MB_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
     W4A16_TC_CASE(16, 64, 2)
-    W4A16_TC_CASE(32, 128, 2)
+    W4A16_TC_CASE(16, 128, 2)
+    W4A16_TC_CASE(16, 256, 1)
     W4A16_TC_CASE(32, 64, 2)
-    W4A16_TC_CASE(64, 128, 2)
+    W4A16_TC_CASE(32, 128, 2)
+    W4A16_TC_CASE(32, 256, 1)
     W4A16_TC_CASE(64, 64, 2)
-    W4A16_TC_CASE(128, 128, 1)
+    W4A16_TC_CASE(64, 128, 2)
+    W4A16_TC_CASE(64, 256, 1)
     W4A16_TC_CASE(128, 64, 1)
-    W4A16_TC_CASE(256, 128, 1)
+    W4A16_TC_CASE(128, 128, 1)
     W4A16_TC_CASE(256, 64, 1)
+    W4A16_TC_CASE(256, 128, 1)
 #undef W4A16_TC_CASE
     return cudaErrorInvalidValue;
 }

@@ -95,18 +95,36 @@ int gemv_pick_split(int M, int N, int K, int sm_count) {
     return split;
 }
 
+bool group_fits(int KC, int G) { return KC >= G ? KC % G == 0 : G % KC == 0; }
+
+// Largest shared-memory ring that fits `budget` bytes for a tile shape.
+int fill_stages(const TcConfig& base, int G, size_t budget, int max_stages) {
+    TcConfig c = base;
+    int best = 2;
+    for (int s = 2; s <= max_stages; ++s) {
+        c.stages = s;
+        if (tc_smem_bytes(c, G) <= budget) best = s;
+    }
+    return best;
+}
+
 TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
     TcConfig c;
     c.m_tile = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-    c.k_chunk = (c.m_tile <= 64 && K % 128 == 0 && (128 % G == 0 || G % 128 == 0)) ? 128 : 64;
-    c.stages = c.m_tile <= 64 ? (c.k_chunk == 128 ? 3 : 6) : 4;
-    while (c.stages > 2 && c.stages * (c.k_chunk / 2) + c.m_tile > 256 && c.m_tile <= 128) --c.stages;
     c.split = 1;
-    const int per_sm = 512 / tc_tmem_cols(c);
-    const int slots = sm_count * per_sm;
+    if (c.m_tile <= 64) {
+        c.k_chunk = (K % 256 == 0 && group_fits(256, G)) ? 256 : (K % 128 == 0 && group_fits(128, G)) ? 128 : 64;
+        c.tmem_stages = 2;
+    } else {
+        c.k_chunk = (K % 128 == 0 && group_fits(128, G)) ? 128 : 64;
+        c.tmem_stages = c.m_tile == 128 ? 3 : 2;
+    }
+    c.stages = fill_stages(c, G, 200 * 1024, 8);
+    const int per_sm = std::max(1, 512 / tc_tmem_cols(c));
+    const int slots = sm_count * std::min(per_sm, static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024)));
     const int tiles = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
     const int C = K / c.k_chunk;
-    // Minimise (waves) x (stages of work per CTA) + a small cost per extra cluster rank.
+    // Minimise (waves) x (stages of work per CTA + fixed cost) + a small cost per cluster rank.
     double best = 1e30;
     for (int s = 1; s <= 16 && s <= C; ++s) {
         const int ctas = tiles * s;
@@ -118,7 +136,6 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
             c.split = s;
         }
     }
-    (void)G;
     return c;
 }
 
@@ -138,11 +155,16 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
         return W4A16_OK;
     }
     TcConfig c = tc_default(M, N, K, G, sm_count);
-    const bool custom = p.m_tile > 0 || p.k_chunk > 0 || p.stages > 0 || p.split_k > 0;
+    const bool custom = p.m_tile > 0 || p.k_chunk > 0 || p.stages > 0 || p.split_k > 0 || p.tmem_stages > 0;
     if (p.m_tile > 0) c.m_tile = p.m_tile;
     if (p.k_chunk > 0) c.k_chunk = p.k_chunk;
-    if (p.stages > 0) c.stages = p.stages;
+    if (p.tmem_stages > 0) c.tmem_stages = p.tmem_stages;
     if (p.split_k > 0) c.split = p.split_k;
+    if (p.stages > 0) {
+        c.stages = p.stages;
+    } else if (custom) {
+        c.stages = fill_stages(c, G, 200 * 1024, 8);
+    }
     if (custom && p.split_k <= 0) c.split = std::min(c.split, K / c.k_chunk);
     if (!tc_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     out->tc = c;
@@ -228,12 +250,13 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     out->path = ch.path;
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
-        out->m_tile = out->k_chunk = out->stages = 0;
+        out->m_tile = out->k_chunk = out->stages = out->tmem_stages = 0;
     } else {
         out->split_k = ch.tc.split;
         out->m_tile = ch.tc.m_tile;
         out->k_chunk = ch.tc.k_chunk;
         out->stages = ch.tc.stages;
+        out->tmem_stages = ch.tc.tmem_stages;
     }
     return W4A16_OK;
 }
@@ -273,10 +296,10 @@ int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
-                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d split_k=%d grid=(%d,%d,%d) "
-                 "block=320 tmem_cols=%d",
-                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.split, ch.tc.split, (N + 127) / 128,
-                 (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc));
+                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d split_k=%d "
+                 "grid=(%d,%d,%d) block=320 tmem_cols=%d smem=%zu",
+                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.split, ch.tc.split,
+                 (N + 127) / 128, (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
