@@ -63,6 +63,7 @@ typedef struct {
     int k_chunk;     /* TC: K per pipeline stage, 64, 128 or 256 */
     int stages;      /* TC: shared-memory pipeline depth, 2..16 */
     int tmem_stages; /* TC: tensor-memory (dequantised A) pipeline depth, 2..8 */
+    int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
 } w4a16_plan;
 
 /* Library version: major*10000 + minor*100 + patch. */

@@ -38,8 +38,8 @@ ORACLE_SCALE_PLANS = [
     None,
     dict(path=1), dict(path=1, split_k=1), dict(path=1, split_k=2), dict(path=1, split_k=5), dict(path=1, split_k=16),
     dict(path=2), dict(path=2, m_tile=16, k_chunk=128, stages=3, split_k=1),
-    dict(path=2, m_tile=16, k_chunk=64, stages=4, split_k=2), dict(path=2, m_tile=16, k_chunk=128, stages=2, split_k=3),
-    dict(path=2, m_tile=16, k_chunk=128, stages=3, split_k=8), dict(path=2, m_tile=32, k_chunk=64, stages=6, split_k=16),
+    dict(path=2, m_tile=16, k_chunk=256, stages=4, split_k=2), dict(path=2, m_tile=16, k_chunk=128, stages=2, split_k=3),
+    dict(path=2, m_tile=16, k_chunk=128, stages=3, split_k=8), dict(path=2, m_tile=32, k_chunk=128, stages=6, split_k=8),
 ]
 
 
@@ -91,20 +91,21 @@ def test_edge_rows_gemv(W, edge_matrix, M):
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
-TC_TILES = [(16, 64), (16, 128), (16, 256), (32, 64), (32, 128), (32, 256), (64, 64), (64, 128), (64, 256),
-            (128, 64), (128, 128), (256, 64), (256, 128)]
+# every instantiated (m_tile, k_chunk, mma_issuers) kernel
+TC_TILES = [(16, 128, 4), (16, 256, 4), (16, 256, 2), (32, 128, 4), (32, 256, 4), (64, 128, 4), (64, 256, 4),
+            (64, 256, 2), (128, 128, 2), (128, 128, 1), (256, 128, 1)]
 
 
-@pytest.mark.parametrize("mt,kc", TC_TILES)
-def test_every_tc_tile(W, mt, kc):
+@pytest.mark.parametrize("mt,kc,ni", TC_TILES)
+def test_every_tc_tile(W, mt, kc, ni):
     M, K, N, G = mt - 3, 1024, 352, 128  # ragged last column tile (96 wide)
-    d, y_ref, abs_ref = _case(M, K, N, G, seed=mt + kc)
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=mt + kc + ni)
     x, qw_r, sc_r = _repacked(W, d, G)
     for split in (1, 3):
         for ts in (2, 3):
-            if ts * kc // 2 + mt > 512:
+            if ts * kc // 2 + ni * mt > 512:
                 continue
-            plan = dict(path=2, m_tile=mt, k_chunk=kc, split_k=split, tmem_stages=ts)
+            plan = dict(path=2, m_tile=mt, k_chunk=kc, split_k=split, tmem_stages=ts, mma_issuers=ni)
             y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
             assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
@@ -113,7 +114,7 @@ def test_shallow_and_deep_rings(W):
     M, K, N, G = 16, 2048, 256, 128
     d, y_ref, abs_ref = _case(M, K, N, G, seed=31)
     x, qw_r, sc_r = _repacked(W, d, G)
-    for (kc, st, ts) in [(64, 2, 2), (64, 16, 8), (128, 2, 2), (128, 7, 3), (256, 2, 2), (256, 5, 2)]:
+    for (kc, st, ts) in [(128, 2, 2), (128, 16, 6), (128, 7, 3), (256, 2, 2), (256, 5, 3)]:
         plan = dict(path=2, m_tile=16, k_chunk=kc, stages=st, tmem_stages=ts, split_k=1)
         y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
@@ -124,7 +125,7 @@ def test_group_sizes(W, G):
     M, K, N = 5, 1024, 128
     d, y_ref, abs_ref = _case(M, K, N, G, seed=G)
     x, qw_r, sc_r = _repacked(W, d, G)
-    plans = [dict(path=1), dict(path=2, k_chunk=64, stages=4), dict(path=2, k_chunk=128, stages=3, split_k=2),
+    plans = [dict(path=1), dict(path=2, k_chunk=128, stages=4), dict(path=2, k_chunk=128, stages=3, split_k=2),
              dict(path=2, k_chunk=256, split_k=2)]
     for plan in plans:
         y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
@@ -144,7 +145,7 @@ def test_one_hot_rows_are_exact(W):
     expect = np.stack([w[k] for k in ks]).astype(np.float16)  # every w is an fp16 value
     xd, qw_r, sc_r = _repacked(W, d, G)
     plans = [dict(path=1, split_k=1), dict(path=1, split_k=4), dict(path=2, split_k=1), dict(path=2, split_k=4),
-             dict(path=2, m_tile=16, k_chunk=64, stages=4, split_k=8)]
+             dict(path=2, m_tile=16, k_chunk=128, stages=4, split_k=4)]
     for plan in plans:
         y = run_gemm(W, xd, qw_r, sc_r, N, K, G, plan=plan).cpu().numpy()
         assert np.array_equal(y.view(np.uint16), expect.view(np.uint16)), W.w4a16_last_dispatch()

@@ -42,7 +42,8 @@ class Plan(ctypes.Structure):
     """Mirror of ``w4a16_plan``; zero fields mean automatic."""
 
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("m_tile", ctypes.c_int),
-                ("k_chunk", ctypes.c_int), ("stages", ctypes.c_int), ("tmem_stages", ctypes.c_int)]
+                ("k_chunk", ctypes.c_int), ("stages", ctypes.c_int), ("tmem_stages", ctypes.c_int),
+                ("mma_issuers", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

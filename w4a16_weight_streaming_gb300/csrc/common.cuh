@@ -82,6 +82,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Same contract as mbar_wait, for single-thread roles on the critical path (producer, MMA
+// issuer): polls with the non-suspending test_wait so the thread reacts as soon as the phase
+// completes instead of after a suspension time slice.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t timeout_ns, unsigned* status) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((spin & 255u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > timeout_ns) {
+                atomicExch(status, kErrTimeout);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Warp-wide wait: lane 0 polls (so a warp puts one poller, not 32, on the barrier), the warp
 // reconverges, then every lane performs its own (now immediate) acquiring test of the phase.
 // Returns the same verdict in all lanes. Must be called by all 32 lanes.
@@ -173,8 +205,20 @@ __device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 
-// One warp loads 8 consecutive 32-bit TMEM columns of its 32 lanes (thread i <- lane i).
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+// One warp loads N consecutive 32-bit TMEM columns of its 32 lanes (thread i <- lane i).
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]);
+
+template <>
+__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr)

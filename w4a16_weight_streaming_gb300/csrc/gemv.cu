@@ -108,6 +108,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 
     const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;      // + kb * wt
     const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;  // + g * wt
+    // scale row of 32-k block b: b / (G / 32), a shift when G / 32 is a power of two
+    const int gb = G / 32;
+    const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
+    auto group_of = [&](int b) { return gshift >= 0 ? (b >> gshift) : b / gb; };
 
     int kb = sl.kb_begin + warp;
     for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         for (int u = 0; u < kUnroll; ++u) {
             const int b = kb + kWarps * u;
             v[u] = ldg_stream(wcol + static_cast<int64_t>(b) * wt);
-            sb[u] = ldg_u16(scol + static_cast<int64_t>((b * 32) / G) * wt);
+            sb[u] = ldg_u16(scol + static_cast<int64_t>(group_of(b)) * wt);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     }
     for (; kb < sl.kb_end; kb += kWarps) {
         const uint4 v = ldg_stream(wcol + static_cast<int64_t>(kb) * wt);
-        const uint16_t sb = ldg_u16(scol + static_cast<int64_t>((kb * 32) / G) * wt);
+        const uint16_t sb = ldg_u16(scol + static_cast<int64_t>(group_of(kb)) * wt);
         gemv_block<MR>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
     }
 

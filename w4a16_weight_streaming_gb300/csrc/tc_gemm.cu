@@ -17,14 +17,21 @@
 //     far from its issue limit.
 //   TMEM A stages (a_stages): KC/2 columns each (fp16 pairs).
 //
-// Warp roles (320 threads):
-//   warps 0-7  dequantise. Warp w owns TMEM lanes 32*(w%4).. (column slice w%4) and belongs to
-//              group w/4; the two groups take alternate stages, so two stages are in
-//              dequantisation at once. Then both groups run the epilogue.
-//   warp 8     TMA producer (one thread).
-//   warp 9     allocates TMEM and issues tcgen05.mma (one thread).
-// Barriers: full[s] (TMA bytes landed) -> afull[a] (A stage written) -> MMA -> tcgen05.commit ->
-// empty[s] (shared stage free) and aempty[a] (TMEM A stage free). Every wait is bounded.
+// Warp roles (672 threads):
+//   warps 0-15 dequantise. Warp w owns TMEM lanes 32*(w%4).. (column slice w%4) and part w/4
+//              of every stage's K range (KC/4 rows of K), so all 16 warps work on the same stage
+//              and every SM sub-partition has four dequantising warps to interleave. Then all 16
+//              run the epilogue.
+//   warp 16    TMA producer (one thread).
+//   warps 17-20 MMA issuers: `issuers` of them (1, 2 or 4) each issue, from one thread, the
+//              k-steps kk = j, j + issuers, ... of every stage into their own fp32 accumulator
+//              D_j. A single thread can issue one tcgen05.mma only every ~45-55 cycles, which at
+//              small N (2,048 weights per MMA) is slower than HBM delivers weights; several
+//              issuers keep the tensor core fed. The epilogue sums D_0.. D_{issuers-1} in order.
+//              Warp 17 also allocates and frees TMEM.
+// Barriers: full[s] (TMA bytes landed) -> afull[a] (A stage written) -> MMA -> tcgen05.commit by
+// every issuer -> empty[s] (shared stage free) and aempty[a] (TMEM A stage free). Every wait is
+// bounded.
 //
 // Split-K: the `split` CTAs of a thread-block cluster cover disjoint K ranges of the same
 // 128 x MT output tile; after the mainloop each CTA writes its fp32 partial tile to shared
@@ -38,10 +45,11 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kGroupWarps = 4;  // dequant warps per group (one per TMEM lane quadrant)
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kDequantWarps = 16;  // 4 lane quadrants x 4 K parts
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp0 = 17;      // first MMA issuer; also the TMEM allocator
+constexpr int kMaxIssuers = 4;
+constexpr int kThreads = 32 * (kDequantWarps + 1 + kMaxIssuers);
 constexpr int kTileN = 128;  // output columns per CTA (= TMEM lanes)
 
 struct SmemPlan {
@@ -50,7 +58,7 @@ struct SmemPlan {
     uint32_t s_off, s_stage;  // scales: s_stages x (ngs * 128 * 2)
     uint32_t red_off;         // split-K partial tile, MT * 128 * 4 (may overlap the x tiles)
     uint32_t bar_off;         // 2 * s_stages + 2 * a_stages + 1 mbarriers
-    uint32_t misc_off;        // tmem address slot, abort flag
+    uint32_t misc_off;        // tmem address slot, abort flag, two issuer go flags
     uint32_t total;           // bytes from the 1024-aligned base
 };
 
@@ -78,10 +86,12 @@ __host__ __device__ inline SmemPlan make_plan(int MT, int KC, int s_stages, int 
     return p;
 }
 
-__host__ __device__ inline int tmem_cols_needed(int MT, int KC, int a_stages) { return a_stages * (KC / 2) + MT; }
+__host__ __device__ inline int tmem_cols_needed(int MT, int KC, int a_stages, int issuers) {
+    return a_stages * (KC / 2) + issuers * MT;
+}
 
-__host__ __device__ inline uint32_t tmem_alloc_cols(int MT, int KC, int a_stages) {
-    const int need = tmem_cols_needed(MT, KC, a_stages);
+__host__ __device__ inline uint32_t tmem_alloc_cols(int MT, int KC, int a_stages, int issuers) {
+    const int need = tmem_cols_needed(MT, KC, a_stages, issuers);
     uint32_t c = 32;
     while (static_cast<int>(c) < need) c <<= 1;
     return c;
@@ -98,15 +108,18 @@ __device__ __forceinline__ void tma_load_x(uint32_t dst, const void* tmap, int k
     }
 }
 
-template <int MT, int KC, int MIN_BLOCKS>
-__global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
+template <int MT, int KC, int NI>
+__global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
                    int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
+    constexpr int issuers = NI;
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
-    static_assert(KC == 64 || KC == 128 || KC == 256, "stage K must be 64, 128 or 256");
-    constexpr int kKB = KC / 32;    // 32-k blocks per stage
-    constexpr int kACols = KC / 2;  // TMEM columns of one A stage (fp16 pairs)
+    static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
+    static_assert(NI == 1 || NI == 2 || NI == 4, "1, 2 or 4 MMA issuers");
+    constexpr int kKB = KC / 32;      // 32-k blocks per stage
+    constexpr int kPartKB = kKB / 4;  // 32-k blocks per dequant warp per stage (1 or 2)
+    constexpr int kACols = KC / 2;    // TMEM columns of one A stage (fp16 pairs)
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -125,22 +138,22 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t ncols = tmem_alloc_cols(MT, KC, a_stages);
+    const uint32_t ncols = tmem_alloc_cols(MT, KC, a_stages, issuers);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < s_stages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), issuers);  // one commit per MMA issuer
         }
         for (int a = 0; a < a_stages; ++a) {
-            mbar_init(afull_bar(a), kGroupWarps);  // one elected arrival per warp of the group
-            mbar_init(aempty_bar(a), 1);
+            mbar_init(afull_bar(a), kDequantWarps);  // one elected arrival per dequant warp
+            mbar_init(aempty_bar(a), issuers);
         }
-        mbar_init(dfull_bar, 1);
+        mbar_init(dfull_bar, issuers);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tmem_alloc(smem_u32(tmem_slot), ncols);
         tmem_relinquish();
     }
@@ -173,12 +186,11 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
             const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
             const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
             int issued = 0;
+            int s = 0;
+            uint32_t ph = 0;  // phase parity of the current use of stage s
             for (int i = 0; i < niter; ++i) {
-                const int s = i % s_stages;
-                if (i >= s_stages &&
-                    !mbar_wait(empty_bar(s), static_cast<uint32_t>(i / s_stages - 1) & 1u, abort_flag, timeout_ns,
-                               status))
-                    break;
+                // far ahead of the consumers: a suspending wait costs no issue slots and no latency here
+                if (i >= s_stages && !mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, timeout_ns, status)) break;
                 const int k0 = (c_begin + i) * KC;
                 const uint32_t fb = full_bar(s);
                 mbar_arrive_expect_tx(fb, bytes);
@@ -192,97 +204,143 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
                     for (int a = 0; a < KC / 64; ++a) tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, fb);
                 }
                 issued = i + 1;
+                if (++s == s_stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             // Let the copies still in flight land before shared memory can be released.
             int dummy_abort = 0;
-            for (int i = issued > s_stages ? issued - s_stages : 0; i < issued; ++i)
+            for (int i = issued > s_stages ? issued - s_stages : 0; i < issued; ++i)  // (only after the loop)
                 mbar_wait(full_bar(i % s_stages), static_cast<uint32_t>(i / s_stages) & 1u, &dummy_abort, timeout_ns,
                           status);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+    } else if (warp >= kMmaWarp0) {
+        const int j = warp - kMmaWarp0;  // issuer index
+        if (j < NI) {
             constexpr uint32_t idesc = idesc_f16_f32(128, MT);
+            const uint32_t d_j = d_tmem + static_cast<uint32_t>(j * MT);
+            // descriptor of k-step 0 of stage 0; stage s and k-step kk add their byte offsets / 16
+            const uint64_t desc0 = smem_desc_sw128(sbase + P.x_off);
+            const uint32_t stage_step = P.x_stage >> 4;
+            int s = 0, a = 0;
+            uint32_t sph = 0, aph = 0;
+            // go[i & 1]: issuer 0's verdict for stage i, double-buffered so that one named barrier per
+            // stage suffices (every reader has read go[(i - 1) & 1] before it reaches barrier i).
+            volatile int* go = reinterpret_cast<volatile int*>(smem + P.misc_off + 8);
             for (int i = 0; i < niter; ++i) {
-                const int s = i % s_stages;
-                const int a = i % a_stages;
-                if (!mbar_wait(afull_bar(a), static_cast<uint32_t>(i / a_stages) & 1u, abort_flag, timeout_ns, status))
-                    break;
-                if (!mbar_wait(full_bar(s), static_cast<uint32_t>(i / s_stages) & 1u, abort_flag, timeout_ns, status))
-                    break;
-                tc_fence_after();
-                const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
-                const uint32_t x_stage = sbase + P.x_off + s * P.x_stage;
+                // issuer 0 polls the two barriers; the others sleep on a named barrier until it has
+                if (j == 0 && lane == 0)
+                    go[i & 1] = (mbar_spin(afull_bar(a), aph, abort_flag, timeout_ns, status) &&
+                                 mbar_spin(full_bar(s), sph, abort_flag, timeout_ns, status))
+                                    ? 1
+                                    : 0;
+                if (NI > 1) asm volatile("bar.sync 1, %0;" ::"n"(32 * NI) : "memory");
+                else __syncwarp();
+                if (go[i & 1] == 0) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
+                    const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
 #pragma unroll
-                for (int kk = 0; kk < KC / 16; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128(x_stage + (kk / 4) * MT * 128 + (kk % 4) * 32);
-                    umma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (i > 0) || (kk > 0));
+                    for (int kk = j; kk < KC / 16; kk += NI) {
+                        const uint32_t koff = static_cast<uint32_t>(((kk / 4) * MT * 128 + (kk % 4) * 32) >> 4);
+                        umma_f16_ts(d_j, a_tmem + kk * 8, dstage + koff, idesc, (i > 0) || (kk >= NI));
+                    }
+                    umma_commit(empty_bar(s));
+                    umma_commit(aempty_bar(a));
                 }
-                umma_commit(empty_bar(s));
-                umma_commit(aempty_bar(a));
+                __syncwarp();
+                if (++s == s_stages) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+                if (++a == a_stages) {
+                    a = 0;
+                    aph ^= 1u;
+                }
             }
-            umma_commit(dfull_bar);
+            if (lane == 0) umma_commit(dfull_bar);
         }
         __syncwarp();
     } else {
         // ---------------- dequantisation warps
         const int q = warp & 3;
-        const int grp = warp >> 2;
+        const int part = warp >> 2;
         const bool valid = 32 * q < wt;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        for (int i = grp; i < niter; i += 2) {
-            const int s = i % s_stages;
-            const int a = i % a_stages;
-            if (!warp_wait(full_bar(s), static_cast<uint32_t>(i / s_stages) & 1u, abort_flag, timeout_ns, status))
-                break;
-            if (i >= a_stages &&
-                !warp_wait(aempty_bar(a), static_cast<uint32_t>(i / a_stages - 1) & 1u, abort_flag, timeout_ns, status))
-                break;
+        // scale row (within a stage's scale block) of each of this warp's 32-k blocks
+        int srow[kPartKB];
+#pragma unroll
+        for (int u = 0; u < kPartKB; ++u) srow[u] = KC >= G ? (32 * (part * kPartKB + u)) / G : 0;
+        const uint4* wst0 = reinterpret_cast<const uint4*>(smem + P.w_off) + 32 * q + lane + part * kPartKB * wt;
+        const uint16_t* sst0 = reinterpret_cast<const uint16_t*>(smem + P.s_off) + 32 * q + lane;
+        const uint32_t a_base = tmem + lane_base + static_cast<uint32_t>(part * kPartKB * 16);
+        int s = 0, a = 0;
+        uint32_t sph = 0, aph = 0;
+        for (int i = 0; i < niter; ++i) {
+            if (!warp_wait(full_bar(s), sph, abort_flag, timeout_ns, status)) break;
+            if (i >= a_stages && !warp_wait(aempty_bar(a), aph ^ 1u, abort_flag, timeout_ns, status)) break;
             if (valid) {
-                const int k0 = (c_begin + i) * KC;
-                const int g0 = k0 / G;
-                const uint4* wst = reinterpret_cast<const uint4*>(smem + P.w_off + s * P.w_stage) + 32 * q + lane;
-                const uint16_t* sst = reinterpret_cast<const uint16_t*>(smem + P.s_off + s * P.s_stage) + 32 * q + lane;
-                const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(a * kACols);
+                const uint4* wst = wst0 + s * (P.w_stage / 16);
+                const uint16_t* sst = sst0 + s * (P.s_stage / 2);
+                uint32_t regs[kPartKB * 16];
+                uint4 v[kPartKB];
+                uint32_t sb[kPartKB];
 #pragma unroll
-                for (int bp = 0; bp < kKB; bp += 2) {
-                    uint32_t regs[32];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int b = bp + u;
-                        const uint4 v = wst[b * wt];
-                        const uint32_t sb = sst[((k0 + 32 * b) / G - g0) * wt];
-                        const uint32_t s2 = sb | (sb << 16);
-                        dequant8(v.x, s2, &regs[u * 16 + 0]);
-                        dequant8(v.y, s2, &regs[u * 16 + 4]);
-                        dequant8(v.z, s2, &regs[u * 16 + 8]);
-                        dequant8(v.w, s2, &regs[u * 16 + 12]);
-                    }
-                    tmem_st<32>(a_col + static_cast<uint32_t>(bp * 16), regs);
+                for (int u = 0; u < kPartKB; ++u) {
+                    v[u] = wst[u * wt];
+                    sb[u] = sst[srow[u] * wt];
                 }
+#pragma unroll
+                for (int u = 0; u < kPartKB; ++u) {
+                    const uint32_t s2 = sb[u] | (sb[u] << 16);
+                    dequant8(v[u].x, s2, &regs[u * 16 + 0]);
+                    dequant8(v[u].y, s2, &regs[u * 16 + 4]);
+                    dequant8(v[u].z, s2, &regs[u * 16 + 8]);
+                    dequant8(v[u].w, s2, &regs[u * 16 + 12]);
+                }
+                tmem_st<kPartKB * 16>(a_base + static_cast<uint32_t>(a * kACols), regs);
                 tmem_wait_st();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(afull_bar(a));
+            if (++s == s_stages) {
+                s = 0;
+                sph ^= 1u;
+            }
+            if (++a == a_stages) {
+                a = 0;
+                aph ^= 1u;
+            }
         }
 
         // ---------------- epilogue: TMEM -> registers -> y (or the split-K partial tile)
         const bool have_d = warp_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
         tc_fence_after();
         if (have_d) {
-            const int mbase = grp * (MT / 2);
+            constexpr int kCols = MT / 4 < 8 ? MT / 4 : 8;  // columns per TMEM load
+            const int mbase = part * (MT / 4);
             float* red = reinterpret_cast<float*>(smem + P.red_off);
             const int n = n0 + 32 * q + lane;
 #pragma unroll 1
-            for (int c = 0; c < MT / 2; c += 8) {
-                uint32_t r[8];
-                tmem_ld8(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
+            for (int c = 0; c < MT / 4; c += kCols) {
+                uint32_t r[kCols];
+                tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
                 tmem_wait_ld();
+                for (int jj = 1; jj < issuers; ++jj) {  // fixed order: D_0 + D_1 + ...
+                    uint32_t r2[kCols];
+                    tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + jj * MT + mbase + c), r2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < kCols; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + __uint_as_float(r2[t]));
+                }
                 if (split == 1) {
                     if (valid) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
+                        for (int j = 0; j < kCols; ++j) {
                             const int m = m0 + mbase + c + j;
                             if (m < M)
                                 y[static_cast<int64_t>(m) * N + n] =
@@ -291,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < kCols; ++j)
                         red[(mbase + c + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
                 }
             }
@@ -331,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
     }
 
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
@@ -380,15 +438,15 @@ bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int KC, int MIN_BLOCKS>
+template <int MT, int KC, int NI>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
                         uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    auto kern = tc_gemm_kernel<MT, KC, MIN_BLOCKS>;
+    auto kern = tc_gemm_kernel<MT, KC, NI>;
     const SmemPlan P = make_plan(MT, KC, c.stages, c.tmem_stages, G, c.split);
     size_t smem = P.total + 1024;  // + alignment slack for the 1024-byte base
     // Keep the number of co-resident CTAs within what TMEM can hold, so that no CTA ever waits
     // in tcgen05.alloc for a CTA of another cluster.
-    const int per_sm_tmem = 512 / static_cast<int>(tmem_alloc_cols(MT, KC, c.tmem_stages));
+    const int per_sm_tmem = 512 / static_cast<int>(tmem_alloc_cols(MT, KC, c.tmem_stages, c.issuers));
     const size_t min_smem = 233472 / (per_sm_tmem + 1) - 1024 + 16;
     if (smem < min_smem) smem = min_smem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -415,16 +473,26 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
 
 }  // namespace
 
+bool tc_instantiated(int m_tile, int k_chunk, int issuers) {
+    static const int kCombos[][3] = {{16, 128, 4},  {16, 256, 4},  {16, 256, 2},  {32, 128, 4},
+                                     {32, 256, 4},  {64, 128, 4},  {64, 256, 4},  {64, 256, 2},
+                                     {128, 128, 2}, {128, 128, 1}, {256, 128, 1}};
+    for (const auto& t : kCombos)
+        if (t[0] == m_tile && t[1] == k_chunk && t[2] == issuers) return true;
+    return false;
+}
+
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
     (void)M;
     (void)N;
     if (c.m_tile != 16 && c.m_tile != 32 && c.m_tile != 64 && c.m_tile != 128 && c.m_tile != 256) return false;
-    if (c.k_chunk != 64 && c.k_chunk != 128 && c.k_chunk != 256) return false;
+    if (c.k_chunk != 128 && c.k_chunk != 256) return false;
     if (K % c.k_chunk != 0) return false;
     if (c.stages < 2 || c.stages > 16) return false;
     if (c.tmem_stages < 2 || c.tmem_stages > 8) return false;
     if (c.split < 1 || c.split > 16 || c.split > K / c.k_chunk) return false;
-    if (tmem_cols_needed(c.m_tile, c.k_chunk, c.tmem_stages) > 512) return false;
+    if (!tc_instantiated(c.m_tile, c.k_chunk, c.issuers)) return false;
+    if (tmem_cols_needed(c.m_tile, c.k_chunk, c.tmem_stages, c.issuers) > 512) return false;
     if (c.k_chunk < G && G % c.k_chunk != 0) return false;
     if (c.k_chunk >= G && c.k_chunk % G != 0) return false;
     const SmemPlan P = make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.split);
@@ -436,28 +504,28 @@ size_t tc_smem_bytes(const TcConfig& c, int G) {
     return make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.split).total + 1024;
 }
 
-int tc_tmem_cols(const TcConfig& c) { return static_cast<int>(tmem_alloc_cols(c.m_tile, c.k_chunk, c.tmem_stages)); }
+int tc_tmem_cols(const TcConfig& c) {
+    return static_cast<int>(tmem_alloc_cols(c.m_tile, c.k_chunk, c.tmem_stages, c.issuers));
+}
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
     CUtensorMap tmap;
     bool three_d = false;
     if (!encode_x_map(&tmap, x, M, K, c.m_tile, c.k_chunk, &three_d)) return cudaErrorInvalidValue;
-#define W4A16_TC_CASE(MT_, KC_, MB_)                                                                          \
-    if (c.m_tile == MT_ && c.k_chunk == KC_)                                                                  \
-        return launch_tc_t<MT_, KC_, MB_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
-    W4A16_TC_CASE(16, 64, 2)
-    W4A16_TC_CASE(16, 128, 2)
-    W4A16_TC_CASE(16, 256, 1)
-    W4A16_TC_CASE(32, 64, 2)
-    W4A16_TC_CASE(32, 128, 2)
-    W4A16_TC_CASE(32, 256, 1)
-    W4A16_TC_CASE(64, 64, 2)
-    W4A16_TC_CASE(64, 128, 2)
-    W4A16_TC_CASE(64, 256, 1)
-    W4A16_TC_CASE(128, 64, 1)
+#define W4A16_TC_CASE(MT_, KC_, NI_)                                                                          \
+    if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_)                                              \
+        return launch_tc_t<MT_, KC_, NI_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
+    W4A16_TC_CASE(16, 128, 4)
+    W4A16_TC_CASE(16, 256, 4)
+    W4A16_TC_CASE(16, 256, 2)
+    W4A16_TC_CASE(32, 128, 4)
+    W4A16_TC_CASE(32, 256, 4)
+    W4A16_TC_CASE(64, 128, 4)
+    W4A16_TC_CASE(64, 256, 4)
+    W4A16_TC_CASE(64, 256, 2)
+    W4A16_TC_CASE(128, 128, 2)
     W4A16_TC_CASE(128, 128, 1)
-    W4A16_TC_CASE(256, 64, 1)
     W4A16_TC_CASE(256, 128, 1)
 #undef W4A16_TC_CASE
     return cudaErrorInvalidValue;

@@ -108,24 +108,23 @@ int fill_stages(const TcConfig& base, int G, size_t budget, int max_stages) {
     return best;
 }
 
-TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
-    TcConfig c;
-    c.m_tile = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-    c.split = 1;
-    if (c.m_tile <= 64) {
-        c.k_chunk = (K % 256 == 0 && group_fits(256, G)) ? 256 : (K % 128 == 0 && group_fits(128, G)) ? 128 : 64;
-        c.tmem_stages = 2;
-    } else {
-        c.k_chunk = (K % 128 == 0 && group_fits(128, G)) ? 128 : 64;
-        c.tmem_stages = c.m_tile == 128 ? 3 : 2;
-    }
-    c.stages = fill_stages(c, G, 200 * 1024, 8);
-    const int per_sm = std::max(1, 512 / tc_tmem_cols(c));
-    const int slots = sm_count * std::min(per_sm, static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024)));
+// MMA issuers: one thread issues a tcgen05.mma only every ~45-55 cycles, while an N = 16..32 MMA
+// executes in 8-16; small tiles need several issuers, N >= 128 tiles are bound by the math.
+int default_issuers(int m_tile) { return m_tile <= 64 ? 4 : m_tile <= 128 ? 2 : 1; }
+
+int default_tmem_stages(int m_tile, int k_chunk, int issuers) {
+    return std::min(4, (512 - issuers * m_tile) / (k_chunk / 2));
+}
+
+// Split along K that minimises (waves) x (stages of work per CTA + fixed cost) + a small cost per
+// cluster rank, for the co-residency the config allows.
+int pick_split(const TcConfig& c, int M, int N, int K, int G, int sm_count) {
+    const int per_sm = std::max(1, std::min(512 / tc_tmem_cols(c), static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024))));
+    const int slots = sm_count * per_sm;
     const int tiles = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
     const int C = K / c.k_chunk;
-    // Minimise (waves) x (stages of work per CTA + fixed cost) + a small cost per cluster rank.
     double best = 1e30;
+    int split = 1;
     for (int s = 1; s <= 16 && s <= C; ++s) {
         const int ctas = tiles * s;
         const int waves = (ctas + slots - 1) / slots;
@@ -133,9 +132,22 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
         const double cost = static_cast<double>(waves) * (per_cta + 2.0) + 0.25 * s;
         if (cost < best - 1e-9) {
             best = cost;
-            c.split = s;
+            split = s;
         }
     }
+    return split;
+}
+
+TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
+    TcConfig c;
+    c.m_tile = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    c.split = 1;
+    const bool kc256 = c.m_tile <= 64 && K % 256 == 0 && group_fits(256, G);
+    c.k_chunk = kc256 ? 256 : 128;
+    c.issuers = default_issuers(c.m_tile);
+    c.tmem_stages = default_tmem_stages(c.m_tile, c.k_chunk, c.issuers);
+    c.stages = fill_stages(c, G, 200 * 1024, 8);
+    c.split = pick_split(c, M, N, K, G, sm_count);
     return c;
 }
 
@@ -155,17 +167,22 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
         return W4A16_OK;
     }
     TcConfig c = tc_default(M, N, K, G, sm_count);
-    const bool custom = p.m_tile > 0 || p.k_chunk > 0 || p.stages > 0 || p.split_k > 0 || p.tmem_stages > 0;
-    if (p.m_tile > 0) c.m_tile = p.m_tile;
-    if (p.k_chunk > 0) c.k_chunk = p.k_chunk;
-    if (p.tmem_stages > 0) c.tmem_stages = p.tmem_stages;
-    if (p.split_k > 0) c.split = p.split_k;
-    if (p.stages > 0) {
-        c.stages = p.stages;
-    } else if (custom) {
-        c.stages = fill_stages(c, G, 200 * 1024, 8);
+    const bool custom =
+        p.m_tile > 0 || p.k_chunk > 0 || p.stages > 0 || p.split_k > 0 || p.tmem_stages > 0 || p.mma_issuers > 0;
+    if (custom) {
+        if (p.m_tile > 0) c.m_tile = p.m_tile;
+        if (p.k_chunk > 0) {
+            c.k_chunk = p.k_chunk;
+        } else {
+            if (c.m_tile > 64) c.k_chunk = 128;
+            // shrink the stage until every cluster rank gets at least one stage
+            if (p.split_k > 0 && K / c.k_chunk < p.split_k) c.k_chunk = 128;
+        }
+        c.issuers = p.mma_issuers > 0 ? p.mma_issuers : default_issuers(c.m_tile);
+        c.tmem_stages = p.tmem_stages > 0 ? p.tmem_stages : default_tmem_stages(c.m_tile, c.k_chunk, c.issuers);
+        c.stages = p.stages > 0 ? p.stages : fill_stages(c, G, 200 * 1024, 8);
+        c.split = p.split_k > 0 ? p.split_k : std::min(pick_split(c, M, N, K, G, sm_count), K / c.k_chunk);
     }
-    if (custom && p.split_k <= 0) c.split = std::min(c.split, K / c.k_chunk);
     if (!tc_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     out->tc = c;
     return W4A16_OK;
@@ -250,13 +267,14 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     out->path = ch.path;
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
-        out->m_tile = out->k_chunk = out->stages = out->tmem_stages = 0;
+        out->m_tile = out->k_chunk = out->stages = out->tmem_stages = out->mma_issuers = 0;
     } else {
         out->split_k = ch.tc.split;
         out->m_tile = ch.tc.m_tile;
         out->k_chunk = ch.tc.k_chunk;
         out->stages = ch.tc.stages;
         out->tmem_stages = ch.tc.tmem_stages;
+        out->mma_issuers = ch.tc.issuers;
     }
     return W4A16_OK;
 }
@@ -296,9 +314,10 @@ int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
-                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d split_k=%d "
-                 "grid=(%d,%d,%d) block=320 tmem_cols=%d smem=%zu",
-                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.split, ch.tc.split,
+                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
+                 "split_k=%d grid=(%d,%d,%d) block=672 tmem_cols=%d smem=%zu",
+                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers, ch.tc.split,
+                 ch.tc.split,
                  (N + 127) / 128, (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
     }
     {
