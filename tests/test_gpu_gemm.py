@@ -92,8 +92,8 @@ def test_edge_rows_gemv(W, edge_matrix, M):
 
 
 # every instantiated (m_tile, k_chunk, mma_issuers) kernel
-TC_TILES = [(16, 128, 4), (16, 256, 4), (16, 256, 2), (32, 128, 4), (32, 256, 4), (64, 128, 4), (64, 256, 4),
-            (64, 256, 2), (128, 128, 2), (128, 128, 1), (256, 128, 1)]
+TC_TILES = [(16, 128, 4), (16, 256, 4), (32, 128, 4), (32, 256, 4), (64, 128, 4), (64, 256, 4), (64, 256, 2),
+            (128, 128, 2), (128, 128, 1), (256, 128, 1)]
 
 
 @pytest.mark.parametrize("mt,kc,ni", TC_TILES)

@@ -13,25 +13,26 @@
 //   shared-memory stages (s_stages): per stage ONE bulk copy of the 128-column tile's packed
 //     weights for KC rows of K (contiguous in the streaming layout), ONE bulk copy of its scales,
 //     ONE 3-D tensor copy of the x tile (KC/64 blocks of 64 k x MT rows, 128-byte swizzle, rows
-//     beyond M zero-filled). Three copy instructions per stage keep the single producer thread
-//     far from its issue limit.
+//     beyond M zero-filled), all completing one mbarrier.
 //   TMEM A stages (a_stages): KC/2 columns each (fp16 pairs).
 //
-// Warp roles (672 threads):
-//   warps 0-15 dequantise. Warp w owns TMEM lanes 32*(w%4).. (column slice w%4) and part w/4
-//              of every stage's K range (KC/4 rows of K), so all 16 warps work on the same stage
-//              and every SM sub-partition has four dequantising warps to interleave. Then all 16
-//              run the epilogue.
-//   warp 16    TMA producer (one thread).
-//   warps 17-20 MMA issuers: `issuers` of them (1, 2 or 4) each issue, from one thread, the
-//              k-steps kk = j, j + issuers, ... of every stage into their own fp32 accumulator
-//              D_j. A single thread can issue one tcgen05.mma only every ~45-55 cycles, which at
-//              small N (2,048 weights per MMA) is slower than HBM delivers weights; several
-//              issuers keep the tensor core fed. The epilogue sums D_0.. D_{issuers-1} in order.
-//              Warp 17 also allocates and frees TMEM.
-// Barriers: full[s] (TMA bytes landed) -> afull[a] (A stage written) -> MMA -> tcgen05.commit by
-// every issuer -> empty[s] (shared stage free) and aempty[a] (TMEM A stage free). Every wait is
-// bounded.
+// Warp roles:
+//   warps 0-15 dequantise: warp w owns TMEM lanes 32*(w%4).. (column slice w%4) and part w/4 of
+//              every stage's K range (KC/4 rows). All 16 run the epilogue.
+//   warp 16    TMA producer (one thread); also allocates and frees TMEM.
+// The stage's k-steps are split among NA fp32 accumulators D_0..D_{NA-1} (summed in order by
+// the epilogue), so that NA threads issue tcgen05.mma: one thread issues one MMA only every
+// ~45-55 cycles, slower than HBM delivers weights for the small-N MMAs of decode shapes. Two
+// issue schemes (template GROUP_ISSUE):
+//   dedicated (small tiles): warps 17.. issue, one per accumulator; the dequant warps arrive on
+//     afull[a]; issuer 0 polls it and wakes the other issuers through a named barrier.
+//   grouped (large tiles): the 16/NA dequant warps of the parts feeding one accumulator meet at a
+//     named barrier once their A pieces are in TMEM, and the group's first warp issues the group's
+//     k-steps itself: no wake-up delay of a separate thread, and the math (N >= 128) hides issue.
+// Barriers: full[s] (TMA bytes landed) -> A in TMEM -> MMAs -> tcgen05.commit by each issuer ->
+// empty[s] (shared stage free; producer) and aempty[a] (TMEM A stage free; dequant warps). Every
+// mbarrier wait is bounded; grouped warps leave their loop only through a barrier reduction, so a
+// group leaves together.
 //
 // Split-K: the `split` CTAs of a thread-block cluster cover disjoint K ranges of the same
 // 128 x MT output tile; after the mainloop each CTA writes its fp32 partial tile to shared
@@ -46,10 +47,12 @@ namespace w4a16 {
 namespace {
 
 constexpr int kDequantWarps = 16;  // 4 lane quadrants x 4 K parts
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp0 = 17;      // first MMA issuer; also the TMEM allocator
-constexpr int kMaxIssuers = 4;
-constexpr int kThreads = 32 * (kDequantWarps + 1 + kMaxIssuers);
+constexpr int kProducerWarp = 16;  // also the TMEM allocator
+constexpr int kIssuerWarp0 = 17;   // first dedicated MMA issuer (dedicated scheme)
+constexpr int kMaxThreads = 32 * (kDequantWarps + 1 + 4);
+__host__ __device__ constexpr int threads_for(bool group_issue, int na) {
+    return 32 * (kDequantWarps + 1 + (group_issue ? 0 : na));
+}
 constexpr int kTileN = 128;  // output columns per CTA (= TMEM lanes)
 
 struct SmemPlan {
@@ -86,40 +89,61 @@ __host__ __device__ inline SmemPlan make_plan(int MT, int KC, int s_stages, int 
     return p;
 }
 
-__host__ __device__ inline int tmem_cols_needed(int MT, int KC, int a_stages, int issuers) {
-    return a_stages * (KC / 2) + issuers * MT;
+__host__ __device__ inline int tmem_cols_needed(int MT, int KC, int a_stages, int accs) {
+    return a_stages * (KC / 2) + accs * MT;
 }
 
-__host__ __device__ inline uint32_t tmem_alloc_cols(int MT, int KC, int a_stages, int issuers) {
-    const int need = tmem_cols_needed(MT, KC, a_stages, issuers);
+__host__ __device__ inline uint32_t tmem_alloc_cols(int MT, int KC, int a_stages, int accs) {
+    const int need = tmem_cols_needed(MT, KC, a_stages, accs);
     uint32_t c = 32;
     while (static_cast<int>(c) < need) c <<= 1;
     return c;
 }
 
-template <int KC>
-__device__ __forceinline__ void tma_load_x(uint32_t dst, const void* tmap, int k0, int m0, uint32_t bar, bool three_d) {
-    if (three_d) {
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-                dst),
-            "l"(tmap), "r"(0), "r"(m0), "r"(k0 / 64), "r"(bar)
-            : "memory");
-    }
+__device__ __forceinline__ void tma_load_x_3d(uint32_t dst, const void* tmap, int k0, int m0, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(tmap), "r"(0), "r"(m0), "r"(k0 / 64), "r"(bar)
+        : "memory");
 }
 
-template <int MT, int KC, int NI>
-__global__ void __launch_bounds__(kThreads, 1)
+// Warp-wide wait with a fast path: when the phase is already complete (the usual case for a deep
+// ring) one non-blocking test by every lane settles it; otherwise lane 0 polls (warp_wait).
+__device__ __forceinline__ bool warp_wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint64_t timeout_ns, unsigned* status) {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    return warp_wait(bar, parity, abort_flag, timeout_ns, status);
+}
+
+// Named barrier over `nthreads` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool group_sync_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0u;
+}
+
+template <int MT, int KC, int NA, bool GROUP_ISSUE>
+__global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
                    int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
-    constexpr int issuers = NI;
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
-    static_assert(NI == 1 || NI == 2 || NI == 4, "1, 2 or 4 MMA issuers");
-    constexpr int kKB = KC / 32;      // 32-k blocks per stage
-    constexpr int kPartKB = kKB / 4;  // 32-k blocks per dequant warp per stage (1 or 2)
-    constexpr int kACols = KC / 2;    // TMEM columns of one A stage (fp16 pairs)
+    static_assert(NA == 1 || NA == 2 || NA == 4, "1, 2 or 4 accumulators");
+    constexpr int kKB = KC / 32;                   // 32-k blocks per stage
+    constexpr int kPartKB = kKB / 4;               // 32-k blocks per dequant warp per stage (1 or 2)
+    constexpr int kACols = KC / 2;                 // TMEM columns of one A stage (fp16 pairs)
+    constexpr int kGroupWarps = kDequantWarps / NA;  // warps feeding one accumulator
+    constexpr int kGroupSteps = KC / 16 / NA;        // k-steps of 16 per accumulator per stage
+    constexpr int kThreads = threads_for(GROUP_ISSUE, NA);
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -130,34 +154,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar0 = sbase + P.bar_off;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (s_stages + s); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a_stages + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a); };
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a_stages + a); };  // dedicated scheme
     const uint32_t dfull_bar = bar0 + 8u * (2 * s_stages + 2 * a_stages);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.misc_off + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t ncols = tmem_alloc_cols(MT, KC, a_stages, issuers);
+    const uint32_t ncols = tmem_alloc_cols(MT, KC, a_stages, NA);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < s_stages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), issuers);  // one commit per MMA issuer
+            mbar_init(empty_bar(s), NA);  // one commit per accumulator group
         }
         for (int a = 0; a < a_stages; ++a) {
+            mbar_init(aempty_bar(a), NA);
             mbar_init(afull_bar(a), kDequantWarps);  // one elected arrival per dequant warp
-            mbar_init(aempty_bar(a), issuers);
         }
-        mbar_init(dfull_bar, issuers);
+        mbar_init(dfull_bar, NA);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp0) {
+    if (warp == kProducerWarp) {
         tmem_alloc(smem_u32(tmem_slot), ncols);
         tmem_relinquish();
+        if (lane == 0) prefetch_tmap(&tmap_x);
     }
-    if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmap_x);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -198,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_g2s(sbase + P.s_off + s * P.s_stage, s_tile + static_cast<int64_t>(k0 / G) * wt, sbytes, fb, pol);
                 const uint32_t xs = sbase + P.x_off + s * P.x_stage;
                 if (x_3d) {
-                    tma_load_x<KC>(xs, &tmap_x, k0, m0, fb, true);
+                    tma_load_x_3d(xs, &tmap_x, k0, m0, fb);
                 } else {
 #pragma unroll
                     for (int a = 0; a < KC / 64; ++a) tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, fb);
@@ -216,58 +240,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                           status);
         }
         __syncwarp();
-    } else if (warp >= kMmaWarp0) {
-        const int j = warp - kMmaWarp0;  // issuer index
-        if (j < NI) {
-            constexpr uint32_t idesc = idesc_f16_f32(128, MT);
-            const uint32_t d_j = d_tmem + static_cast<uint32_t>(j * MT);
-            // descriptor of k-step 0 of stage 0; stage s and k-step kk add their byte offsets / 16
-            const uint64_t desc0 = smem_desc_sw128(sbase + P.x_off);
-            const uint32_t stage_step = P.x_stage >> 4;
-            int s = 0, a = 0;
-            uint32_t sph = 0, aph = 0;
-            // go[i & 1]: issuer 0's verdict for stage i, double-buffered so that one named barrier per
-            // stage suffices (every reader has read go[(i - 1) & 1] before it reaches barrier i).
-            volatile int* go = reinterpret_cast<volatile int*>(smem + P.misc_off + 8);
-            for (int i = 0; i < niter; ++i) {
-                // issuer 0 polls the two barriers; the others sleep on a named barrier until it has
-                if (j == 0 && lane == 0)
-                    go[i & 1] = (mbar_spin(afull_bar(a), aph, abort_flag, timeout_ns, status) &&
-                                 mbar_spin(full_bar(s), sph, abort_flag, timeout_ns, status))
-                                    ? 1
-                                    : 0;
-                if (NI > 1) asm volatile("bar.sync 1, %0;" ::"n"(32 * NI) : "memory");
-                else __syncwarp();
-                if (go[i & 1] == 0) break;
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
-                    const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
+    } else if (!GROUP_ISSUE && warp >= kIssuerWarp0) {
+        // ---------------- dedicated MMA issuers, one per accumulator
+        const int j = warp - kIssuerWarp0;
+        constexpr uint32_t idesc = idesc_f16_f32(128, MT);
+        const uint32_t d_j = d_tmem + static_cast<uint32_t>(j * MT);
+        const uint64_t desc0 = smem_desc_sw128(sbase + P.x_off);
+        const uint32_t stage_step = P.x_stage >> 4;
+        // go[i & 1]: issuer 0's verdict for stage i, double-buffered so that one named barrier per
+        // stage suffices (every reader has read go[(i - 1) & 1] before it reaches barrier i).
+        volatile int* go = reinterpret_cast<volatile int*>(smem + P.misc_off + 8);
+        int s = 0, a = 0;
+        uint32_t sph = 0, aph = 0;
+        for (int i = 0; i < niter; ++i) {
+            if (j == 0 && lane == 0)
+                go[i & 1] = (mbar_spin(afull_bar(a), aph, abort_flag, timeout_ns, status) &&
+                             mbar_spin(full_bar(s), sph, abort_flag, timeout_ns, status))
+                                ? 1
+                                : 0;
+            if (NA > 1) asm volatile("bar.sync 5, %0;" ::"n"(32 * NA) : "memory");
+            else __syncwarp();
+            if (go[i & 1] == 0) break;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
+                const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
 #pragma unroll
-                    for (int kk = j; kk < KC / 16; kk += NI) {
-                        const uint32_t koff = static_cast<uint32_t>(((kk / 4) * MT * 128 + (kk % 4) * 32) >> 4);
-                        umma_f16_ts(d_j, a_tmem + kk * 8, dstage + koff, idesc, (i > 0) || (kk >= NI));
-                    }
-                    umma_commit(empty_bar(s));
-                    umma_commit(aempty_bar(a));
+                for (int t = 0; t < kGroupSteps; ++t) {
+                    const int ks = j + t * NA;  // interleaved k-steps keep the issuers evenly busy
+                    const uint32_t koff = static_cast<uint32_t>(((ks / 4) * MT * 128 + (ks % 4) * 32) >> 4);
+                    umma_f16_ts(d_j, a_tmem + ks * 8, dstage + koff, idesc, (i > 0) || (t > 0));
                 }
-                __syncwarp();
-                if (++s == s_stages) {
-                    s = 0;
-                    sph ^= 1u;
-                }
-                if (++a == a_stages) {
-                    a = 0;
-                    aph ^= 1u;
-                }
+                umma_commit(empty_bar(s));
+                umma_commit(aempty_bar(a));
             }
-            if (lane == 0) umma_commit(dfull_bar);
+            __syncwarp();
+            if (++s == s_stages) {
+                s = 0;
+                sph ^= 1u;
+            }
+            if (++a == a_stages) {
+                a = 0;
+                aph ^= 1u;
+            }
         }
+        if (lane == 0) umma_commit(dfull_bar);
         __syncwarp();
     } else {
-        // ---------------- dequantisation warps
+        // ---------------- dequantisation warps (and, grouped scheme, per group one MMA issuer)
         const int q = warp & 3;
         const int part = warp >> 2;
+        const int grp = warp / kGroupWarps;               // accumulator group
+        const bool issuer = (warp % kGroupWarps) == 0;    // first warp of the group issues its MMAs
         const bool valid = 32 * q < wt;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         // scale row (within a stage's scale block) of each of this warp's 32-k blocks
@@ -277,12 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4* wst0 = reinterpret_cast<const uint4*>(smem + P.w_off) + 32 * q + lane + part * kPartKB * wt;
         const uint16_t* sst0 = reinterpret_cast<const uint16_t*>(smem + P.s_off) + 32 * q + lane;
         const uint32_t a_base = tmem + lane_base + static_cast<uint32_t>(part * kPartKB * 16);
+        // MMA operands of this group: k-steps grp*kGroupSteps .. +kGroupSteps of each stage
+        constexpr uint32_t idesc = idesc_f16_f32(128, MT);
+        const uint32_t d_g = d_tmem + static_cast<uint32_t>(grp * MT);
+        const uint64_t desc0 = smem_desc_sw128(sbase + P.x_off);
+        const uint32_t stage_step = P.x_stage >> 4;
         int s = 0, a = 0;
         uint32_t sph = 0, aph = 0;
         for (int i = 0; i < niter; ++i) {
-            if (!warp_wait(full_bar(s), sph, abort_flag, timeout_ns, status)) break;
-            if (i >= a_stages && !warp_wait(aempty_bar(a), aph ^ 1u, abort_flag, timeout_ns, status)) break;
-            if (valid) {
+            bool ok = warp_wait_fast(full_bar(s), sph, abort_flag, timeout_ns, status);
+            if (ok && i >= a_stages) ok = warp_wait_fast(aempty_bar(a), aph ^ 1u, abort_flag, timeout_ns, status);
+            if (ok && valid) {
                 const uint4* wst = wst0 + s * (P.w_stage / 16);
                 const uint16_t* sst = sst0 + s * (P.s_stage / 2);
                 uint32_t regs[kPartKB * 16];
@@ -305,8 +334,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
             }
             tc_fence_before();
+            if (!GROUP_ISSUE) {
+                __syncwarp();
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(afull_bar(a));
+            } else {
+            // the group's A pieces for this stage are in TMEM (or some warp gave up a wait)
+            if (!group_sync_and(1 + grp, 32 * kGroupWarps, ok)) break;
+            if (issuer && lane == 0) {
+                tc_fence_after();
+                const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
+                const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
+#pragma unroll
+                for (int t = 0; t < kGroupSteps; ++t) {
+                    const int ks = grp * kGroupSteps + t;  // k-step of 16 within the stage
+                    const uint32_t koff = static_cast<uint32_t>(((ks / 4) * MT * 128 + (ks % 4) * 32) >> 4);
+                    umma_f16_ts(d_g, a_tmem + ks * 8, dstage + koff, idesc, (i > 0) || (t > 0));
+                }
+                umma_commit(empty_bar(s));
+                umma_commit(aempty_bar(a));
+            }
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(a));
             if (++s == s_stages) {
                 s = 0;
                 sph ^= 1u;
@@ -316,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 aph ^= 1u;
             }
         }
+        if (GROUP_ISSUE && issuer && lane == 0) umma_commit(dfull_bar);
+        __syncwarp();
 
         // ---------------- epilogue: TMEM -> registers -> y (or the split-K partial tile)
         const bool have_d = warp_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
@@ -330,9 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[kCols];
                 tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
                 tmem_wait_ld();
-                for (int jj = 1; jj < issuers; ++jj) {  // fixed order: D_0 + D_1 + ...
+#pragma unroll
+                for (int g = 1; g < NA; ++g) {  // fixed order: D_0 + D_1 + ...
                     uint32_t r2[kCols];
-                    tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + jj * MT + mbase + c), r2);
+                    tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + g * MT + mbase + c), r2);
                     tmem_wait_ld();
 #pragma unroll
                     for (int t = 0; t < kCols; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + __uint_as_float(r2[t]));
@@ -364,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int beg = static_cast<int>((static_cast<int64_t>(rank) * E4) / split);
         const int end = static_cast<int>((static_cast<int64_t>(rank + 1) * E4) / split);
         const uint32_t red_s = sbase + P.red_off;
-        for (int e4 = beg + static_cast<int>(threadIdx.x); e4 < end; e4 += kThreads) {
+        for (int e4 = beg + static_cast<int>(threadIdx.x); e4 < end; e4 += kThreads) {  // all warps
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int p = 0; p < split; ++p) {
                 const float4 v = ld_dsmem_f4(map_peer(red_s + 16u * e4, p));
@@ -389,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
-    if (warp == kMmaWarp0) {
+    if (warp == kProducerWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
@@ -438,10 +490,10 @@ bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int KC, int NI>
+template <int MT, int KC, int NI, bool GI>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
                         uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    auto kern = tc_gemm_kernel<MT, KC, NI>;
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI>;
     const SmemPlan P = make_plan(MT, KC, c.stages, c.tmem_stages, G, c.split);
     size_t smem = P.total + 1024;  // + alignment slack for the 1024-byte base
     // Keep the number of co-resident CTAs within what TMEM can hold, so that no CTA ever waits
@@ -457,7 +509,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.split, (N + kTileN - 1) / kTileN, (M + MT - 1) / MT);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(GI, NI), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx.stream;
     cudaLaunchAttribute attr[1];
@@ -474,9 +526,8 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
 }  // namespace
 
 bool tc_instantiated(int m_tile, int k_chunk, int issuers) {
-    static const int kCombos[][3] = {{16, 128, 4},  {16, 256, 4},  {16, 256, 2},  {32, 128, 4},
-                                     {32, 256, 4},  {64, 128, 4},  {64, 256, 4},  {64, 256, 2},
-                                     {128, 128, 2}, {128, 128, 1}, {256, 128, 1}};
+    static const int kCombos[][3] = {{16, 128, 4}, {16, 256, 4}, {32, 128, 4},  {32, 256, 4},  {64, 128, 4},
+                                     {64, 256, 4}, {64, 256, 2}, {128, 128, 2}, {128, 128, 1}, {256, 128, 1}};
     for (const auto& t : kCombos)
         if (t[0] == m_tile && t[1] == k_chunk && t[2] == issuers) return true;
     return false;
@@ -513,20 +564,19 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16
     CUtensorMap tmap;
     bool three_d = false;
     if (!encode_x_map(&tmap, x, M, K, c.m_tile, c.k_chunk, &three_d)) return cudaErrorInvalidValue;
-#define W4A16_TC_CASE(MT_, KC_, NI_)                                                                          \
+#define W4A16_TC_CASE(MT_, KC_, NI_, GI_)                                                                     \
     if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_)                                              \
-        return launch_tc_t<MT_, KC_, NI_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
-    W4A16_TC_CASE(16, 128, 4)
-    W4A16_TC_CASE(16, 256, 4)
-    W4A16_TC_CASE(16, 256, 2)
-    W4A16_TC_CASE(32, 128, 4)
-    W4A16_TC_CASE(32, 256, 4)
-    W4A16_TC_CASE(64, 128, 4)
-    W4A16_TC_CASE(64, 256, 4)
-    W4A16_TC_CASE(64, 256, 2)
-    W4A16_TC_CASE(128, 128, 2)
-    W4A16_TC_CASE(128, 128, 1)
-    W4A16_TC_CASE(256, 128, 1)
+        return launch_tc_t<MT_, KC_, NI_, GI_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
+    W4A16_TC_CASE(16, 128, 4, false)
+    W4A16_TC_CASE(16, 256, 4, false)
+    W4A16_TC_CASE(32, 128, 4, false)
+    W4A16_TC_CASE(32, 256, 4, false)
+    W4A16_TC_CASE(64, 128, 4, false)
+    W4A16_TC_CASE(64, 256, 4, false)
+    W4A16_TC_CASE(64, 256, 2, true)
+    W4A16_TC_CASE(128, 128, 2, true)
+    W4A16_TC_CASE(128, 128, 1, true)
+    W4A16_TC_CASE(256, 128, 1, true)
 #undef W4A16_TC_CASE
     return cudaErrorInvalidValue;
 }
