@@ -41,6 +41,8 @@ bool tc_instantiated(int m_tile, int k_chunk, int issuers);
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G);
 size_t tc_smem_bytes(const TcConfig& c, int G);
 int tc_tmem_cols(const TcConfig& c);
+// CTAs of this config resident on the current device at once (cluster occupancy), 0 if unknown.
+int tc_resident_ctas(const TcConfig& c, int G);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
 

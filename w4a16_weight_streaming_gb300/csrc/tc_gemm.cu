@@ -490,37 +490,74 @@ bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int KC, int NI, bool GI>
-cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
-                        uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    auto kern = tc_gemm_kernel<MT, KC, NI, GI>;
+// Dynamic shared memory for a config: the plan, plus padding so that no more CTAs share an SM
+// than its TMEM can hold (no CTA ever waits in tcgen05.alloc for a CTA of another cluster).
+size_t launch_smem(int MT, int KC, int G, const TcConfig& c) {
     const SmemPlan P = make_plan(MT, KC, c.stages, c.tmem_stages, G, c.split);
     size_t smem = P.total + 1024;  // + alignment slack for the 1024-byte base
-    // Keep the number of co-resident CTAs within what TMEM can hold, so that no CTA ever waits
-    // in tcgen05.alloc for a CTA of another cluster.
     const int per_sm_tmem = 512 / static_cast<int>(tmem_alloc_cols(MT, KC, c.tmem_stages, c.issuers));
     const size_t min_smem = 233472 / (per_sm_tmem + 1) - 1024 + 16;
-    if (smem < min_smem) smem = min_smem;
+    return smem < min_smem ? min_smem : smem;
+}
+
+template <typename Kern>
+cudaError_t prepare_kernel(Kern kern, size_t smem, int split) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    if (c.split > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
+    if (split > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+template <int MT, int KC, int NI, bool GI>
+cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cudaStream_t stream,
+                               cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.split, (N + kTileN - 1) / kTileN, (M + MT - 1) / MT);
     cfg.blockDim = dim3(threads_for(GI, NI), 1, 1);
     cfg.dynamicSmemBytes = smem;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
+    cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = c.split;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = c.split > 1 ? 1 : 0;
+    return cfg;
+}
+
+template <int MT, int KC, int NI, bool GI>
+cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
+                        uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI>;
+    const size_t smem = launch_smem(MT, KC, G, c);
+    cudaError_t e = prepare_kernel(kern, smem, c.split);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI>(c, M, N, smem, ctx.stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
                               c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
+}
+
+// CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.
+template <int MT, int KC, int NI, bool GI>
+int resident_ctas_t(const TcConfig& c, int G) {
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI>;
+    const size_t smem = launch_smem(MT, KC, G, c);
+    if (prepare_kernel(kern, smem, c.split) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchAttribute attr[1];
+    TcConfig one = c;
+    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI>(one, 1, kTileN, smem, nullptr, attr);
+    cfg.gridDim = dim3(c.split, 1, 1);
+    cfg.numAttrs = 1;  // query with the cluster shape even for split 1
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters * c.split;
 }
 
 }  // namespace
@@ -557,6 +594,23 @@ size_t tc_smem_bytes(const TcConfig& c, int G) {
 
 int tc_tmem_cols(const TcConfig& c) {
     return static_cast<int>(tmem_alloc_cols(c.m_tile, c.k_chunk, c.tmem_stages, c.issuers));
+}
+
+int tc_resident_ctas(const TcConfig& c, int G) {
+#define W4A16_TC_RES(MT_, KC_, NI_, GI_) \
+    if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_) return resident_ctas_t<MT_, KC_, NI_, GI_>(c, G);
+    W4A16_TC_RES(16, 128, 4, false)
+    W4A16_TC_RES(16, 256, 4, false)
+    W4A16_TC_RES(32, 128, 4, false)
+    W4A16_TC_RES(32, 256, 4, false)
+    W4A16_TC_RES(64, 128, 4, false)
+    W4A16_TC_RES(64, 256, 4, false)
+    W4A16_TC_RES(64, 256, 2, true)
+    W4A16_TC_RES(128, 128, 2, true)
+    W4A16_TC_RES(128, 128, 1, true)
+    W4A16_TC_RES(256, 128, 1, true)
+#undef W4A16_TC_RES
+    return 0;
 }
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,

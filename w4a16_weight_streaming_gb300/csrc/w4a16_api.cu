@@ -6,7 +6,9 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "internal.h"
 #include "w4a16.h"
@@ -118,15 +120,23 @@ int default_tmem_stages(int m_tile, int k_chunk, int issuers) {
 }
 
 // Split along K that minimises (waves) x (stages of work per CTA + fixed cost) + a small cost per
-// cluster rank, for the co-residency the config allows.
-int pick_split(const TcConfig& c, int M, int N, int K, int G, int sm_count) {
-    const int per_sm = std::max(1, std::min(512 / tc_tmem_cols(c), static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024))));
-    const int slots = sm_count * per_sm;
-    const int tiles = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
-    const int C = K / c.k_chunk;
+// cluster rank. Waves use the device's cluster occupancy for each split (clusters must fit inside
+// one GPC, so large clusters leave SMs idle); without a device, the SM count.
+int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, bool have_device) {
+    const int tiles = ((N + 127) / 128) * ((M + base.m_tile - 1) / base.m_tile);
+    const int C = K / base.k_chunk;
     double best = 1e30;
     int split = 1;
     for (int s = 1; s <= 16 && s <= C; ++s) {
+        TcConfig c = base;
+        c.split = s;
+        int slots = have_device ? tc_resident_ctas(c, G) : 0;
+        if (slots <= 0) {
+            const int per_sm = std::max(1, std::min(512 / tc_tmem_cols(c),
+                                                    static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024))));
+            slots = (sm_count * per_sm / s) * s;
+        }
+        if (slots <= 0) continue;
         const int ctas = tiles * s;
         const int waves = (ctas + slots - 1) / slots;
         const int per_cta = (C + s - 1) / s;
@@ -139,7 +149,7 @@ int pick_split(const TcConfig& c, int M, int N, int K, int G, int sm_count) {
     return split;
 }
 
-TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
+TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) {
     TcConfig c;
     c.m_tile = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     c.split = 1;
@@ -148,11 +158,43 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count) {
     c.issuers = default_issuers(c.m_tile);
     c.tmem_stages = default_tmem_stages(c.m_tile, c.k_chunk, c.issuers);
     c.stages = fill_stages(c, G, 225 * 1024, 8);
-    c.split = pick_split(c, M, N, K, G, sm_count);
+    c.split = pick_split(c, M, N, K, G, sm_count, have_device);
     return c;
 }
 
-int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, Choice* out) {
+int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
+                          Choice* out);
+
+// Automatic plans are resolved once per (device, M, N, K, group) and cached: the resolution queries
+// the driver's cluster occupancy for every candidate split.
+std::map<std::tuple<int, int, int, int, int>, Choice> g_plan_cache;
+
+int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, Choice* out) {
+    const bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
+                                               plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
+                                               plan->mma_issuers == 0);
+    if (!automatic || !have_device) return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, M, N, K, G);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_plan_cache.find(key);
+        if (it != g_plan_cache.end()) {
+            *out = it->second;
+            return W4A16_OK;
+        }
+    }
+    const int rc = resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
+    if (rc == W4A16_OK) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_plan_cache.size() < 4096) g_plan_cache[key] = *out;
+    }
+    return rc;
+}
+
+int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
+                          Choice* out) {
     w4a16_plan p = {};
     if (plan) p = *plan;
     if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
@@ -169,7 +211,7 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
         out->gemv_split = split;
         return W4A16_OK;
     }
-    TcConfig c = tc_default(M, N, K, G, sm_count);
+    TcConfig c = tc_default(M, N, K, G, sm_count, have_device);
     const bool custom =
         p.m_tile > 0 || p.k_chunk > 0 || p.stages > 0 || p.split_k > 0 || p.tmem_stages > 0 || p.mma_issuers > 0;
     if (custom) {
@@ -184,7 +226,7 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
         c.issuers = p.mma_issuers > 0 ? p.mma_issuers : default_issuers(c.m_tile);
         c.tmem_stages = p.tmem_stages > 0 ? p.tmem_stages : default_tmem_stages(c.m_tile, c.k_chunk, c.issuers);
         c.stages = p.stages > 0 ? p.stages : fill_stages(c, G, 225 * 1024, 8);
-        c.split = p.split_k > 0 ? p.split_k : std::min(pick_split(c, M, N, K, G, sm_count), K / c.k_chunk);
+        c.split = p.split_k > 0 ? p.split_k : std::min(pick_split(c, M, N, K, G, sm_count, have_device), K / c.k_chunk);
     }
     if (!tc_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     out->tc = c;
@@ -263,9 +305,10 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     if (sh != W4A16_OK) return sh;
     if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     DeviceInfo d;
-    const int sms = device_info(&d) ? d.sm_count : 152;
+    const bool dev = device_info(&d);
+    const int sms = dev ? d.sm_count : 152;
     Choice ch;
-    const int rc = resolve_plan(M, N, K, group, nullptr, sms, &ch);
+    const int rc = resolve_plan(M, N, K, group, nullptr, sms, dev, &ch);
     if (rc != W4A16_OK) return rc;
     out->path = ch.path;
     if (ch.path == W4A16_PATH_GEMV) {
@@ -299,7 +342,7 @@ int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r
     DeviceInfo d;
     if (!device_info(&d)) return W4A16_ERR_CUDA;
     Choice ch;
-    const int rc = resolve_plan(M, N, K, group, plan, d.sm_count, &ch);
+    const int rc = resolve_plan(M, N, K, group, plan, d.sm_count, true, &ch);
     if (rc != W4A16_OK) return rc;
     LaunchCtx ctx;
     ctx.stream = static_cast<cudaStream_t>(stream);
