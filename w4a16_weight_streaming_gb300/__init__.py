@@ -29,6 +29,7 @@ ERR_DEVICE_TIMEOUT = 5
 PATH_AUTO = 0
 PATH_GEMV = 1
 PATH_TC = 2
+PATH_STREAM = 3
 
 # every symbol include/w4a16.h declares
 EXPORTED = [
@@ -43,7 +44,7 @@ class Plan(ctypes.Structure):
 
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("m_tile", ctypes.c_int),
                 ("k_chunk", ctypes.c_int), ("stages", ctypes.c_int), ("tmem_stages", ctypes.c_int),
-                ("mma_issuers", ctypes.c_int)]
+                ("mma_issuers", ctypes.c_int), ("clusters", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

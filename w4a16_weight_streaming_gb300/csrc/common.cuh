@@ -114,6 +114,60 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Non-blocking test of a phase with acquire semantics at cluster scope: for phases completed by
+// arrivals of other CTAs of the cluster (mbar_arrive_remote), so that their prior shared-memory
+// writes are seen. (Measured: a thread suspended in try_wait is not woken promptly by a remote
+// arrival, so these phases are polled.)
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// Bounded wait of mbar_wait's contract on a phase completed by cluster peers (polled).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t timeout_ns, unsigned* status) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_test_wait_cluster(bar, parity)) return true;
+        if ((spin & 255u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > timeout_ns) {
+                atomicExch(status, kErrTimeout);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Arrives once, with release semantics at cluster scope, on the mbarrier at shared address `bar`
+// in the CTA of cluster rank `rank` (may be this CTA).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
+        "r"(rank)
+        : "memory");
+}
+
+// Named barriers (ids 1..15; id 0 is __syncthreads). `nthreads` counts every participating
+// thread, a multiple of 32. arrive does not wait; sync waits for the generation to complete.
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Warp-wide wait: lane 0 polls (so a warp puts one poller, not 32, on the barrier), the warp
 // reconverges, then every lane performs its own (now immediate) acquiring test of the phase.
 // Returns the same verdict in all lanes. Must be called by all 32 lanes.
@@ -124,6 +178,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) mbar_try_wait(bar, parity);
     return ok != 0;
+}
+
+// ------------------------------------------------------------------------------------ shared memory
+// Explicit shared-space loads by 32-bit shared address (a generic pointer into dynamic shared
+// memory is not always recognised as shared and would take the generic load path).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
 }
 
 // ------------------------------------------------------------------------------------ TMA

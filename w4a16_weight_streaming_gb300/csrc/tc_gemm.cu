@@ -298,8 +298,9 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
         int srow[kPartKB];
 #pragma unroll
         for (int u = 0; u < kPartKB; ++u) srow[u] = KC >= G ? (32 * (part * kPartKB + u)) / G : 0;
-        const uint4* wst0 = reinterpret_cast<const uint4*>(smem + P.w_off) + 32 * q + lane + part * kPartKB * wt;
-        const uint16_t* sst0 = reinterpret_cast<const uint16_t*>(smem + P.s_off) + 32 * q + lane;
+        // shared addresses of this lane's first vector / scale in stage 0 (explicit shared loads)
+        const uint32_t wst0 = sbase + P.w_off + 16u * static_cast<uint32_t>(32 * q + lane + part * kPartKB * wt);
+        const uint32_t sst0 = sbase + P.s_off + 2u * static_cast<uint32_t>(32 * q + lane);
         const uint32_t a_base = tmem + lane_base + static_cast<uint32_t>(part * kPartKB * 16);
         // MMA operands of this group: k-steps grp*kGroupSteps .. +kGroupSteps of each stage
         constexpr uint32_t idesc = idesc_f16_f32(128, MT);
@@ -312,15 +313,15 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
             bool ok = warp_wait_fast(full_bar(s), sph, abort_flag, timeout_ns, status);
             if (ok && i >= a_stages) ok = warp_wait_fast(aempty_bar(a), aph ^ 1u, abort_flag, timeout_ns, status);
             if (ok && valid) {
-                const uint4* wst = wst0 + s * (P.w_stage / 16);
-                const uint16_t* sst = sst0 + s * (P.s_stage / 2);
+                const uint32_t wst = wst0 + static_cast<uint32_t>(s) * P.w_stage;
+                const uint32_t sst = sst0 + static_cast<uint32_t>(s) * P.s_stage;
                 uint32_t regs[kPartKB * 16];
                 uint4 v[kPartKB];
                 uint32_t sb[kPartKB];
 #pragma unroll
                 for (int u = 0; u < kPartKB; ++u) {
-                    v[u] = wst[u * wt];
-                    sb[u] = sst[srow[u] * wt];
+                    v[u] = lds128(wst + 16u * static_cast<uint32_t>(u * wt));
+                    sb[u] = lds16(sst + 2u * static_cast<uint32_t>(srow[u] * wt));
                 }
 #pragma unroll
                 for (int u = 0; u < kPartKB; ++u) {
@@ -449,47 +450,6 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
 }
 
 // ------------------------------------------------------------------------------------ host
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// x viewed as [K/64 blocks][M rows][64 k] (strides 128 B and 2K B): one box = the whole stage
-// tile [KC/64][MT][64], laid out in shared memory exactly as the MMA's 128-byte-swizzle K-major
-// operand atoms expect. Falls back to a 2-D map ([M][K], box 64 x MT, KC/64 copies per stage)
-// if the driver refuses the 3-D one.
-bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int KC, bool* three_d) {
-    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr) return false;
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    {
-        const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128u};
-        const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MT), static_cast<cuuint32_t>(KC / 64)};
-        if (encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
-            *three_d = true;
-            return true;
-        }
-    }
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(MT)};
-    *three_d = false;
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Dynamic shared memory for a config: the plan, plus padding so that no more CTAs share an SM
 // than its TMEM can hold (no CTA ever waits in tcgen05.alloc for a CTA of another cluster).
 size_t launch_smem(int MT, int KC, int G, const TcConfig& c) {
@@ -561,6 +521,47 @@ int resident_ctas_t(const TcConfig& c, int G) {
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// x viewed as [K/64 blocks][M rows][64 k] (strides 128 B and 2K B): one box = the whole stage
+// tile [KC/64][MT][64], laid out in shared memory exactly as the MMA's 128-byte-swizzle K-major
+// operand atoms expect. Falls back to a 2-D map ([M][K], box 64 x MT, KC/64 copies per stage)
+// if the driver refuses the 3-D one.
+bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int KC, bool* three_d) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    {
+        const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128u};
+        const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MT), static_cast<cuuint32_t>(KC / 64)};
+        if (encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            *three_d = true;
+            return true;
+        }
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(MT)};
+    *three_d = false;
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool tc_instantiated(int m_tile, int k_chunk, int issuers) {
     static const int kCombos[][3] = {{16, 128, 4}, {16, 256, 4}, {32, 128, 4},  {32, 256, 4},  {64, 128, 4},

@@ -84,6 +84,7 @@ int check_matrix_shape(int N, int K, int G) {
 struct Choice {
     int path;
     TcConfig tc;
+    StreamConfig st;
     int gemv_split;
 };
 
@@ -162,6 +163,80 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) 
     return c;
 }
 
+// ---- persistent streaming kernel (M <= 64)
+int stream_m_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+// MMA issuers: one thread issues a tcgen05.mma only every ~110 cycles while the tensor pipe takes one
+// per ~40; each issuer owns an accumulator of m_tile TMEM columns.
+int stream_default_issuers(int m_tile) { return m_tile <= 32 ? 4 : 2; }
+
+// TMEM A ring depth (at most 7: two named barriers per stage) and accumulator buffering: two buffers (the epilogue
+// of a tile overlaps the next tile's MMAs) when that still leaves a ring of at least 3 (or the
+// requested depth), else one.
+void stream_tmem_layout(StreamConfig* c, int want_stages) {
+    for (int dbuf = 2; dbuf >= 1; --dbuf) {
+        const int room = (512 - dbuf * c->issuers * c->m_tile) / (c->k_chunk / 2);
+        const int a = want_stages > 0 ? want_stages : std::min(7, room);
+        if (a <= room && a >= (want_stages > 0 ? 2 : 3)) {
+            c->dbuf = dbuf;
+            c->tmem_stages = a;
+            return;
+        }
+    }
+    c->dbuf = 1;
+    c->tmem_stages = want_stages > 0 ? want_stages : std::min(7, (512 - c->issuers * c->m_tile) / (c->k_chunk / 2));
+}
+
+// Deepest shared-memory ring (at most `max_stages`) that fits next to the resident x slice and
+// the split-K partial tiles; 0 if not even two stages fit.
+int stream_fill_stages(StreamConfig c, int K, int G, int max_stages) {
+    int best = 0;
+    for (int s = 2; s <= max_stages; ++s) {
+        c.stages = s;
+        if (stream_smem_bytes(c, G, K) <= 225 * 1024) best = s;
+    }
+    return best;
+}
+
+// Split along K and number of persistent clusters. Each cluster walks ceil(tiles / clusters) tiles of
+// ceil(C / split) stages each; the clusters the device holds at once come from the driver's cluster
+// occupancy (clusters live inside one GPC, so some sizes leave SMs idle); without a device, the SM
+// count. A small cost per tile (epilogue hand-off) and per cluster rank (reduction) breaks ties.
+bool stream_pick(StreamConfig* io, int M, int N, int K, int G, int sm_count, bool have_device, int force_split,
+                 int force_stages, int force_clusters) {
+    (void)M;
+    const int tiles = (N + 127) / 128;
+    const int C = K / io->k_chunk;
+    double best = 1e30;
+    StreamConfig best_c = *io;
+    bool found = false;
+    for (int s = 1; s <= 16 && s <= C; ++s) {
+        if (force_split > 0 && s != force_split) continue;
+        StreamConfig c = *io;
+        c.split = s;
+        c.clusters = 1;
+        c.stages = force_stages > 0 ? force_stages : stream_fill_stages(c, K, G, 12);
+        if (c.stages < 2) continue;
+        int slots = have_device ? stream_max_clusters(c, G, K) : sm_count / s;
+        if (slots <= 0) continue;
+        c.clusters = force_clusters > 0 ? force_clusters : std::min(slots, tiles);
+        const int per_cluster = (tiles + c.clusters - 1) / c.clusters;
+        const int per_cta = (C + s - 1) / s;
+        // weight bytes in flight per CTA: below ~96 KB the stream slows down (measured on GB300)
+        const double ring = static_cast<double>(c.stages) * io->k_chunk * 64.0;
+        const double eff = std::min(1.0, ring / 98304.0);
+        const double cost =
+            static_cast<double>(per_cluster) * (per_cta * (io->k_chunk / 256.0) + 0.3) / eff + 0.05 * s;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_c = c;
+            found = true;
+        }
+    }
+    if (found) *io = best_c;
+    return found;
+}
+
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
                           Choice* out);
 
@@ -172,7 +247,7 @@ std::map<std::tuple<int, int, int, int, int>, Choice> g_plan_cache;
 int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, Choice* out) {
     const bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
                                                plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
-                                               plan->mma_issuers == 0);
+                                               plan->mma_issuers == 0 && plan->clusters == 0);
     if (!automatic || !have_device) return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
     int dev = 0;
     cudaGetDevice(&dev);
@@ -197,12 +272,33 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
                           Choice* out) {
     w4a16_plan p = {};
     if (plan) p = *plan;
-    if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
+    if (p.path < 0 || p.path > 3) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
-    // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one or two
-    // activation rows (no barriers, no TMEM round trip); from 4 rows on the tcgen05 path wins.
-    if (path == W4A16_PATH_AUTO) path = M <= 2 ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+    if (path == W4A16_PATH_AUTO) {
+        // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one or
+        // two activation rows; from 3 rows on the tcgen05 tiles. (The persistent streaming kernel is
+        // still slower than the tiles on every measured decode / verify shape and is only run when a
+        // plan asks for it.)
+        path = M <= 2 ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+    }
     out->path = path;
+    if (path == W4A16_PATH_STREAM) {
+        if (M > 64) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        StreamConfig c;
+        c.m_tile = p.m_tile > 0 ? p.m_tile : stream_m_tile(M);
+        c.k_chunk = p.k_chunk > 0 ? p.k_chunk : (K % 256 == 0 && group_fits(256, G) ? 256 : 128);
+        c.issuers = p.mma_issuers > 0 ? p.mma_issuers : stream_default_issuers(c.m_tile);
+        if (!stream_instantiated(c.m_tile, c.k_chunk, c.issuers)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        stream_tmem_layout(&c, p.tmem_stages);
+        c.stages = 2;
+        c.split = 1;
+        c.clusters = 1;
+        if (!stream_pick(&c, M, N, K, G, sm_count, have_device, p.split_k, p.stages, p.clusters))
+            return W4A16_ERR_UNSUPPORTED_SHAPE;
+        if (!stream_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        out->st = c;
+        return W4A16_OK;
+    }
     if (path == W4A16_PATH_GEMV) {
         if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
         int split = p.split_k > 0 ? p.split_k : gemv_pick_split(M, N, K, sm_count);
@@ -311,9 +407,18 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     const int rc = resolve_plan(M, N, K, group, nullptr, sms, dev, &ch);
     if (rc != W4A16_OK) return rc;
     out->path = ch.path;
+    out->clusters = 0;
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
         out->m_tile = out->k_chunk = out->stages = out->tmem_stages = out->mma_issuers = 0;
+    } else if (ch.path == W4A16_PATH_STREAM) {
+        out->split_k = ch.st.split;
+        out->m_tile = ch.st.m_tile;
+        out->k_chunk = ch.st.k_chunk;
+        out->stages = ch.st.stages;
+        out->tmem_stages = ch.st.tmem_stages;
+        out->mma_issuers = ch.st.issuers;
+        out->clusters = ch.st.clusters;
     } else {
         out->split_k = ch.tc.split;
         out->m_tile = ch.tc.m_tile;
@@ -356,6 +461,15 @@ int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r
                         group, ch.gemv_split, ctx);
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%d,%d,1) block=128", M, N, K,
                  group, ch.gemv_split, ch.gemv_split, N / 32);
+    } else if (ch.path == W4A16_PATH_STREAM) {
+        e = launch_stream(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
+                          K, group, ch.st, ctx);
+        snprintf(desc, sizeof(desc),
+                 "path=stream M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
+                 "acc_buffers=%d split_k=%d clusters=%d grid=(%d,%d,1) tmem_cols=%d smem=%zu",
+                 M, N, K, group, ch.st.m_tile, ch.st.k_chunk, ch.st.stages, ch.st.tmem_stages, ch.st.issuers,
+                 ch.st.dbuf, ch.st.split, ch.st.clusters, ch.st.split, ch.st.clusters, stream_tmem_columns(ch.st),
+                 stream_smem_bytes(ch.st, group, K));
     } else {
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
