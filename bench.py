@@ -67,6 +67,34 @@ def bound_tokens_per_s(bandwidth_bytes_s: float, bytes_per_token: float) -> floa
     return bandwidth_bytes_s / bytes_per_token
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each workload's dominant
+# kernel from one ncu capture (summaries under profiles/), with the SHA-256 prefix of the kernel
+# sources it was taken from: a figure is reported only while those sources are unchanged.
+MEASURED_TRAFFIC = {
+    "path=gemv M=1 N=5120 K=17408 ": (46_025_728, ("gemv.cu", "common.cuh"), "e1ec87a3eef619bf",
+                                      "profiles/gemv_decode_m1_17408x5120.md"),
+    "path=tc M=16 N=34816 K=5120 ": (94_774_272, ("tc_gemm.cu", "common.cuh"), "cf7b2695b6eca078",
+                                     "profiles/tc_gemm_verify_m16_5120x34816.md"),
+    "path=tc M=256 N=34816 K=5120 ": (97_609_728, ("tc_gemm.cu", "common.cuh"), "cf7b2695b6eca078",
+                                      "profiles/tc_gemm_batched_m256_5120x34816.md"),
+}
+
+
+def measured_traffic(plan: str):
+    """(bytes per launch, summary file) if a capture of this launch's current kernel exists."""
+    import hashlib
+    for prefix, (nbytes, files, digest, summary) in MEASURED_TRAFFIC.items():
+        if not plan.startswith(prefix):
+            continue
+        m = hashlib.sha256()
+        for f in files:
+            with open(os.path.join(ROOT, "w4a16_weight_streaming_gb300", "csrc", f), "rb") as fh:
+                m.update(fh.read())
+        if m.hexdigest()[:16] == digest:
+            return nbytes, summary
+    return None, None
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -379,7 +407,7 @@ def main():
     else:
         roof = {"bound": "tensor", "achieved": fl / t_k / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"], roof["traffic_source"] = measured_traffic(plans[j])
     roof["kernel"] = plans[j]
     roof["us_per_launch"] = kernel_ms[j] * 1e3
     roof["algorithmic_bytes"] = alg
