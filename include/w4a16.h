@@ -53,7 +53,8 @@ typedef enum {
     W4A16_PATH_AUTO = 0, /* the dispatcher decides from (M, N, K) */
     W4A16_PATH_GEMV = 1,  /* CUDA-core split-K GEMV, M <= 8 */
     W4A16_PATH_TC = 2,    /* tcgen05 tensor-core tiles, any M */
-    W4A16_PATH_STREAM = 3 /* persistent tcgen05 streaming kernel, M <= 64 (x resident on chip) */
+    W4A16_PATH_STREAM = 3, /* persistent tcgen05 streaming kernel, M <= 64 (x resident on chip) */
+    W4A16_PATH_GEMV_TMA = 4 /* CUDA-core GEMV fed by TMA through a shared-memory ring, M <= 4 */
 } w4a16_path;
 
 /* A launch plan. Zero fields mean "choose automatically". */
@@ -61,8 +62,8 @@ typedef struct {
     int path;        /* w4a16_path */
     int split_k;     /* CTAs of one thread-block cluster splitting K (1..16) */
     int m_tile;      /* TC, STREAM: activation rows per tile: 16, 32, 64 (STREAM), 128, 256 (TC) */
-    int k_chunk;     /* TC, STREAM: K per pipeline stage, 128 or 256 */
-    int stages;      /* TC, STREAM: shared-memory pipeline depth, 2..16 */
+    int k_chunk;     /* TC, STREAM, GEMV_TMA: K per pipeline stage, 128 or 256 */
+    int stages;      /* TC, STREAM, GEMV_TMA: shared-memory pipeline depth, 2..16 */
     int tmem_stages; /* TC, STREAM: tensor-memory (dequantised A) pipeline depth, 2..8 */
     int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
     int clusters;    /* STREAM: persistent thread-block clusters (each walks every clusters-th tile) */

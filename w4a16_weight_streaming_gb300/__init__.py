@@ -30,6 +30,7 @@ PATH_AUTO = 0
 PATH_GEMV = 1
 PATH_TC = 2
 PATH_STREAM = 3
+PATH_GEMV_TMA = 4
 
 # every symbol include/w4a16.h declares
 EXPORTED = [

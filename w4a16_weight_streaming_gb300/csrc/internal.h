@@ -29,6 +29,13 @@ size_t gemv_smem_bytes(int M, int N, int K, int split);
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                         int N, int K, int G, int split, const LaunchCtx& ctx);
 
+// ---- gemv_tma.cu: TMA-fed CUDA-core GEMV, M <= 4 (k_chunk 128 or 256 rows of k per stage).
+constexpr int kGemvTmaMaxM = 4;
+size_t gemv_tma_smem_bytes(int M, int K, int G, int KC, int split, int stages);
+int gemv_tma_resident_ctas(int M, int N, int K, int G, int KC, int split, int stages);
+cudaError_t launch_gemv_tma(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
+                            int M, int N, int K, int G, int KC, int split, int stages, const LaunchCtx& ctx);
+
 // ---- tc_gemm.cu: the x operand's tensor map (shared by both tensor-core kernels). x viewed as
 // [K/64 blocks][M rows][64 k]; one box = one stage tile [KC/64][MT][64] in the MMA's 128-byte-swizzle
 // K-major layout; rows >= M read as zero. Falls back to a 2-D map when the driver refuses the 3-D one.

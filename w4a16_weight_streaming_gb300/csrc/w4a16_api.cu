@@ -86,6 +86,7 @@ struct Choice {
     TcConfig tc;
     StreamConfig st;
     int gemv_split;
+    int gt_kc, gt_stages;  // GEMV_TMA: stage K and ring depth (split in gemv_split)
 };
 
 // Split along K for the CUDA-core GEMV: enough 128-thread CTAs to cover every SM about four
@@ -237,6 +238,31 @@ bool stream_pick(StreamConfig* io, int M, int N, int K, int G, int sm_count, boo
     return found;
 }
 
+// ---- TMA-fed GEMV: K-slices per tile from the cluster occupancy (waves x stages per CTA).
+int gemv_tma_pick_split(int M, int N, int K, int G, int KC, int stages, int sm_count, bool have_device,
+                        int force_split) {
+    const int tiles = (N + 127) / 128;
+    const int R = KC / 32;
+    const int C = (K / 32 + R - 1) / R;
+    double best = 1e30;
+    int split = 0;
+    for (int s = 1; s <= 16 && s <= C; ++s) {
+        if (force_split > 0 && s != force_split) continue;
+        if (gemv_tma_smem_bytes(M, K, G, KC, s, stages) > 225 * 1024) continue;
+        int slots = have_device ? gemv_tma_resident_ctas(M, N, K, G, KC, s, stages) : 0;
+        if (slots <= 0) slots = have_device ? 0 : (2 * sm_count / s) * s;
+        if (slots <= 0) continue;
+        const int waves = (tiles * s + slots - 1) / slots;
+        const int per_cta = (C + s - 1) / s;
+        const double cost = static_cast<double>(waves) * (per_cta + 1.5) + 0.1 * s;
+        if (cost < best - 1e-9) {
+            best = cost;
+            split = s;
+        }
+    }
+    return split;
+}
+
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
                           Choice* out);
 
@@ -272,7 +298,7 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
                           Choice* out) {
     w4a16_plan p = {};
     if (plan) p = *plan;
-    if (p.path < 0 || p.path > 3) return W4A16_ERR_INVALID_ARG;
+    if (p.path < 0 || p.path > 4) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
     if (path == W4A16_PATH_AUTO) {
         // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one or
@@ -282,6 +308,19 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         path = M <= 2 ? W4A16_PATH_GEMV : W4A16_PATH_TC;
     }
     out->path = path;
+    if (path == W4A16_PATH_GEMV_TMA) {
+        if (M > kGemvTmaMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        const int kc = p.k_chunk > 0 ? p.k_chunk : 256;
+        const int stages = p.stages > 0 ? p.stages : 4;
+        if (kc != 128 && kc != 256) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        if (stages < 2 || stages > 16) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        const int split = gemv_tma_pick_split(M, N, K, G, kc, stages, sm_count, have_device, p.split_k);
+        if (split < 1) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        out->gemv_split = split;
+        out->gt_kc = kc;
+        out->gt_stages = stages;
+        return W4A16_OK;
+    }
     if (path == W4A16_PATH_STREAM) {
         if (M > 64) return W4A16_ERR_UNSUPPORTED_SHAPE;
         StreamConfig c;
@@ -411,6 +450,11 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
         out->m_tile = out->k_chunk = out->stages = out->tmem_stages = out->mma_issuers = 0;
+    } else if (ch.path == W4A16_PATH_GEMV_TMA) {
+        out->split_k = ch.gemv_split;
+        out->k_chunk = ch.gt_kc;
+        out->stages = ch.gt_stages;
+        out->m_tile = out->tmem_stages = out->mma_issuers = 0;
     } else if (ch.path == W4A16_PATH_STREAM) {
         out->split_k = ch.st.split;
         out->m_tile = ch.st.m_tile;
@@ -461,6 +505,14 @@ int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r
                         group, ch.gemv_split, ctx);
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%d,%d,1) block=128", M, N, K,
                  group, ch.gemv_split, ch.gemv_split, N / 32);
+    } else if (ch.path == W4A16_PATH_GEMV_TMA) {
+        e = launch_gemv_tma(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
+                            K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages, ctx);
+        snprintf(desc, sizeof(desc),
+                 "path=gemv_tma M=%d N=%d K=%d group=%d k_chunk=%d stages=%d split_k=%d grid=(%d,%d,1) block=288 "
+                 "smem=%zu",
+                 M, N, K, group, ch.gt_kc, ch.gt_stages, ch.gemv_split, ch.gemv_split, (N + 127) / 128,
+                 gemv_tma_smem_bytes(M, K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages));
     } else if (ch.path == W4A16_PATH_STREAM) {
         e = launch_stream(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
                           K, group, ch.st, ctx);
