@@ -139,6 +139,18 @@ int w4a16_device_status(void* stream);
  * Host-side setting applied to launches made after the call. */
 int w4a16_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * Exercises the failure-reporting path without a fault: launches (asynchronously, on `stream`) a
+ * one-warp kernel whose bounded wait can never complete (an mbarrier phase nothing arrives on),
+ * using the kernels' own wait routine: mode 0 = the suspending wait, mode 1 = the polling wait.
+ * The wait gives up after the current wait limit (w4a16_set_wait_timeout_ns), so a following
+ * w4a16_device_status(stream) returns W4A16_ERR_DEVICE_TIMEOUT and clears it; the CUDA context
+ * stays usable. (The pages' engine died of an allocation failure inside its GEMM: this library
+ * reports failures as status codes instead.) Allocates nothing.
+ * Errors: INVALID_ARG (mode not 0 or 1), CUDA (launch refused).
+ */
+int w4a16_selftest_wait_timeout(int mode, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -104,3 +104,9 @@ def test_plan_for_host_only(W):
 def test_wait_timeout_setting(W):
     assert W.w4a16_set_wait_timeout_ns(10) == 1
     assert W.w4a16_set_wait_timeout_ns(2_000_000_000) == 0
+
+
+def test_selftest_rejects_bad_mode(W):
+    # host-side check before any launch
+    assert W.w4a16_selftest_wait_timeout(2) == 1
+    assert W.w4a16_selftest_wait_timeout(-1) == 1

@@ -36,7 +36,7 @@ PATH_GEMV_TMA = 4
 EXPORTED = [
     "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
     "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
-    "w4a16_device_status", "w4a16_set_wait_timeout_ns",
+    "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout",
 ]
 
 
@@ -83,6 +83,8 @@ def _load() -> ctypes.CDLL:
     lib.w4a16_device_status.argtypes = [P]
     lib.w4a16_set_wait_timeout_ns.restype = I
     lib.w4a16_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.w4a16_selftest_wait_timeout.restype = I
+    lib.w4a16_selftest_wait_timeout.argtypes = [I, P]
     return lib
 
 
@@ -147,6 +149,11 @@ def w4a16_device_status(stream: int | None = None) -> int:
 
 def w4a16_set_wait_timeout_ns(ns: int) -> int:
     return lib.w4a16_set_wait_timeout_ns(int(ns))
+
+
+def w4a16_selftest_wait_timeout(mode: int, stream: int | None = None) -> int:
+    """Raw C ABI: `stream` is a cudaStream_t handle (None = the legacy default stream)."""
+    return lib.w4a16_selftest_wait_timeout(int(mode), stream)
 
 
 # ------------------------------------------------------------------------------ torch conveniences

@@ -180,6 +180,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return ok != 0;
 }
 
+// Warp-wide bounded wait that never suspends: lane 0 polls with test_wait (a thread suspended in
+// try_wait wakes up hundreds to thousands of cycles after the phase completes), then every lane
+// takes the acquire of the completed phase. Returns the same verdict in all lanes.
+__device__ __forceinline__ bool warp_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t timeout_ns,
+                                          unsigned* status) {
+    int ok = 1;
+    if ((threadIdx.x & 31u) == 0u) ok = mbar_spin(bar, parity, abort_flag, timeout_ns, status) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_test_wait(bar, parity);
+    return ok != 0;
+}
+
 // ------------------------------------------------------------------------------------ shared memory
 // Explicit shared-space loads by 32-bit shared address (a generic pointer into dynamic shared
 // memory is not always recognised as shared and would take the generic load path).

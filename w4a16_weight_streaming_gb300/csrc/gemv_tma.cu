@@ -55,16 +55,6 @@ __host__ __device__ inline GtSmem gt_plan(int MR, int KC, int G, int stages, int
     return p;
 }
 
-// Warp-wide bounded wait that never suspends: lane 0 polls test_wait, every lane then acquires.
-__device__ __forceinline__ bool gt_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             uint64_t timeout_ns, unsigned* status) {
-    int ok = 1;
-    if ((threadIdx.x & 31u) == 0u) ok = mbar_spin(bar, parity, abort_flag, timeout_ns, status) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_test_wait(bar, parity);
-    return ok != 0;
-}
-
 template <int MR, int KC>
 __global__ void __launch_bounds__(kThreads) gemv_tma_kernel(const uint16_t* __restrict__ x,
                                                             const uint4* __restrict__ wr,
@@ -167,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tma_kernel(const uint16_t* __re
         uint32_t ph = 0;
         bool ok = true;
         for (int c = c_begin; c < c_end; ++c) {
-            if (ok) ok = gt_warp_wait(full_bar(s), ph, abort_flag, timeout_ns, status);
+            if (ok) ok = warp_spin(full_bar(s), ph, abort_flag, timeout_ns, status);
             const int b0 = c * kR, b1 = min(KB, b0 + kR);
             const int g0 = b0 / gb;
             if (ok && valid) {

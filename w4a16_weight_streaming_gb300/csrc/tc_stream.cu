@@ -103,17 +103,6 @@ __device__ __forceinline__ void tma_load_x_3d_s(uint32_t dst, const void* tmap, 
         : "memory");
 }
 
-// Warp-wide bounded wait that never suspends: lane 0 polls with test_wait, then every lane takes
-// the acquire of the completed phase. Returns the same verdict in all lanes.
-__device__ __forceinline__ bool warp_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t timeout_ns, unsigned* status) {
-    int ok = 1;
-    if ((threadIdx.x & 31u) == 0u) ok = mbar_spin(bar, parity, abort_flag, timeout_ns, status) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_test_wait(bar, parity);
-    return ok != 0;
-}
-
 // Barrier over the four epilogue warps (named barrier 15) that also ANDs a predicate across them.
 __device__ __forceinline__ bool epi_sync_and(bool pred) {
     uint32_t r;

@@ -10,6 +10,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "common.cuh"
 #include "internal.h"
 #include "w4a16.h"
 
@@ -371,6 +372,34 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
 }  // namespace
 }  // namespace w4a16
 
+namespace w4a16 {
+namespace {
+
+// A one-warp kernel whose bounded wait can never complete: nothing arrives on its mbarrier. The
+// wait gives up after `timeout_ns`, records kErrTimeout in the status word and the kernel returns.
+// mode 0: the suspending wait (mbar_wait); mode 1: the polling wait (mbar_spin).
+__global__ void wait_timeout_selftest_kernel(unsigned* status, uint64_t timeout_ns, int mode) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) {
+        if (mode == 0)
+            mbar_wait(b, 0, &abort_flag, timeout_ns, status);
+        else
+            mbar_spin(b, 0, &abort_flag, timeout_ns, status);
+    }
+    __syncwarp();
+}
+
+}  // namespace
+}  // namespace w4a16
+
 using namespace w4a16;
 
 extern "C" {
@@ -567,6 +596,15 @@ int w4a16_device_status(void* stream) {
         if (cudaMemcpy(d.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return W4A16_ERR_CUDA;
     }
     return v == 0 ? W4A16_OK : static_cast<int>(v);
+}
+
+int w4a16_selftest_wait_timeout(int mode, void* stream) {
+    if (mode != 0 && mode != 1) return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d.status, g_timeout_ns.load(), mode);
+    if (cudaGetLastError() != cudaSuccess) return W4A16_ERR_CUDA;
+    return W4A16_OK;
 }
 
 int w4a16_set_wait_timeout_ns(uint64_t ns) {
