@@ -67,6 +67,7 @@ typedef struct {
     int tmem_stages; /* TC, STREAM: tensor-memory (dequantised A) pipeline depth, 2..8 */
     int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
     int clusters;    /* STREAM: persistent thread-block clusters (each walks every clusters-th tile) */
+    int dequant_warps; /* TC: 16, or 8 (m_tile <= 64, k_chunk 128: half-size CTAs, two per SM) */
 } w4a16_plan;
 
 /* Library version: major*10000 + minor*100 + patch. */

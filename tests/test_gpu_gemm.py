@@ -241,3 +241,20 @@ def test_layer_sweep_all_rows(W):
 
 def test_status_word_clean(W):
     assert W.w4a16_device_status() == W.OK
+
+
+# the half-size tile kernels (8 dequant warps, two CTAs per SM)
+@pytest.mark.parametrize("mt,ni", [(16, 4), (32, 4), (64, 2)])
+def test_half_size_tiles(W, mt, ni):
+    M, K, N, G = mt - 3, 1280, 352, 128  # ragged last column tile (96 wide), 10 chunks of 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=70 + mt)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    for split in (1, 3):
+        for ts in (2, 3):
+            if ts * 64 + ni * mt > 256:
+                continue
+            plan = dict(path=2, m_tile=mt, k_chunk=128, split_k=split, tmem_stages=ts, mma_issuers=ni,
+                        dequant_warps=8)
+            y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+            assert "dequant_warps=8" in W.w4a16_last_dispatch()
+            assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())

@@ -49,8 +49,9 @@ struct TcConfig {
     int split;        // CTAs per cluster along K, 1..16
     int tmem_stages;  // TMEM A ring depth, 2..8
     int issuers;      // MMA-issuing threads (1, 2 or 4), each with its own accumulator
+    int dequant_warps;  // 16, or 8 (small tiles that fit two CTAs per SM)
 };
-bool tc_instantiated(int m_tile, int k_chunk, int issuers);
+bool tc_instantiated(int m_tile, int k_chunk, int issuers, int dequant_warps);
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G);
 size_t tc_smem_bytes(const TcConfig& c, int G);
 int tc_tmem_cols(const TcConfig& c);

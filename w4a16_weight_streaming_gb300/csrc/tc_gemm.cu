@@ -46,12 +46,10 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kDequantWarps = 16;  // 4 lane quadrants x 4 K parts
-constexpr int kProducerWarp = 16;  // also the TMEM allocator
-constexpr int kIssuerWarp0 = 17;   // first dedicated MMA issuer (dedicated scheme)
-constexpr int kMaxThreads = 32 * (kDequantWarps + 1 + 4);
-__host__ __device__ constexpr int threads_for(bool group_issue, int na) {
-    return 32 * (kDequantWarps + 1 + (group_issue ? 0 : na));
+// DW dequant warps = 4 lane quadrants x DW/4 K parts (16, or 8 for the two-CTAs-per-SM variant);
+// warp DW is the TMA producer and TMEM allocator, warps DW+1.. the dedicated MMA issuers.
+__host__ __device__ constexpr int threads_for(bool group_issue, int na, int dw) {
+    return 32 * (dw + 1 + (group_issue ? 0 : na));
 }
 constexpr int kTileN = 128;  // output columns per CTA (= TMEM lanes)
 
@@ -130,8 +128,8 @@ __device__ __forceinline__ bool group_sync_and(int id, int nthreads, bool pred) 
     return r != 0u;
 }
 
-template <int MT, int KC, int NA, bool GROUP_ISSUE>
-__global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
+template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW>
+__global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
                    int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
@@ -139,11 +137,18 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
     static_assert(NA == 1 || NA == 2 || NA == 4, "1, 2 or 4 accumulators");
     constexpr int kKB = KC / 32;                   // 32-k blocks per stage
-    constexpr int kPartKB = kKB / 4;               // 32-k blocks per dequant warp per stage (1 or 2)
+    constexpr int kDequantWarps = DW;
+    constexpr int kProducerWarp = DW;              // also the TMEM allocator
+    constexpr int kIssuerWarp0 = DW + 1;           // first dedicated MMA issuer (dedicated scheme)
+    constexpr int kParts = DW / 4;                 // K parts of a stage
+    static_assert(DW == 8 || DW == 16, "8 or 16 dequant warps");
+    static_assert(kKB % kParts == 0, "stage rows split evenly over the K parts");
+    constexpr int kPartKB = kKB / kParts;          // 32-k blocks per dequant warp per stage (1 or 2)
+    static_assert(kPartKB == 1 || kPartKB == 2, "1 or 2 blocks per warp per stage");
     constexpr int kACols = KC / 2;                 // TMEM columns of one A stage (fp16 pairs)
     constexpr int kGroupWarps = kDequantWarps / NA;  // warps feeding one accumulator
     constexpr int kGroupSteps = KC / 16 / NA;        // k-steps of 16 per accumulator per stage
-    constexpr int kThreads = threads_for(GROUP_ISSUE, NA);
+    constexpr int kThreads = threads_for(GROUP_ISSUE, NA, DW);
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -373,12 +378,13 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA), 1)
         const bool have_d = warp_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
         tc_fence_after();
         if (have_d) {
-            constexpr int kCols = MT / 4 < 8 ? MT / 4 : 8;  // columns per TMEM load
-            const int mbase = part * (MT / 4);
+            constexpr int kPartCols = MT / kParts;  // accumulator columns (activation rows) per K part
+            constexpr int kCols = kPartCols < 8 ? kPartCols : 8;  // columns per TMEM load
+            const int mbase = part * kPartCols;
             float* red = reinterpret_cast<float*>(smem + P.red_off);
             const int n = n0 + 32 * q + lane;
 #pragma unroll 1
-            for (int c = 0; c < MT / 4; c += kCols) {
+            for (int c = 0; c < kPartCols; c += kCols) {
                 uint32_t r[kCols];
                 tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
                 tmem_wait_ld();
@@ -468,12 +474,12 @@ cudaError_t prepare_kernel(Kern kern, size_t smem, int split) {
     return e;
 }
 
-template <int MT, int KC, int NI, bool GI>
+template <int MT, int KC, int NI, bool GI, int DW>
 cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.split, (N + kTileN - 1) / kTileN, (M + MT - 1) / MT);
-    cfg.blockDim = dim3(threads_for(GI, NI), 1, 1);
+    cfg.blockDim = dim3(threads_for(GI, NI, DW), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -485,23 +491,23 @@ cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cud
     return cfg;
 }
 
-template <int MT, int KC, int NI, bool GI>
+template <int MT, int KC, int NI, bool GI, int DW>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
                         uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    auto kern = tc_gemm_kernel<MT, KC, NI, GI>;
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW>;
     const size_t smem = launch_smem(MT, KC, G, c);
     cudaError_t e = prepare_kernel(kern, smem, c.split);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI>(c, M, N, smem, ctx.stream, attr);
+    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(c, M, N, smem, ctx.stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
                               c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
 }
 
 // CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.
-template <int MT, int KC, int NI, bool GI>
+template <int MT, int KC, int NI, bool GI, int DW>
 int resident_ctas_t(const TcConfig& c, int G) {
-    auto kern = tc_gemm_kernel<MT, KC, NI, GI>;
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW>;
     const size_t smem = launch_smem(MT, KC, G, c);
     if (prepare_kernel(kern, smem, c.split) != cudaSuccess) {
         cudaGetLastError();
@@ -509,7 +515,7 @@ int resident_ctas_t(const TcConfig& c, int G) {
     }
     cudaLaunchAttribute attr[1];
     TcConfig one = c;
-    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI>(one, 1, kTileN, smem, nullptr, attr);
+    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(one, 1, kTileN, smem, nullptr, attr);
     cfg.gridDim = dim3(c.split, 1, 1);
     cfg.numAttrs = 1;  // query with the cluster shape even for split 1
     int clusters = 0;
@@ -563,11 +569,18 @@ bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tc_instantiated(int m_tile, int k_chunk, int issuers) {
-    static const int kCombos[][3] = {{16, 128, 4}, {16, 256, 4}, {32, 128, 4},  {32, 256, 4},  {64, 128, 4},
-                                     {64, 256, 4}, {64, 256, 2}, {128, 128, 2}, {128, 128, 1}, {256, 128, 1}};
-    for (const auto& t : kCombos)
-        if (t[0] == m_tile && t[1] == k_chunk && t[2] == issuers) return true;
+// (m_tile, k_chunk, issuers, group issue, dequant warps) of every instantiated kernel.
+#define W4A16_TC_COMBOS(X)                                                                              \
+    X(16, 128, 4, false, 16) X(16, 256, 4, false, 16) X(32, 128, 4, false, 16) X(32, 256, 4, false, 16) \
+    X(64, 128, 4, false, 16) X(64, 256, 4, false, 16) X(64, 256, 2, true, 16) X(128, 128, 2, true, 16)   \
+    X(128, 128, 1, true, 16) X(256, 128, 1, true, 16) X(16, 128, 4, false, 8) X(32, 128, 4, false, 8)     \
+    X(64, 128, 2, false, 8)
+
+bool tc_instantiated(int m_tile, int k_chunk, int issuers, int dequant_warps) {
+#define W4A16_TC_IS(MT_, KC_, NI_, GI_, DW_) \
+    if (m_tile == MT_ && k_chunk == KC_ && issuers == NI_ && dequant_warps == DW_) return true;
+    W4A16_TC_COMBOS(W4A16_TC_IS)
+#undef W4A16_TC_IS
     return false;
 }
 
@@ -580,7 +593,7 @@ bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
     if (c.stages < 2 || c.stages > 16) return false;
     if (c.tmem_stages < 2 || c.tmem_stages > 8) return false;
     if (c.split < 1 || c.split > 16 || c.split > K / c.k_chunk) return false;
-    if (!tc_instantiated(c.m_tile, c.k_chunk, c.issuers)) return false;
+    if (!tc_instantiated(c.m_tile, c.k_chunk, c.issuers, c.dequant_warps)) return false;
     if (tmem_cols_needed(c.m_tile, c.k_chunk, c.tmem_stages, c.issuers) > 512) return false;
     if (c.k_chunk < G && G % c.k_chunk != 0) return false;
     if (c.k_chunk >= G && c.k_chunk % G != 0) return false;
@@ -598,18 +611,10 @@ int tc_tmem_cols(const TcConfig& c) {
 }
 
 int tc_resident_ctas(const TcConfig& c, int G) {
-#define W4A16_TC_RES(MT_, KC_, NI_, GI_) \
-    if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_) return resident_ctas_t<MT_, KC_, NI_, GI_>(c, G);
-    W4A16_TC_RES(16, 128, 4, false)
-    W4A16_TC_RES(16, 256, 4, false)
-    W4A16_TC_RES(32, 128, 4, false)
-    W4A16_TC_RES(32, 256, 4, false)
-    W4A16_TC_RES(64, 128, 4, false)
-    W4A16_TC_RES(64, 256, 4, false)
-    W4A16_TC_RES(64, 256, 2, true)
-    W4A16_TC_RES(128, 128, 2, true)
-    W4A16_TC_RES(128, 128, 1, true)
-    W4A16_TC_RES(256, 128, 1, true)
+#define W4A16_TC_RES(MT_, KC_, NI_, GI_, DW_)                                                           \
+    if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_ && c.dequant_warps == DW_) \
+        return resident_ctas_t<MT_, KC_, NI_, GI_, DW_>(c, G);
+    W4A16_TC_COMBOS(W4A16_TC_RES)
 #undef W4A16_TC_RES
     return 0;
 }
@@ -619,19 +624,10 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16
     CUtensorMap tmap;
     bool three_d = false;
     if (!encode_x_map(&tmap, x, M, K, c.m_tile, c.k_chunk, &three_d)) return cudaErrorInvalidValue;
-#define W4A16_TC_CASE(MT_, KC_, NI_, GI_)                                                                     \
-    if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_)                                              \
-        return launch_tc_t<MT_, KC_, NI_, GI_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
-    W4A16_TC_CASE(16, 128, 4, false)
-    W4A16_TC_CASE(16, 256, 4, false)
-    W4A16_TC_CASE(32, 128, 4, false)
-    W4A16_TC_CASE(32, 256, 4, false)
-    W4A16_TC_CASE(64, 128, 4, false)
-    W4A16_TC_CASE(64, 256, 4, false)
-    W4A16_TC_CASE(64, 256, 2, true)
-    W4A16_TC_CASE(128, 128, 2, true)
-    W4A16_TC_CASE(128, 128, 1, true)
-    W4A16_TC_CASE(256, 128, 1, true)
+#define W4A16_TC_CASE(MT_, KC_, NI_, GI_, DW_)                                                          \
+    if (c.m_tile == MT_ && c.k_chunk == KC_ && c.issuers == NI_ && c.dequant_warps == DW_)               \
+        return launch_tc_t<MT_, KC_, NI_, GI_, DW_>(tmap, three_d, qweight_r, scales_r, y, M, N, K, G, c, ctx);
+    W4A16_TC_COMBOS(W4A16_TC_CASE)
 #undef W4A16_TC_CASE
     return cudaErrorInvalidValue;
 }
