@@ -71,11 +71,11 @@ def bound_tokens_per_s(bandwidth_bytes_s: float, bytes_per_token: float) -> floa
 # kernel from one ncu capture (summaries under profiles/), with the SHA-256 prefix of the kernel
 # sources it was taken from: a figure is reported only while those sources are unchanged.
 MEASURED_TRAFFIC = {
-    "path=gemv M=1 N=5120 K=17408 ": (46_025_728, ("gemv.cu", "common.cuh"), "e1ec87a3eef619bf",
+    "path=gemv M=1 N=5120 K=17408 ": (46_027_008, ("gemv.cu", "common.cuh"), "7f97cbde400939bb",
                                       "profiles/gemv_decode_m1_17408x5120.md"),
-    "path=tc M=16 N=34816 K=5120 ": (94_774_272, ("tc_gemm.cu", "common.cuh"), "cf7b2695b6eca078",
+    "path=tc M=16 N=34816 K=5120 ": (95_082_240, ("tc_gemm.cu", "common.cuh"), "e5db09846ea61779",
                                      "profiles/tc_gemm_verify_m16_5120x34816.md"),
-    "path=tc M=256 N=34816 K=5120 ": (97_609_728, ("tc_gemm.cu", "common.cuh"), "cf7b2695b6eca078",
+    "path=tc M=256 N=34816 K=5120 ": (97_315_840, ("tc_gemm.cu", "common.cuh"), "e5db09846ea61779",
                                       "profiles/tc_gemm_batched_m256_5120x34816.md"),
 }
 
