@@ -45,9 +45,9 @@ def test_rows_and_partial_stages(W, M, K):
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
-@pytest.mark.parametrize("G", [32, 128, 256, 384])
-def test_group_sizes(W, G):
-    M, K, N = 2, 1536, 256
+@pytest.mark.parametrize("G,K", [(32, 1536), (128, 1536), (256, 1536), (384, 1536), (96, 1920), (160, 1920)])
+def test_group_sizes(W, G, K):
+    M, N = 2, 256
     d = inputs.generate(M, K, N, G, seed=G)
     y_ref, abs_ref = oracle.gemm(d["x"], d["qweight"], d["scales"], G)
     x, qw_r, sc_r = _repacked(W, d, G)

@@ -37,8 +37,9 @@ struct GtSmem {
 };
 
 __host__ __device__ inline int gt_rows_per_stage(int KC) { return KC / 32; }
-// scale rows one stage can touch: its rows span at most this many groups
-__host__ __device__ inline int gt_groups_per_stage(int KC, int G) { return KC >= G ? KC / G + 1 : 2; }
+// scale rows one stage can touch: KC consecutive k starting anywhere inside a group span at most
+// (KC - 1) / G + 2 groups (G need not divide KC, e.g. G = 96)
+__host__ __device__ inline int gt_groups_per_stage(int KC, int G) { return (KC - 1) / G + 2; }
 
 __host__ __device__ inline GtSmem gt_plan(int MR, int KC, int G, int stages, int klen_max) {
     GtSmem p;
