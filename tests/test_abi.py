@@ -101,6 +101,17 @@ def test_plan_for_host_only(W):
         W.w4a16_plan_for(0, 5120, 5120, 128)
 
 
+def test_plan_for_group_sizes(W):
+    # groups that divide 128 or are multiples of it run on the tiles; others on the GEMV (M <= 8)
+    for G in (32, 64, 128, 256, 384):
+        assert W.w4a16_plan_for(16, 256, 1536, G).path == W.PATH_TC
+    for G in (96, 160):
+        for M in (1, 3, 8):
+            assert W.w4a16_plan_for(M, 256, 1920, G).path == W.PATH_GEMV
+        with pytest.raises(W.W4A16Error):
+            W.w4a16_plan_for(9, 256, 1920, G)
+
+
 def test_wait_timeout_setting(W):
     assert W.w4a16_set_wait_timeout_ns(10) == 1
     assert W.w4a16_set_wait_timeout_ns(2_000_000_000) == 0

@@ -132,6 +132,18 @@ def test_group_sizes(W, G):
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
+@pytest.mark.parametrize("G", [96, 160])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_groups_not_dividing_a_stage(W, G, M):
+    # automatic plans send these to the GEMV, which reads one scale per 32-k row
+    K, N = 1920, 160
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=G + M)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    y = run_gemm(W, x, qw_r, sc_r, N, K, G)
+    assert "path=gemv" in W.w4a16_last_dispatch()
+    assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
 # ------------------------------------------------------------------------------ exact cases
 def test_one_hot_rows_are_exact(W):
     K, N, G = 512, 256, 128

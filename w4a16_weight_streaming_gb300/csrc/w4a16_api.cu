@@ -321,6 +321,9 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         // still slower than the tiles on every measured decode / verify shape and is only run when a
         // plan asks for it.)
         path = M <= 2 ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+        // The tile kernels stage whole scale groups per 128-k stage; a group that neither divides
+        // nor is a multiple of 128 (96, 160, ...) goes to the GEMV, which reads one per 32-k row.
+        if (path == W4A16_PATH_TC && !group_fits(128, G) && M <= kGemvMaxM) path = W4A16_PATH_GEMV;
     }
     out->path = path;
     if (path == W4A16_PATH_GEMV_TMA) {
