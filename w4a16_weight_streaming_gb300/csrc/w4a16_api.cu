@@ -143,10 +143,10 @@ int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, b
         const int ctas = tiles * s;
         const int waves = (ctas + slots - 1) / slots;
         const int per_cta = (C + s - 1) / s;
-        // In stages of the CTA's own K loop. 256-row tiles (one CTA per SM), fitted to GB300
-        // timings at M = 256..1024: ~0.71 us per 128-k stage, plus ~12 us per wave (prologue,
-        // ring fill, epilogue) and a cluster reduction that grows with the split.
-        const double cost = base.m_tile >= 256 ? static_cast<double>(waves) * (per_cta + 17.0 + s)
+        // In stages of the CTA's own K loop. 128- and 256-row tiles (one CTA per SM), fitted to
+        // GB300 timings at M = 128..1024: ~0.71 us per 128-k stage (256 rows), plus ~12 us per
+        // wave (prologue, ring fill, epilogue) and a cluster reduction that grows with the split.
+        const double cost = base.m_tile >= 128 ? static_cast<double>(waves) * (per_cta + 17.0 + s)
                                                : static_cast<double>(waves) * (per_cta + 2.0) + 0.25 * s;
         if (cost < best - 1e-9) {
             best = cost;
