@@ -320,11 +320,14 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
     if (p.path < 0 || p.path > 4) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
     if (path == W4A16_PATH_AUTO) {
-        // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one or
-        // two activation rows; from 3 rows on the tcgen05 tiles. (The persistent streaming kernel is
+        // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one
+        // activation row; from 3 rows on the tcgen05 tiles. (The persistent streaming kernel is
         // still slower than the tiles on every measured decode / verify shape and is only run when a
         // plan asks for it.)
-        path = M <= 2 ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+        // At two rows the GEMV wins only on the smaller matrices (5120 x 5120, 5120 x 7168); on
+        // 5120 x 34816 and 17408 x 5120 the tiles are 1-2 us faster.
+        const bool small = static_cast<int64_t>(K) * N < (int64_t{64} << 20);
+        path = (M == 1 || (M == 2 && small)) ? W4A16_PATH_GEMV : W4A16_PATH_TC;
         // The tile kernels stage whole scale groups per 128-k stage; a group that neither divides
         // nor is a multiple of 128 (96, 160, ...) goes to the GEMV, which reads one per 32-k row.
         if (path == W4A16_PATH_TC && !group_fits(128, G) && M <= kGemvMaxM) path = W4A16_PATH_GEMV;
