@@ -9,8 +9,8 @@ rate, weight bytes (0.5 B per weight + fp16 scales) / step time, beside TFLOP/s.
 Timing: W untimed warm-up steps; the K timed steps are one CUDA-graph replay bracketed by a
 barrier and torch.cuda.synchronize(), timed with CUDA events on the launching stream. Every
 step reads the next of R device copies of the weights (R x weight bytes > 4 x L2), so no step
-finds its weights in L2. `e2e` repeats the K steps through the Python/C API with host buffers:
-each step copies x from pinned host memory and reads y back.
+finds its weights in L2. `e2e` repeats the K steps through the C ABI with host buffers
+(w4a16_gemm_host): each step copies x from pinned host memory and reads y back.
 
 --impl reference times the CPU oracle (fp64, oracle/) on the same metric; under torchrun only
 rank 0 runs it. --workload selects another configuration (for profiles); --sweep prints the
@@ -413,15 +413,23 @@ def main():
     roof["algorithmic_bytes"] = alg
     roof["peak_source"] = peaks["source"] + (" (burst copy)" if roof["bound"] == "hbm" else " (bf16 burst; fp16 same rate)")
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the C ABI with host buffers: w4a16_gemm_host queues, per matrix, the
+    # copy of x from pinned host memory, the GEMM and the copy of y back to pinned host memory
     h2d = sum(bb["x"].numel() * 2 for bb in bufs)
     d2h = sum(bb["y"].numel() * 2 for bb in bufs)
+    stream = torch.cuda.current_stream().cuda_stream
+    calls = [[(bb["x_host"].data_ptr(), bb["x"].data_ptr(), qr.data_ptr(), sr.data_ptr(), bb["y"].data_ptr(),
+               bb["y_host"].data_ptr(), bb["M"], bb["N"], bb["K"], GROUP, stream) for (qr, sr) in bb["copies"]]
+             for bb in bufs]
+
+    def e2e_step(i: int):
+        for c in calls:
+            rc = W.w4a16_gemm_host(*c[i % R])
+            if rc != W.OK:
+                raise RuntimeError(f"w4a16_gemm_host: {W.status_string(rc)}")
+
     for i in range(3):
-        for bb in bufs:
-            bb["x"].copy_(bb["x_host"], non_blocking=True)
-            qr, sr = bb["copies"][i % R]
-            W.gemm(bb["x"], qr, sr, bb["N"], bb["K"], GROUP, y=bb["y"])
-            bb["y_host"].copy_(bb["y"], non_blocking=True)
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -429,11 +437,7 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(args.steps):
-        for bb in bufs:
-            bb["x"].copy_(bb["x_host"], non_blocking=True)
-            qr, sr = bb["copies"][i % R]
-            W.gemm(bb["x"], qr, sr, bb["N"], bb["K"], GROUP, y=bb["y"])
-            bb["y_host"].copy_(bb["y"], non_blocking=True)
+        e2e_step(i)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = dist_max(dist, e0.elapsed_time(e1), dev) / args.steps

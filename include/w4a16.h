@@ -123,6 +123,24 @@ int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, u
 int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                   int group, const w4a16_plan* plan, void* stream);
 
+/*
+ * w4a16_gemm for activations and results in HOST memory, queued on `stream` as three operations:
+ * copy x_host -> x_dev (M*K fp16), the GEMM into y_dev (automatic plan), copy y_dev -> y_host
+ * (M*N fp16). The step of the paths above that a serving loop runs each decode step, with its
+ * host<->device copies; one call instead of three keeps the host cost of a step low.
+ *   x_host, y_host: host buffers (pinned, for the copies to be asynchronous), caller-owned; they
+ *                   must not overlap. y_host is valid once `stream` has been synchronised.
+ *   x_dev, y_dev:   caller-owned device buffers of M*K and M*N fp16 (16-byte aligned); the
+ *                   library allocates nothing.
+ *   qweight_r, scales_r, M, N, K, group, stream: as w4a16_gemm.
+ * Every check of w4a16_gemm (on x_dev, y_dev and the weights) runs before anything is queued, and
+ * x_host / y_host are rejected (INVALID_ARG) when null, overlapping or known to the runtime as
+ * device memory. A rejected call queues nothing. Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * MISALIGNED, CUDA (a copy or launch refused; operations queued before it stay queued).
+ */
+int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight_r, const void* scales_r,
+                    uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* stream);
+
 /* The plan w4a16_gemm would use for this shape (host only; launches nothing). */
 int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
 

@@ -79,6 +79,25 @@ def test_gemm_rejects_bad_arguments_on_host(W, args, code):
     assert W.w4a16_gemm(*args, None) == code
 
 
+def test_gemm_host_rejects_bad_arguments_on_host(W):
+    ok = [FAKE * 8, FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 9]  # x_host x_dev qw sc y_dev y_host
+    shape = (4, 1024, 1024, 128)
+
+    def call(i, v, *sh):
+        a = list(ok)
+        if i is not None:
+            a[i] = v
+        return W.w4a16_gemm_host(*a, *(sh or shape), None)
+
+    assert call(0, 0) == 1                     # null x_host
+    assert call(5, 0) == 1                     # null y_host
+    assert call(1, 0) == 1                     # null x_dev
+    assert call(4, 0) == 1                     # null y_dev
+    assert call(None, 0, 4, 1000, 1024, 128) == 2   # N % 32
+    assert call(1, FAKE + 8) == 3              # misaligned x_dev
+    assert call(4, FAKE + 1024) == 1           # y_dev overlaps x_dev
+
+
 def test_repack_rejects_bad_arguments_on_host(W):
     assert W.w4a16_repack(0, FAKE, FAKE * 2, FAKE * 3, 1024, 1024, 128, None) == 1
     assert W.w4a16_repack(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 1000, 1024, 128, None) == 2

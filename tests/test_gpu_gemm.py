@@ -144,6 +144,27 @@ def test_groups_not_dividing_a_stage(W, G, M):
     assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
+def test_host_buffer_entry_point(W):
+    M, K, N, G = 3, 1280, 352, 128
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=90)
+    x_dev, qw, sc = to_dev(d)
+    qw_r, sc_r = W.repack(qw, sc, G)
+    x_host = x_dev.cpu().pin_memory()
+    y_host = torch.zeros((M, N), dtype=torch.float16).pin_memory()
+    x_buf = torch.empty_like(x_dev)
+    y_buf = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    W.gemm_host(x_host, x_buf, qw_r, sc_r, y_buf, y_host, N, K, G)
+    torch.cuda.synchronize()
+    assert_parity(y_f64(y_host), y_ref, abs_ref, W.w4a16_last_dispatch())
+    y_dev = W.gemm(x_dev, qw_r, sc_r, N, K, G)  # the same plan on device buffers: the same bits
+    assert torch.equal(y_dev.cpu().view(torch.int16), y_host.view(torch.int16))
+    both = torch.zeros(M * K + M * N, dtype=torch.float16).pin_memory()
+    with pytest.raises(W.W4A16Error):  # host buffers overlapping
+        W.gemm_host(both[: M * K].view(M, K), x_buf, qw_r, sc_r, y_buf, both[: M * N].view(M, N), N, K, G)
+    with pytest.raises(W.W4A16Error):  # a device buffer as x_host
+        W.gemm_host(x_dev, x_buf, qw_r, sc_r, y_buf, y_host, N, K, G)
+
+
 # ------------------------------------------------------------------------------ exact cases
 def test_one_hot_rows_are_exact(W):
     K, N, G = 512, 256, 128

@@ -36,7 +36,7 @@ PATH_GEMV_TMA = 4
 EXPORTED = [
     "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
     "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
-    "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout",
+    "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout", "w4a16_gemm_host",
 ]
 
 
@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
     lib.w4a16_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
     lib.w4a16_gemm_ex.restype = I
     lib.w4a16_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
+    lib.w4a16_gemm_host.restype = I
+    lib.w4a16_gemm_host.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.w4a16_plan_for.restype = I
     lib.w4a16_plan_for.argtypes = [I, I, I, I, ctypes.POINTER(Plan)]
     lib.w4a16_last_dispatch.restype = I
@@ -130,6 +132,11 @@ def w4a16_gemm_ex(x: int, qweight_r: int, scales_r: int, y: int, M: int, N: int,
                              ctypes.byref(plan) if plan is not None else None, stream)
 
 
+def w4a16_gemm_host(x_host: int, x_dev: int, qweight_r: int, scales_r: int, y_dev: int, y_host: int, M: int, N: int,
+                    K: int, group: int, stream: int | None) -> int:
+    return lib.w4a16_gemm_host(x_host, x_dev, qweight_r, scales_r, y_dev, y_host, M, N, K, group, stream)
+
+
 def w4a16_plan_for(M: int, N: int, K: int, group: int) -> Plan:
     p = Plan()
     rc = lib.w4a16_plan_for(M, N, K, group, ctypes.byref(p))
@@ -177,6 +184,16 @@ def repack(qweight: torch.Tensor, scales: torch.Tensor, group: int = 128, stream
     _check(w4a16_repack(qweight.data_ptr(), scales.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), N, K, group,
                         _stream_handle(stream)), "w4a16_repack")
     return qw_r, sc_r
+
+
+def gemm_host(x_host: torch.Tensor, x_dev: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor,
+              y_dev: torch.Tensor, y_host: torch.Tensor, N: int, K: int, group: int = 128, stream=None) -> None:
+    """w4a16_gemm_host on tensors: x_host / y_host fp16 on the CPU (pinned), x_dev / y_dev on cuda.
+    Queues the three operations on `stream`; y_host is valid after that stream is synchronised."""
+    M = x_host.shape[0]
+    _check(w4a16_gemm_host(x_host.data_ptr(), x_dev.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(),
+                           y_dev.data_ptr(), y_host.data_ptr(), M, N, K, group, _stream_handle(stream)),
+           "w4a16_gemm_host")
 
 
 def unrepack(qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, group: int = 128, stream=None):

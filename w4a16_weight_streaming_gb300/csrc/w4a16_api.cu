@@ -69,6 +69,16 @@ bool is_host_pointer(const void* p) {
     return a.type == cudaMemoryTypeHost;
 }
 
+// True for pointers the runtime knows to be device (or managed) memory.
+bool is_device_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + nb && b0 < a0 + na;
@@ -436,6 +446,84 @@ __global__ void wait_timeout_selftest_kernel(unsigned* status, uint64_t timeout_
 
 using namespace w4a16;
 
+namespace w4a16 {
+namespace {
+
+// Every argument check of a GEMM on device buffers, then the plan; launches nothing.
+int prepare_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
+                 int group, const w4a16_plan* plan, DeviceInfo* d, Choice* ch) {
+    if (!x || !qweight_r || !scales_r || !y) return W4A16_ERR_INVALID_ARG;
+    if (M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(qweight_r) || !aligned16(scales_r) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+    const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
+    const size_t qb = static_cast<size_t>(N) * K / 2, sb = static_cast<size_t>(K / group) * N * 2;
+    if (overlaps(x, xb, y, yb) || overlaps(qweight_r, qb, y, yb) || overlaps(scales_r, sb, y, yb))
+        return W4A16_ERR_INVALID_ARG;
+    if (is_host_pointer(x) || is_host_pointer(qweight_r) || is_host_pointer(scales_r) || is_host_pointer(y))
+        return W4A16_ERR_INVALID_ARG;
+    if (!device_info(d)) return W4A16_ERR_CUDA;
+    return resolve_plan(M, N, K, group, plan, d->sm_count, true, ch);
+}
+
+int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M,
+                int N, int K, int group, const DeviceInfo& d, void* stream) {
+    LaunchCtx ctx;
+    ctx.stream = static_cast<cudaStream_t>(stream);
+    ctx.status = d.status;
+    ctx.timeout_ns = g_timeout_ns.load();
+    ctx.sm_count = d.sm_count;
+    cudaError_t e;
+    char desc[256];
+    if (ch.path == W4A16_PATH_GEMV) {
+        e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
+                        group, ch.gemv_split, ctx);
+        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%d,%d,1) block=128", M, N, K,
+                 group, ch.gemv_split, ch.gemv_split, N / 32);
+    } else if (ch.path == W4A16_PATH_GEMV_TMA) {
+        e = launch_gemv_tma(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
+                            K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages, ctx);
+        snprintf(desc, sizeof(desc),
+                 "path=gemv_tma M=%d N=%d K=%d group=%d k_chunk=%d stages=%d split_k=%d grid=(%d,%d,1) block=288 "
+                 "smem=%zu",
+                 M, N, K, group, ch.gt_kc, ch.gt_stages, ch.gemv_split, ch.gemv_split, (N + 127) / 128,
+                 gemv_tma_smem_bytes(M, K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages));
+    } else if (ch.path == W4A16_PATH_STREAM) {
+        e = launch_stream(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
+                          K, group, ch.st, ctx);
+        snprintf(desc, sizeof(desc),
+                 "path=stream M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
+                 "acc_buffers=%d split_k=%d clusters=%d grid=(%d,%d,1) tmem_cols=%d smem=%zu",
+                 M, N, K, group, ch.st.m_tile, ch.st.k_chunk, ch.st.stages, ch.st.tmem_stages, ch.st.issuers,
+                 ch.st.dbuf, ch.st.split, ch.st.clusters, ch.st.split, ch.st.clusters, stream_tmem_columns(ch.st),
+                 stream_smem_bytes(ch.st, group, K));
+    } else {
+        e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
+                      group, ch.tc, ctx);
+        snprintf(desc, sizeof(desc),
+                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
+                 "dequant_warps=%d split_k=%d grid=(%d,%d,%d) tmem_cols=%d smem=%zu",
+                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
+                 ch.tc.dequant_warps, ch.tc.split,
+                 ch.tc.split,
+                 (N + 127) / 128, (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        snprintf(g_last, sizeof(g_last), "%s%s", desc, e == cudaSuccess ? "" : " (launch failed)");
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
 extern "C" {
 
 int w4a16_version(void) { return 100; }
@@ -541,68 +629,31 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
 
 int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                   int group, const w4a16_plan* plan, void* stream) {
-    if (!x || !qweight_r || !scales_r || !y) return W4A16_ERR_INVALID_ARG;
-    if (M <= 0) return W4A16_ERR_INVALID_ARG;
-    const int sh = check_matrix_shape(N, K, group);
-    if (sh != W4A16_OK) return sh;
-    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned16(x) || !aligned16(qweight_r) || !aligned16(scales_r) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
-    const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
-    const size_t qb = static_cast<size_t>(N) * K / 2, sb = static_cast<size_t>(K / group) * N * 2;
-    if (overlaps(x, xb, y, yb) || overlaps(qweight_r, qb, y, yb) || overlaps(scales_r, sb, y, yb))
-        return W4A16_ERR_INVALID_ARG;
-    if (is_host_pointer(x) || is_host_pointer(qweight_r) || is_host_pointer(scales_r) || is_host_pointer(y))
-        return W4A16_ERR_INVALID_ARG;
     DeviceInfo d;
-    if (!device_info(&d)) return W4A16_ERR_CUDA;
     Choice ch;
-    const int rc = resolve_plan(M, N, K, group, plan, d.sm_count, true, &ch);
+    const int rc = prepare_gemm(x, qweight_r, scales_r, y, M, N, K, group, plan, &d, &ch);
     if (rc != W4A16_OK) return rc;
-    LaunchCtx ctx;
-    ctx.stream = static_cast<cudaStream_t>(stream);
-    ctx.status = d.status;
-    ctx.timeout_ns = g_timeout_ns.load();
-    ctx.sm_count = d.sm_count;
-    cudaError_t e;
-    char desc[256];
-    if (ch.path == W4A16_PATH_GEMV) {
-        e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
-                        group, ch.gemv_split, ctx);
-        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%d,%d,1) block=128", M, N, K,
-                 group, ch.gemv_split, ch.gemv_split, N / 32);
-    } else if (ch.path == W4A16_PATH_GEMV_TMA) {
-        e = launch_gemv_tma(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
-                            K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages, ctx);
-        snprintf(desc, sizeof(desc),
-                 "path=gemv_tma M=%d N=%d K=%d group=%d k_chunk=%d stages=%d split_k=%d grid=(%d,%d,1) block=288 "
-                 "smem=%zu",
-                 M, N, K, group, ch.gt_kc, ch.gt_stages, ch.gemv_split, ch.gemv_split, (N + 127) / 128,
-                 gemv_tma_smem_bytes(M, K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages));
-    } else if (ch.path == W4A16_PATH_STREAM) {
-        e = launch_stream(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
-                          K, group, ch.st, ctx);
-        snprintf(desc, sizeof(desc),
-                 "path=stream M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "acc_buffers=%d split_k=%d clusters=%d grid=(%d,%d,1) tmem_cols=%d smem=%zu",
-                 M, N, K, group, ch.st.m_tile, ch.st.k_chunk, ch.st.stages, ch.st.tmem_stages, ch.st.issuers,
-                 ch.st.dbuf, ch.st.split, ch.st.clusters, ch.st.split, ch.st.clusters, stream_tmem_columns(ch.st),
-                 stream_smem_bytes(ch.st, group, K));
-    } else {
-        e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
-                      group, ch.tc, ctx);
-        snprintf(desc, sizeof(desc),
-                 "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "dequant_warps=%d split_k=%d grid=(%d,%d,%d) tmem_cols=%d smem=%zu",
-                 M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
-                 ch.tc.dequant_warps, ch.tc.split,
-                 ch.tc.split,
-                 (N + 127) / 128, (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
+    return launch_gemm(ch, x, qweight_r, scales_r, y, M, N, K, group, d, stream);
+}
+
+int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight_r, const void* scales_r,
+                    uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* stream) {
+    if (!x_host || !y_host) return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    Choice ch;
+    const int rc = prepare_gemm(x_dev, qweight_r, scales_r, y_dev, M, N, K, group, nullptr, &d, &ch);
+    if (rc != W4A16_OK) return rc;
+    const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
+    if (overlaps(x_host, xb, y_host, yb) || is_device_pointer(x_host) || is_device_pointer(y_host))
+        return W4A16_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
     }
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        snprintf(g_last, sizeof(g_last), "%s%s", desc, e == cudaSuccess ? "" : " (launch failed)");
-    }
-    if (e != cudaSuccess) {
+    const int lr = launch_gemm(ch, x_dev, qweight_r, scales_r, y_dev, M, N, K, group, d, stream);
+    if (lr != W4A16_OK) return lr;
+    if (cudaMemcpyAsync(y_host, y_dev, yb, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
         cudaGetLastError();
         return W4A16_ERR_CUDA;
     }
