@@ -28,8 +28,8 @@
  *   - Supported shapes: N % 32 == 0, K % 64 == 0, group % 32 == 0, K % group == 0,
  *     1 <= M <= 2^20, N <= 2^23, K <= 2^22. x, y, qweight and scales 16-byte aligned.
  *     x and y must not overlap. The tensor-core paths (M > 8, or M >= 3 with automatic plans)
- *     also need group to divide 128 or be a multiple of it (32, 64, 128, 256, 384, ...); for
- *     M <= 8 the automatic plan takes the CUDA-core GEMV when it does not.
+ *     also need K % 128 == 0 and group dividing 128 or a multiple of it (32, 64, 128, 256,
+ *     384, ...); for M <= 8 the automatic plan takes the CUDA-core GEMV when they do not.
  */
 #ifndef W4A16_H
 #define W4A16_H

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -129,6 +130,30 @@ def test_plan_for_group_sizes(W):
             assert W.w4a16_plan_for(M, 256, 1920, G).path == W.PATH_GEMV
         with pytest.raises(W.W4A16Error):
             W.w4a16_plan_for(9, 256, 1920, G)
+
+
+def test_every_supported_shape_gets_a_plan(W):
+    # host-only property of the dispatcher: inside the supported set every automatic plan resolves,
+    # except, at more than 8 rows, shapes the tiles cannot stage (K % 128, odd group sizes)
+    rng = np.random.default_rng(5)
+    for _ in range(400):
+        G = int(rng.choice([32, 64, 96, 128, 160, 256, 384, 512]))
+        K = G * int(rng.integers(1, 40))
+        K = K if K % 64 == 0 else 2 * K
+        N = 32 * int(rng.integers(1, 1200))
+        M = int(rng.choice([1, 2, 3, 5, 8, 9, 16, 31, 64, 65, 128, 200, 256, 511, 1024, 4096]))
+        fits = (128 % G == 0 or G % 128 == 0) and K % 128 == 0
+        if M > 8 and not fits:
+            with pytest.raises(W.W4A16Error):
+                W.w4a16_plan_for(M, N, K, G)
+            continue
+        p = W.w4a16_plan_for(M, N, K, G)
+        assert p.path in (W.PATH_GEMV, W.PATH_TC)
+        assert p.split_k >= 1
+        if p.path == W.PATH_TC:
+            assert p.k_chunk in (128, 256) and K % p.k_chunk == 0
+            assert p.split_k <= K // p.k_chunk
+            assert 2 <= p.stages <= 16 and p.m_tile in (16, 32, 64, 128, 256)
 
 
 def test_wait_timeout_setting(W):

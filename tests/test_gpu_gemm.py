@@ -132,11 +132,12 @@ def test_group_sizes(W, G):
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
-@pytest.mark.parametrize("G", [96, 160])
+@pytest.mark.parametrize("G,K", [(96, 1920), (160, 1920), (64, 1216)])
 @pytest.mark.parametrize("M", [1, 3, 8])
-def test_groups_not_dividing_a_stage(W, G, M):
-    # automatic plans send these to the GEMV, which reads one scale per 32-k row
-    K, N = 1920, 160
+def test_shapes_the_tiles_cannot_stage(W, G, K, M):
+    # group sizes that do not fit a 128-k stage, and K = 64 mod 128: automatic plans send these to
+    # the GEMV, which works in 32-k rows with one scale each
+    N = 160
     d, y_ref, abs_ref = _case(M, K, N, G, seed=G + M)
     x, qw_r, sc_r = _repacked(W, d, G)
     y = run_gemm(W, x, qw_r, sc_r, N, K, G)

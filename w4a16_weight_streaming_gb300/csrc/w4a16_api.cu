@@ -338,9 +338,11 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         // 5120 x 34816 and 17408 x 5120 the tiles are 1-2 us faster.
         const bool small = static_cast<int64_t>(K) * N < (int64_t{64} << 20);
         path = (M == 1 || (M == 2 && small)) ? W4A16_PATH_GEMV : W4A16_PATH_TC;
-        // The tile kernels stage whole scale groups per 128-k stage; a group that neither divides
-        // nor is a multiple of 128 (96, 160, ...) goes to the GEMV, which reads one per 32-k row.
-        if (path == W4A16_PATH_TC && !group_fits(128, G) && M <= kGemvMaxM) path = W4A16_PATH_GEMV;
+        // The tile kernels run whole 128-k stages and stage whole scale groups per stage; a K that
+        // is not a multiple of 128, or a group that neither divides nor is a multiple of 128
+        // (96, 160, ...), goes to the GEMV, which works in 32-k rows with one scale each.
+        if (path == W4A16_PATH_TC && (K % 128 != 0 || !group_fits(128, G)) && M <= kGemvMaxM)
+            path = W4A16_PATH_GEMV;
     }
     out->path = path;
     if (path == W4A16_PATH_GEMV_TMA) {
