@@ -110,7 +110,7 @@ int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight
  *   qweight_r: repacked weights from w4a16_repack, device
  *   scales_r:  repacked scales from w4a16_repack, device
  *   y:         fp16 [M][N] row-major, device, written in full (every element)
- * The dispatcher picks the kernel family and launch plan from (M, N, K); w4a16_last_dispatch
+ * The dispatcher picks the kernel family and launch plan from (M, N, K, group); w4a16_last_dispatch
  * reports what ran. Accuracy: every element is within 2^-10*|y_exact| + 2^-10*sum_k|x*w| of the
  * exact result (fp32 accumulation chains are kept short enough for that bound).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA (launch refused).
