@@ -169,19 +169,25 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
 
-        backend = "nccl"
+        # NCCL between the GPUs of one node; gloo where there is no GPU (the CPU reference arm
+        # and the multi-process tests)
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
         return dist, rank, world, local
     return None, 0, 1, 0
 
 
 def dist_max(dist, value: float, device) -> float:
+    """Maximum of `value` over the ranks (identity without a process group)."""
     if dist is None:
         return value
     import torch
 
+    if dist.get_backend() != "nccl":
+        device = "cpu"
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
