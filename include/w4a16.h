@@ -141,7 +141,12 @@ int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r
 int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight_r, const void* scales_r,
                     uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* stream);
 
-/* The plan w4a16_gemm would use for this shape (host only; launches nothing). */
+/* The plan w4a16_gemm would use for this shape (host only; launches nothing).
+ * Automatic plans (w4a16_gemm, w4a16_gemm_host, w4a16_gemm_ex with NULL or all-zero plan, this
+ * call) can be overridden without rebuilding: the environment variable W4A16_PLAN, read once per
+ * process, holds "field=value[,field=value...]" with the w4a16_plan field names, no spaces
+ * (e.g. "path=2,m_tile=64,split_k=3"). It is then used as the plan of every such call. A malformed
+ * W4A16_PLAN makes them return INVALID_ARG; a plan invalid for a shape, UNSUPPORTED_SHAPE. */
 int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
 
 /* Describes the last GEMM this process launched (path, tile, split, grid) into buf (NUL

@@ -156,6 +156,31 @@ def test_every_supported_shape_gets_a_plan(W):
             assert 2 <= p.stages <= 16 and p.m_tile in (16, 32, 64, 128, 256)
 
 
+def _plan_in_subprocess(env_value):
+    import subprocess
+    import sys
+
+    code = ("import w4a16_weight_streaming_gb300 as W\n"
+            "try:\n"
+            "    p = W.w4a16_plan_for(1, 5120, 5120, 128); print(p.path, p.split_k, p.m_tile)\n"
+            "except W.W4A16Error as e:\n"
+            "    print('error', e.code)\n")
+    env = dict(os.environ)
+    env.pop("W4A16_PLAN", None)
+    if env_value is not None:
+        env["W4A16_PLAN"] = env_value
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    return out.stdout.split()
+
+
+def test_plan_override_from_environment(W):
+    assert _plan_in_subprocess(None)[0] == str(W.PATH_GEMV)           # automatic: the GEMV at M = 1
+    assert _plan_in_subprocess("path=2,m_tile=16,split_k=2") == ["2", "2", "16"]
+    assert _plan_in_subprocess("path=2,bogus=1") == ["error", "1"]    # malformed: refused loudly
+    assert _plan_in_subprocess("path=2,split_k=x") == ["error", "1"]
+    assert _plan_in_subprocess("path=1,split_k=40") == ["error", "2"]  # valid syntax, invalid plan
+
+
 def test_wait_timeout_setting(W):
     assert W.w4a16_set_wait_timeout_ns(10) == 1
     assert W.w4a16_set_wait_timeout_ns(2_000_000_000) == 0

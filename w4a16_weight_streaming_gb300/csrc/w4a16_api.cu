@@ -5,9 +5,11 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <string>
 #include <tuple>
 
 #include "common.cuh"
@@ -298,11 +300,63 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
 // the driver's cluster occupancy for every candidate split.
 std::map<std::tuple<int, int, int, int, int>, Choice> g_plan_cache;
 
+// W4A16_PLAN: an override of every automatic plan, read once per process. Its value is
+// "field=value[,field=value...]" with the w4a16_plan field names, e.g. "path=2,m_tile=64,split_k=3",
+// no spaces. A malformed value fails every automatic call with INVALID_ARG instead of being ignored.
+struct EnvPlan {
+    bool present = false;
+    bool valid = true;
+    w4a16_plan plan = {};
+};
+
+const EnvPlan& env_plan() {
+    static const EnvPlan e = [] {
+        EnvPlan r;
+        const char* v = std::getenv("W4A16_PLAN");
+        if (!v || !*v) return r;
+        r.present = true;
+        const std::string s(v);
+        size_t pos = 0;
+        while (r.valid && pos <= s.size()) {
+            size_t end = s.find(',', pos);
+            if (end == std::string::npos) end = s.size();
+            const std::string item = s.substr(pos, end - pos);
+            const size_t eq = item.find('=');
+            const std::string key = eq == std::string::npos ? item : item.substr(0, eq);
+            const std::string val = eq == std::string::npos ? std::string() : item.substr(eq + 1);
+            char* stop = nullptr;
+            const long n = val.empty() ? -1 : std::strtol(val.c_str(), &stop, 10);
+            int* field = key == "path"            ? &r.plan.path
+                         : key == "split_k"       ? &r.plan.split_k
+                         : key == "m_tile"        ? &r.plan.m_tile
+                         : key == "k_chunk"       ? &r.plan.k_chunk
+                         : key == "stages"        ? &r.plan.stages
+                         : key == "tmem_stages"   ? &r.plan.tmem_stages
+                         : key == "mma_issuers"   ? &r.plan.mma_issuers
+                         : key == "clusters"      ? &r.plan.clusters
+                         : key == "dequant_warps" ? &r.plan.dequant_warps
+                                                  : nullptr;
+            if (!field || n < 0 || n > 4096 || (stop && *stop != '\0')) {
+                r.valid = false;
+                break;
+            }
+            *field = static_cast<int>(n);
+            pos = end + 1;
+        }
+        return r;
+    }();
+    return e;
+}
+
 int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, Choice* out) {
-    const bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
-                                               plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
-                                               plan->mma_issuers == 0 && plan->clusters == 0 &&
-                                               plan->dequant_warps == 0);
+    bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
+                                         plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
+                                         plan->mma_issuers == 0 && plan->clusters == 0 && plan->dequant_warps == 0);
+    if (automatic && env_plan().present) {
+        if (!env_plan().valid) return W4A16_ERR_INVALID_ARG;
+        plan = &env_plan().plan;
+        automatic = false;
+    }
     if (!automatic || !have_device) return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
     int dev = 0;
     cudaGetDevice(&dev);
