@@ -43,6 +43,8 @@ WORKLOADS = {
     "verify": ("single-stream speculative verify", inputs.WORKLOADS["spec_verify"]),
     "batched": ("batched verify", inputs.WORKLOADS["batched_verify"]),
     "oracle_scale": ("oracle-scale GEMM", inputs.WORKLOADS["oracle_scale"]),
+    "head": ("output-head GEMV", inputs.WORKLOADS["output_head"]),
+    "head_verify": ("output-head verify", inputs.WORKLOADS["output_head_verify"]),
 }
 
 

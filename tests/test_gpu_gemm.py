@@ -166,6 +166,27 @@ def test_host_buffer_entry_point(W):
         W.gemm_host(x_dev, x_buf, qw_r, sc_r, y_buf, y_host, N, K, G)
 
 
+@pytest.fixture(scope="module")
+def output_head(W):
+    # the output-head matrix K x N = 5120 x 248320 (636 MB packed), generated once for both row counts
+    (_, K, N, seed), = inputs.WORKLOADS["output_head"]
+    qweight, scales = inputs.generate_weights(K, N, 128, seed=seed)
+    qw_r, sc_r = W.repack(torch.from_numpy(qweight).cuda(), torch.from_numpy(scales.view(np.int16)).cuda(), 128)
+    return K, N, seed, qweight, scales, qw_r, sc_r
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_output_head_sampled(W, output_head, M):
+    K, N, seed, qweight, scales, qw_r, sc_r = output_head
+    x = inputs.generate_x(M, K, seed + M)
+    y = y_f64(run_gemm(W, x_to_dev(x), qw_r, sc_r, N, K, 128))
+    rng = np.random.default_rng(M)
+    ns = np.concatenate([rng.integers(0, N, 240), np.arange(N - 8, N)])  # the last tile too
+    ms = rng.integers(0, M, ns.size)
+    y_ref, abs_ref = oracle.gemm_sampled(x, qweight, scales, 128, ms, ns)
+    assert_parity(y[ms, ns], y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
 # ------------------------------------------------------------------------------ exact cases
 def test_one_hot_rows_are_exact(W):
     K, N, G = 512, 256, 128

@@ -30,6 +30,9 @@ WORKLOADS = {
     "decode_gemv": [(1, 5120, 5120, 1), (1, 17408, 5120, 1)],
     "spec_verify": [(16, 5120, 34816, 2)],
     "batched_verify": [(256, 5120, 34816, 3), (256, 17408, 5120, 3)],
+    # the output head (vocabulary projection) of the same model: one decode row, and a verify step
+    "output_head": [(1, 5120, 248320, 5)],
+    "output_head_verify": [(16, 5120, 248320, 5)],
 }
 SWEEP_MATRICES = [("qkv", 5120, 7168), ("o", 5120, 5120), ("gate_up", 5120, 34816), ("down", 17408, 5120)]
 SWEEP_M = [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024]
