@@ -27,7 +27,7 @@
  *     call launches nothing and leaves every buffer untouched.
  *   - Supported shapes: N % 32 == 0, K % 64 == 0, group % 32 == 0, K % group == 0,
  *     1 <= M <= 2^20, N <= 2^23, K <= 2^22. x, y, qweight and scales 16-byte aligned.
- *     x and y must not overlap. The tensor-core paths (M > 8, or M >= 3 with automatic plans)
+ *     x and y must not overlap. The tensor-core paths (M > 8, or M >= 2 with automatic plans)
  *     also need K % 128 == 0 and group dividing 128 or a multiple of it (32, 64, 128, 256,
  *     384, ...); for M <= 8 the automatic plan takes the CUDA-core GEMV when they do not.
  */
