@@ -1,24 +1,30 @@
 #!/usr/bin/env python3
 """Benchmark of the W4A16 weight-streaming GEMM on GB300 (one JSON line on stdout).
 
-Step = one pass of the hot path over one batch: the single-stream decode GEMV workload, M = 1
-activation row through two matrices (K x N = 5120 x 5120 and 17408 x 5120, group 128), each
-y = x . dequant(W) through the C ABI (w4a16_gemm). The metric is the effective weight-stream
-rate, weight bytes (0.5 B per weight + fp16 scales) / step time, beside TFLOP/s.
+Default workload: the dense-layer sweep. The four matrices of one dense layer (K x N = 5120 x 7168
+fused qkv, 5120 x 5120 o, 5120 x 34816 fused gate+up, 17408 x 5120 down; group 128) at every
+M in {1, 2, 4, ..., 1024}. One step = one pass of the hot path over all 44 (M, matrix) GEMMs, in
+layer order (for each M: qkv, o, gate+up, down), each y = x . dequant(W) through the C ABI.
+`value` = weight bytes streamed per step / step time (effective weight-stream GB/s of the whole
+sweep); `tflops` likewise; `rows` gives every (matrix, M) launch on its own: mean us (plain CUDA
+graph), median / p10 / p90 us (per-launch event pairs), weight GB/s, TFLOP/s, roofline fraction,
+bound and plan.
 
-Timing: W untimed warm-up steps; the K timed steps are one CUDA-graph replay bracketed by a
-barrier and torch.cuda.synchronize(), timed with CUDA events on the launching stream. Every
-step reads the next of R device copies of the weights (R x weight bytes > 4 x L2), so no step
-finds its weights in L2. `e2e` repeats the K steps through the C ABI with host buffers
-(w4a16_gemm_host): each step copies x from pinned host memory and reads y back.
+Timing: W untimed warm-up steps; the K timed steps are K replays of a CUDA graph of one step,
+bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on the launching
+stream. L2: every weight matrix exists in R device copies and consecutive uses of one copy are at
+least 4 x L2 bytes of other weights apart, so no launch finds its weights in L2. `e2e` repeats
+steps through w4a16_gemm_host with host buffers (x copied in from pinned host memory, y copied
+back, every GEMM of the step).
 
---impl reference times the CPU oracle (fp64, oracle/) on the same metric; under torchrun only
-rank 0 runs it. --workload selects another configuration (for profiles); --sweep prints the
-dense-layer sweep table to stderr.
+--workload picks one of the single configurations instead (decode, verify, batched, head, ...):
+the same line for that configuration. --impl reference times the CPU oracle (fp64, oracle/) on a
+bounded sample of the same workload; under torchrun only rank 0 runs it.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -50,7 +56,7 @@ WORKLOADS = {
 
 # ------------------------------------------------------------------------------ accounting
 def weight_bytes(K: int, N: int, group: int = GROUP) -> int:
-    """Packed weights (4 bits each) + fp16 scales: what one step must stream from HBM."""
+    """Packed weights (4 bits each) + fp16 scales: what one launch must stream from HBM."""
     return K * N // 2 + (K // group) * N * 2
 
 
@@ -64,35 +70,31 @@ def gemm_flops(M: int, K: int, N: int) -> int:
     return 2 * M * N * K
 
 
-def bound_tokens_per_s(bandwidth_bytes_s: float, bytes_per_token: float) -> float:
-    """Single-stream ceiling: every weight read once per token."""
-    return bandwidth_bytes_s / bytes_per_token
+def roofline_seconds(M: int, K: int, N: int, peaks: dict) -> tuple[float, float]:
+    """(t_mem, t_tensor): the weight + activation bytes at the HBM peak, the FLOPs at the tensor peak."""
+    t_mem = (weight_bytes(K, N) + activation_bytes(M, K, N)) / (peaks["hbm_gbs"] * 1e9)
+    t_tc = gemm_flops(M, K, N) / (peaks["bf16_tflops"] * 1e12)
+    return t_mem, t_tc
 
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each workload's dominant
-# kernel from one ncu capture (summaries under profiles/), with the SHA-256 prefix of the kernel
-# sources it was taken from: a figure is reported only while those sources are unchanged.
-MEASURED_TRAFFIC = {
-    "path=gemv M=1 N=5120 K=17408 ": (46_027_008, ("gemv.cu", "common.cuh"), "7f97cbde400939bb",
-                                      "profiles/gemv_decode_m1_17408x5120.md"),
-    "path=tc M=16 N=34816 K=5120 ": (95_082_240, ("tc_gemm.cu", "common.cuh"), "e5db09846ea61779",
-                                     "profiles/tc_gemm_verify_m16_5120x34816.md"),
-    "path=tc M=256 N=34816 K=5120 ": (97_315_840, ("tc_gemm.cu", "common.cuh"), "e5db09846ea61779",
-                                      "profiles/tc_gemm_batched_m256_5120x34816.md"),
-}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a launch shape from one
+# ncu capture (summaries under profiles/), with the SHA-256 prefix of the kernel sources it was
+# taken from: a figure is reported only while those sources are unchanged.
+MEASURED_TRAFFIC: dict[str, tuple[int, tuple[str, ...], str, str]] = {}
+
+
+def source_digest(files) -> str:
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "w4a16_weight_streaming_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
 
 
 def measured_traffic(plan: str):
     """(bytes per launch, summary file) if a capture of this launch's current kernel exists."""
-    import hashlib
     for prefix, (nbytes, files, digest, summary) in MEASURED_TRAFFIC.items():
-        if not plan.startswith(prefix):
-            continue
-        m = hashlib.sha256()
-        for f in files:
-            with open(os.path.join(ROOT, "w4a16_weight_streaming_gb300", "csrc", f), "rb") as fh:
-                m.update(fh.read())
-        if m.hexdigest()[:16] == digest:
+        if plan.startswith(prefix) and source_digest(files) == digest:
             return nbytes, summary
     return None, None
 
@@ -195,46 +197,131 @@ def dist_max(dist, value: float, device) -> float:
     return float(t.item())
 
 
-# ------------------------------------------------------------------------------ CPU oracle timing
-def oracle_prepare(mats, cols: int):
-    """The workload's inputs restricted to the first `cols` columns of every matrix (a bounded
-    sample for the CPU oracle)."""
-    prepared = []
+# ------------------------------------------------------------------------------ the work of a step
+def sweep_rows():
+    """(name, M, K, N) of every GEMM of one sweep step, in execution order (layer order per M)."""
+    return [(name, M, K, N) for M in inputs.SWEEP_M for (name, K, N) in inputs.SWEEP_MATRICES]
+
+
+def workload_rows(mats):
+    return [(f"{K}x{N}", M, K, N) for (M, K, N, _) in mats]
+
+
+def describe(workload: str):
+    """(config dict, rows) of a workload name."""
+    if workload == "sweep":
+        rows = sweep_rows()
+        mats = ", ".join(f"{n} {K}x{N}" for (n, K, N) in inputs.SWEEP_MATRICES)
+        cfg = {"workload": f"dense-layer sweep: M in {inputs.SWEEP_M} x ({mats}), K x N, group {GROUP}, "
+                           f"seed {inputs.SWEEP_SEED} (x of each M from seed 1000+M)",
+               "M": inputs.SWEEP_M, "matrices": [{"name": n, "K": K, "N": N} for (n, K, N) in inputs.SWEEP_MATRICES],
+               "group": GROUP, "seed": inputs.SWEEP_SEED}
+        return cfg, rows
+    name, mats = WORKLOADS[workload]
+    cfg = {"workload": f"{name}: M={mats[0][0]}, K x N = " + ", ".join(f"{K}x{N}" for (_, K, N, _) in mats)
+                       + f", group {GROUP}",
+           "M": mats[0][0], "matrices": [{"K": K, "N": N, "seed": s} for (_, K, N, s) in mats], "group": GROUP}
+    return cfg, workload_rows(mats)
+
+
+def host_inputs(workload: str, cols: int | None = None):
+    """Host-side inputs of every row: list of dict(name, M, K, N, x, qweight, scales) with the
+    weights restricted to the first `cols` columns when given (bounded oracle samples)."""
+    out = []
+    if workload == "sweep":
+        weights = {}
+        for (name, K, N) in inputs.SWEEP_MATRICES:
+            qw, sc = inputs.generate_weights(K, N, GROUP, seed=inputs.SWEEP_SEED)
+            if cols is not None:
+                qw, sc = np.ascontiguousarray(qw[:, :cols]), np.ascontiguousarray(sc[:, :cols])
+            weights[name] = (qw, sc)
+        xs = {}
+        for (name, M, K, N) in sweep_rows():
+            if (M, K) not in xs:
+                xs[(M, K)] = inputs.generate_x(M, K, seed=1000 + M)
+            qw, sc = weights[name]
+            out.append(dict(name=name, M=M, K=K, N=N, x=xs[(M, K)], qweight=qw, scales=sc))
+        return out
+    _, mats = WORKLOADS[workload]
     for (M, K, N, seed) in mats:
         d = inputs.generate(M, K, N, GROUP, seed=seed)
-        c = min(cols, N)
-        prepared.append((d["x"], np.ascontiguousarray(d["qweight"][:, :c]), np.ascontiguousarray(d["scales"][:, :c]),
-                         weight_bytes(K, c)))
-    return prepared
+        qw, sc = d["qweight"], d["scales"]
+        if cols is not None:
+            qw, sc = np.ascontiguousarray(qw[:, :cols]), np.ascontiguousarray(sc[:, :cols])
+        out.append(dict(name=f"{K}x{N}", M=M, K=K, N=N, x=d["x"], qweight=qw, scales=sc))
+    return out
 
 
-def oracle_pass(prepared, nthreads: int) -> int:
+# ------------------------------------------------------------------------------ CPU oracle timing
+def oracle_pass(items, nthreads: int) -> int:
     """One pass of the fp64 oracle over the sample; returns the weight bytes it covered."""
     import oracle
 
     nbytes = 0
-    for (x, qw, sc, wb) in prepared:
-        oracle.gemm(x, qw, sc, GROUP, nthreads=nthreads)
-        nbytes += wb
+    for it in items:
+        oracle.gemm(it["x"], it["qweight"], it["scales"], GROUP, nthreads=nthreads)
+        nbytes += weight_bytes(it["K"], it["qweight"].shape[1])
     return nbytes
 
 
-def oracle_sample(mats, cols: int, target_s: float, nthreads: int):
-    """Times the oracle on the sample, repeated for about target_s seconds.
+def column_sample(items, cols: int):
+    """The same rows with every weight matrix cut to its first `cols` columns."""
+    return [dict(it, qweight=np.ascontiguousarray(it["qweight"][:, :cols]),
+                 scales=np.ascontiguousarray(it["scales"][:, :cols])) for it in items]
+
+
+def oracle_sample(items, cols: int, target_s: float, nthreads: int):
+    """The oracle on a bounded sample of the rows, repeated for about target_s seconds.
     Returns (GB/s of weights processed, seconds, repetitions)."""
     import oracle
 
     oracle.build()
-    prepared = oracle_prepare(mats, cols)
-    oracle_pass(prepared, nthreads)  # warm
+    items = column_sample(items, cols)
+    oracle_pass(items, nthreads)  # warm
     reps, nbytes, t0 = 0, 0, time.perf_counter()
     while True:
-        nbytes += oracle_pass(prepared, nthreads)
+        nbytes += oracle_pass(items, nthreads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= target_s:
             break
     return nbytes / el / 1e9, el, reps
+
+
+def oracle_single_thread_configs(budget_s: float = 4.0):
+    """The oracle on ONE thread for the three smallest configurations (oracle-scale in full, decode
+    and verify on a column sample), as us per call extrapolated to the full matrix."""
+    import oracle
+
+    oracle.build()
+    res = []
+    for key, cols in (("oracle_scale", None), ("decode", 128), ("verify", 32)):
+        items = host_inputs(key, cols)
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle_pass(items, 1)
+            reps += 1
+            if time.perf_counter() - t0 >= budget_s / 3:
+                break
+        el = (time.perf_counter() - t0) / reps
+        frac = sum(it["qweight"].shape[1] for it in items) / sum(it["N"] for it in items)
+        res.append({"config": key, "threads": 1, "columns_timed": cols or "all",
+                    "s_per_call_full_matrix": el / frac, "weight_gbs": sum(
+                        weight_bytes(it["K"], it["qweight"].shape[1]) for it in items) / el / 1e9})
+    return res
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                low = line.lower()
+                if low.startswith("model name") or low.startswith("cpu part"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def run_reference(args, rank: int):
@@ -243,48 +330,48 @@ def run_reference(args, rank: int):
     import oracle
 
     oracle.build()
-    name, mats = WORKLOADS[args.workload]
+    cfg, rows = describe(args.workload)
     nthreads = oracle.default_threads()
-    cols = 256
-    prepared = oracle_prepare(mats, cols)
+    cols = 4 if args.workload == "sweep" else 256
+    items = host_inputs(args.workload, cols)
     for _ in range(args.warmup):
-        oracle_pass(prepared, nthreads)
+        oracle_pass(items, nthreads)
     t0 = time.perf_counter()
     total_bytes = 0
     for _ in range(args.steps):
-        total_bytes += oracle_pass(prepared, nthreads)
+        total_bytes += oracle_pass(items, nthreads)
     el = time.perf_counter() - t0
     value = total_bytes / el / 1e9
-    sample = f"first {cols} columns of each matrix per step, all M rows, fp64 oracle"
+    sample = (f"fp64 oracle on the first {cols} columns of every matrix, every M row of every GEMM of the "
+              f"step, {nthreads} threads")
+    cfg = dict(cfg, columns_per_matrix=cols)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(name, mats, extra={"columns_per_matrix": cols}),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "sample": sample,
+                             "cpu": cpu_model()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def workload_config(name, mats, extra=None):
-    cfg = {"workload": f"{name}: M={mats[0][0]}, K x N = " + ", ".join(f"{K}x{N}" for (_, K, N, _) in mats)
-           + f", group {GROUP}",
-           "M": mats[0][0], "matrices": [{"K": K, "N": N, "seed": s} for (_, K, N, s) in mats], "group": GROUP}
-    if extra:
-        cfg.update(extra)
-    return cfg
-
-
 # ------------------------------------------------------------------------------ GPU arm
+def percentile(v, q):
+    return float(np.percentile(np.asarray(v, dtype=np.float64), q))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
-    ap.add_argument("--sweep", action="store_true", help="also print the dense-layer sweep table to stderr")
+    ap.add_argument("--workload", choices=["sweep"] + sorted(WORKLOADS), default="sweep")
+    ap.add_argument("--launches", type=int, default=200, help="per-row launches for median / p10 / p90")
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--table", action="store_true", help="also print the per-row table to stderr")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -304,43 +391,53 @@ def main():
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
     peaks = measured_peaks()
-    name, mats = WORKLOADS[args.workload]
+    cfg, _ = describe(args.workload)
 
-    # ---- inputs: canonical weights on the host -> R repacked device copies per matrix
-    step_wbytes = sum(weight_bytes(K, N) for (_, K, N, _) in mats)
-    R = max(2, -(-4 * l2 // step_wbytes))
-    bufs = []
-    for (M, K, N, seed) in mats:
-        d = inputs.generate(M, K, N, GROUP, seed=seed)
-        qw = torch.from_numpy(d["qweight"]).to(dev)
-        sc = torch.from_numpy(d["scales"].view(np.int16)).to(dev)
-        copies = [W.repack(qw, sc, GROUP) for _ in range(R)]
-        x_host = torch.from_numpy(d["x"].view(np.int16)).view(torch.float16).pin_memory()
-        x = x_host.to(dev)
-        y = torch.empty((M, N), dtype=torch.float16, device=dev)
-        y_host = torch.empty((M, N), dtype=torch.float16).pin_memory()
-        bufs.append(dict(M=M, K=K, N=N, copies=copies, x=x, y=y, x_host=x_host, y_host=y_host))
+    # ---- inputs: canonical weights on the host -> repacked device copies per matrix. Every launch
+    # of the step reads its own copy, and a matrix has enough copies that its copies cycle through
+    # more than 4 x L2 bytes: no launch finds its weights in L2.
+    items = host_inputs(args.workload)
+    mats = {}
+    for it in items:
+        if it["name"] in mats:
+            continue
+        wb = weight_bytes(it["K"], it["N"])
+        uses = sum(1 for jt in items if jt["name"] == it["name"])
+        R = max(uses + 1, -(-4 * l2 // wb))
+        qw = torch.from_numpy(it["qweight"]).to(dev)
+        sc = torch.from_numpy(it["scales"].view(np.int16)).to(dev)
+        mats[it["name"]] = dict(K=it["K"], N=it["N"], wb=wb, copies=[W.repack(qw, sc, GROUP) for _ in range(R)])
         del qw, sc
+    step_wbytes = 0
+    use_count = {n: 0 for n in mats}
+    for it in items:
+        it["x_host"] = torch.from_numpy(it["x"].view(np.int16)).view(torch.float16).pin_memory()
+        it["xd"] = it["x_host"].to(dev)
+        it["yd"] = torch.empty((it["M"], it["N"]), dtype=torch.float16, device=dev)
+        it["y_host"] = torch.empty((it["M"], it["N"]), dtype=torch.float16).pin_memory()
+        it["copy"] = use_count[it["name"]]  # the step's own copy of this matrix for this GEMM
+        use_count[it["name"]] += 1
+        step_wbytes += mats[it["name"]]["wb"]
     torch.cuda.synchronize()
 
-    def step(i: int):
-        for b in bufs:
-            qr, sr = b["copies"][i % R]
-            W.gemm(b["x"], qr, sr, b["N"], b["K"], GROUP, y=b["y"])
+    def launch(it, copy):
+        qr, sr = mats[it["name"]]["copies"][copy]
+        W.gemm(it["xd"], qr, sr, it["N"], it["K"], GROUP, y=it["yd"])
 
-    plans = []
-    for b in bufs:
-        qr, sr = b["copies"][0]
-        W.gemm(b["x"], qr, sr, b["N"], b["K"], GROUP, y=b["y"])
-        plans.append(W.w4a16_last_dispatch())
-    for i in range(args.warmup):
-        step(i)
+    def step():
+        for it in items:
+            launch(it, it["copy"])
+
+    for it in items:
+        launch(it, it["copy"])
+        it["plan"] = W.w4a16_last_dispatch()
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
     st = W.w4a16_device_status()
     if st != W.OK:
         raise RuntimeError(f"device status after warm-up: {W.status_string(st)}")
 
-    # ---- capture K steps (and, per matrix, K launches alone for the per-kernel roofline)
     cap_stream = torch.cuda.Stream(device=dev)
 
     def capture(fn):
@@ -351,38 +448,32 @@ def main():
         torch.cuda.synchronize()
         return g
 
-    g_step = capture(lambda: [step(i) for i in range(args.steps)])
-    per_matrix_graphs = []
-    for j, b in enumerate(bufs):
-        def one(b=b):
-            for i in range(args.steps):
-                qr, sr = b["copies"][i % R]
-                W.gemm(b["x"], qr, sr, b["N"], b["K"], GROUP, y=b["y"])
-        per_matrix_graphs.append(capture(one))
-    g_step.replay()  # upload + warm
-    torch.cuda.synchronize()
-
-    def timed_replay(g) -> float:
+    def timed(fn_replay, reps: int = 1) -> float:
+        """ms of `reps` calls of fn_replay, CUDA events on the current stream, barrier + sync around."""
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        g.replay()
+        for _ in range(reps):
+            fn_replay()
         e1.record()
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        return e0.elapsed_time(e1)  # ms
+        return e0.elapsed_time(e1)
 
-    # keep the GPU busy around the timed region so the clock samples reflect load
+    # ---- the timed region: K replays of the one-step graph
+    g_step = capture(step)
+    g_step.replay()
+    torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    t_end = time.perf_counter() + 0.8
+    t_end = time.perf_counter() + 0.8  # keep the GPU busy so the clock samples reflect load
     while time.perf_counter() < t_end:
         g_step.replay()
-    ms_total = timed_replay(g_step)
+    ms_total = timed(g_step.replay, args.steps)
     t_end = time.perf_counter() + 0.3
     while time.perf_counter() < t_end:
         g_step.replay()
@@ -390,67 +481,111 @@ def main():
     clocks = sampler.stop()
     ms_total = dist_max(dist, ms_total, dev)
     ms_step = ms_total / args.steps
-
-    kernel_ms = []
-    for g in per_matrix_graphs:
-        kernel_ms.append(timed_replay(g) / args.steps)
     st = W.w4a16_device_status()
     if st != W.OK:
         raise RuntimeError(f"device status after timing: {W.status_string(st)}")
 
-    flops_step = sum(gemm_flops(b["M"], b["K"], b["N"]) for b in bufs)
-    value = world * step_wbytes / (ms_step * 1e-3) / 1e9
-    tflops = world * flops_step / (ms_step * 1e-3) / 1e12
+    # ---- every row on its own: a plain graph of n launches cycling over the matrix's copies (mean),
+    # then the same launches with an event pair around each (median, p10, p90 of single launches)
+    n = max(args.launches, 20)
+    have_ext = True
+    rows = []
+    for it in items:
+        R = len(mats[it["name"]]["copies"])
+        g = capture(lambda it=it: [launch(it, i % R) for i in range(n)])
+        g.replay()
+        mean_us = timed(g.replay) / n * 1e3
+        del g
+        per = []
+        if have_ext:
+            try:
+                evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
 
-    # ---- dominant kernel roofline (the matrix with the longest launches)
-    j = int(np.argmax(kernel_ms))
-    b = bufs[j]
-    alg = weight_bytes(b["K"], b["N"]) + activation_bytes(b["M"], b["K"], b["N"])
-    fl = gemm_flops(b["M"], b["K"], b["N"])
-    t_k = kernel_ms[j] * 1e-3
-    # arithmetic intensity decides which roof binds: ridge = peak flops / peak bytes
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if fl / alg < ridge:
+                def evloop(it=it, evs=evs):
+                    for i in range(n):
+                        evs[i].record()
+                        launch(it, i % R)
+                    evs[n].record()
+
+                g = capture(evloop)
+                g.replay()
+                torch.cuda.synchronize()
+                per = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(n)]
+                del g
+            except (TypeError, RuntimeError):
+                have_ext = False
+                per = []
+        M, K, N = it["M"], it["K"], it["N"]
+        t_mem, t_tc = roofline_seconds(M, K, N, peaks)
+        wb = mats[it["name"]]["wb"]
+        rows.append(dict(matrix=it["name"], M=M, K=K, N=N, us=mean_us,
+                         us_median=statistics.median(per) if per else None,
+                         us_p10=percentile(per, 10) if per else None, us_p90=percentile(per, 90) if per else None,
+                         weight_gbs=wb / (mean_us * 1e-6) / 1e9, tflops=gemm_flops(M, K, N) / (mean_us * 1e-6) / 1e12,
+                         roofline_frac=max(t_mem, t_tc) / (mean_us * 1e-6), bound="hbm" if t_mem >= t_tc else "tensor",
+                         plan=it["plan"]))
+    st = W.w4a16_device_status()
+    if st != W.OK:
+        raise RuntimeError(f"device status after the per-row timing: {W.status_string(st)}")
+
+    # ---- one cold launch (L2 flushed by a write larger than L2, then one launch outside any graph)
+    flush = torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
+    cold = {}
+    for it in items:
+        if it["M"] != 1 and args.workload == "sweep":
+            continue
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        cold[f"{it['name']} M={it['M']}"] = timed(lambda it=it: launch(it, 0)) * 1e3
+    del flush
+
+    # ---- dominant kernel: the row with the largest share of the step
+    j = int(np.argmax([r["us"] for r in rows]))
+    r = rows[j]
+    alg = weight_bytes(r["K"], r["N"]) + activation_bytes(r["M"], r["K"], r["N"])
+    fl = gemm_flops(r["M"], r["K"], r["N"])
+    t_k = r["us"] * 1e-6
+    if r["bound"] == "hbm":
         roof = {"bound": "hbm", "achieved": alg / t_k / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         roof = {"bound": "tensor", "achieved": fl / t_k / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"], roof["traffic_source"] = measured_traffic(plans[j])
-    roof["kernel"] = plans[j]
-    roof["us_per_launch"] = kernel_ms[j] * 1e3
+    roof["traffic"], roof["traffic_source"] = measured_traffic(r["plan"])
+    roof["kernel"] = r["plan"]
+    roof["us_per_launch"] = r["us"]
+    roof["share_of_step"] = r["us"] / (ms_step * 1e3)
     roof["algorithmic_bytes"] = alg
-    roof["peak_source"] = peaks["source"] + (" (burst copy)" if roof["bound"] == "hbm" else " (bf16 burst; fp16 same rate)")
+    roof["algorithmic_flops"] = fl
+    roof["peak_source"] = peaks["source"] + (" (burst copy)" if roof["bound"] == "hbm"
+                                             else " (bf16 cuBLAS burst; fp16 runs at the same tensor rate)")
+    t_roof_step = sum(max(*roofline_seconds(x["M"], x["K"], x["N"], peaks)) for x in rows)
 
-    # ---- end to end through the C ABI with host buffers: w4a16_gemm_host queues, per matrix, the
-    # copy of x from pinned host memory, the GEMM and the copy of y back to pinned host memory
-    h2d = sum(bb["x"].numel() * 2 for bb in bufs)
-    d2h = sum(bb["y"].numel() * 2 for bb in bufs)
+    # ---- end to end through the C ABI with host buffers: per GEMM, w4a16_gemm_host queues the copy of
+    # x from pinned host memory, the GEMM and the copy of y back to pinned host memory
+    h2d = sum(it["xd"].numel() * 2 for it in items)
+    d2h = sum(it["yd"].numel() * 2 for it in items)
     stream = torch.cuda.current_stream().cuda_stream
-    calls = [[(bb["x_host"].data_ptr(), bb["x"].data_ptr(), qr.data_ptr(), sr.data_ptr(), bb["y"].data_ptr(),
-               bb["y_host"].data_ptr(), bb["M"], bb["N"], bb["K"], GROUP, stream) for (qr, sr) in bb["copies"]]
-             for bb in bufs]
+    calls = []
+    for it in items:
+        qr, sr = mats[it["name"]]["copies"][it["copy"]]
+        calls.append((it["x_host"].data_ptr(), it["xd"].data_ptr(), qr.data_ptr(), sr.data_ptr(),
+                      it["yd"].data_ptr(), it["y_host"].data_ptr(), it["M"], it["N"], it["K"], GROUP, stream))
 
-    def e2e_step(i: int):
+    def e2e_step():
         for c in calls:
-            rc = W.w4a16_gemm_host(*c[i % R])
+            rc = W.w4a16_gemm_host(*c)
             if rc != W.OK:
                 raise RuntimeError(f"w4a16_gemm_host: {W.status_string(rc)}")
 
-    for i in range(3):
-        e2e_step(i)
+    e2e_step()
     torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_ms = dist_max(dist, e0.elapsed_time(e1), dev) / args.steps
+    ne = max(1, args.e2e_steps)
+    e2e_ms = dist_max(dist, timed(e2e_step, ne), dev) / ne
     e2e = {"value": world * step_wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": ne}
+    st = W.w4a16_device_status()
+    if st != W.OK:
+        raise RuntimeError(f"device status after the end-to-end steps: {W.status_string(st)}")
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -458,89 +593,49 @@ def main():
         import oracle
 
         nthreads = oracle.default_threads()
-        cols = 256
-        gbs, el, reps = oracle_sample(mats, cols, args.cpu_seconds, nthreads)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
-               "sample": f"fp64 oracle on the first {cols} columns of each matrix, {reps} repetitions, {el:.1f} s"}
+        cols = 16 if args.workload == "sweep" else 256
+        gbs, el, reps = oracle_sample(items, cols, args.cpu_seconds, nthreads)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "cpu": cpu_model(),
+               "sample": f"fp64 oracle on the first {cols} columns of every matrix, every M row of every GEMM "
+                         f"of the step, {reps} repetitions, {el:.1f} s",
+               "single_thread": oracle_single_thread_configs()}
 
-    if args.sweep and rank == 0:
-        sweep(W, dev, peaks, l2)
+    if args.table and rank == 0:
+        print(f"{'matrix':8s} {'M':>5s} {'us':>9s} {'med':>8s} {'p10':>8s} {'p90':>8s} {'wGB/s':>7s} "
+              f"{'TFLOP/s':>8s} {'roof%':>6s} bound  plan", file=sys.stderr)
+        for x in rows:
+            f = lambda v: f"{v:8.2f}" if v is not None else "       -"  # noqa: E731
+            print(f"{x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} {f(x['us_median'])} {f(x['us_p10'])} "
+                  f"{f(x['us_p90'])} {x['weight_gbs']:7.0f} {x['tflops']:8.1f} {100 * x['roofline_frac']:6.1f} "
+                  f"{x['bound']:6s} {x['plan']}", file=sys.stderr)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-                "config": workload_config(name, mats, extra={
-                    "l2": f"each step reads the next of {R} weight copies ({R * step_wbytes / 1e6:.0f} MB, "
-                          f"> 4x the {l2 / 1e6:.0f} MB L2)",
-                    "timing": "CUDA graph of K steps, CUDA events", "plans": plans,
+        layer = {}
+        if args.workload == "sweep":
+            total_wb = sum(weight_bytes(K, N) for (_, K, N) in inputs.SWEEP_MATRICES)
+            for M in inputs.SWEEP_M:
+                us = sum(x["us"] for x in rows if x["M"] == M)
+                layer[str(M)] = {"us": us, "weight_gbs": total_wb / (us * 1e-6) / 1e9}
+        flops_step = sum(gemm_flops(x["M"], x["K"], x["N"]) for x in rows)
+        line = {"metric": METRIC, "value": world * step_wbytes / (ms_step * 1e-3) / 1e9, "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                "data": "synthetic",
+                "config": dict(cfg, **{
+                    "l2": "inputs larger than L2: every launch reads its own weight copy; a matrix's copies cycle "
+                          f"through more than 4x the {l2 / 1e6:.0f} MB L2 (no flush needed)",
+                    "timing": "K replays of a CUDA graph of one step, CUDA events on the launching stream",
                     "parallelism": "replicas" if world > 1 else "single GPU"}),
-                "tflops": tflops, "us_per_matrix": [k * 1e3 for k in kernel_ms],
+                "value_is": "weight bytes streamed per step / step time (all GEMMs of the step)",
+                "tflops": world * flops_step / (ms_step * 1e-3) / 1e12,
+                "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
+                "layer_step": layer, "rows": rows, "cold_launch_us": cold,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * len(bufs), "clocks": clocks,
+                "gpu_launches": args.steps * len(items), "clocks": clocks,
                 "peaks": {k: v for k, v in peaks.items()}}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
-
-
-def sweep(W, dev, peaks, l2):
-    """Dense-layer sweep: every matrix at every M, L2-cold, CUDA-graph timed. Table on stderr."""
-    import torch
-
-    rows = []
-    reps = 50
-    layer_us = {}
-    for mname, K, N in inputs.SWEEP_MATRICES:
-        qweight, scales = inputs.generate_weights(K, N, GROUP, seed=inputs.SWEEP_SEED)
-        qw = torch.from_numpy(qweight).to(dev)
-        sc = torch.from_numpy(scales.view(np.int16)).to(dev)
-        wb = weight_bytes(K, N)
-        R = max(2, -(-4 * l2 // wb))
-        copies = [W.repack(qw, sc, GROUP) for _ in range(R)]
-        del qw, sc
-        for M in inputs.SWEEP_M:
-            x = torch.from_numpy(inputs.generate_x(M, K, seed=1000 + M).view(np.int16)).view(torch.float16).to(dev)
-            y = torch.empty((M, N), dtype=torch.float16, device=dev)
-            for i in range(3):
-                W.gemm(x, copies[i % R][0], copies[i % R][1], N, K, GROUP, y=y)
-            plan = W.w4a16_last_dispatch()
-            g = torch.cuda.CUDAGraph()
-            s = torch.cuda.Stream(device=dev)
-            s.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
-                for i in range(reps):
-                    W.gemm(x, copies[i % R][0], copies[i % R][1], N, K, GROUP, y=y)
-            g.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            g.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) / reps * 1e3
-            alg = wb + activation_bytes(M, K, N)
-            fl = gemm_flops(M, K, N)
-            t_mem = alg / (peaks["hbm_gbs"] * 1e9)
-            t_tc = fl / (peaks["bf16_tflops"] * 1e12)
-            frac = max(t_mem, t_tc) / (us * 1e-6)
-            rows.append(dict(matrix=mname, K=K, N=N, M=M, us=us, weight_gbs=wb / (us * 1e-6) / 1e9,
-                             tflops=fl / (us * 1e-6) / 1e12, roofline_frac=frac,
-                             bound="hbm" if t_mem >= t_tc else "tensor", plan=plan))
-            layer_us[M] = layer_us.get(M, 0.0) + us
-            del g
-        del copies
-        torch.cuda.empty_cache()
-    print(f"{'matrix':8s} {'M':>5s} {'us':>9s} {'wGB/s':>8s} {'TFLOP/s':>8s} {'roof%':>6s} bound  plan",
-          file=sys.stderr)
-    for r in rows:
-        print(f"{r['matrix']:8s} {r['M']:5d} {r['us']:9.2f} {r['weight_gbs']:8.0f} {r['tflops']:8.1f} "
-              f"{100 * r['roofline_frac']:6.1f} {r['bound']:6s} {r['plan']}", file=sys.stderr)
-    total_wb = sum(weight_bytes(K, N) for _, K, N in inputs.SWEEP_MATRICES)
-    for M in inputs.SWEEP_M:
-        print(f"layer step M={M:5d}: {layer_us[M]:9.2f} us  ({total_wb / (layer_us[M] * 1e-6) / 1e9:7.0f} weight GB/s)",
-              file=sys.stderr)
-    print("SWEEP_JSON " + json.dumps({"rows": rows, "layer_us": layer_us}), file=sys.stderr)
 
 
 if __name__ == "__main__":

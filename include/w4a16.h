@@ -27,9 +27,11 @@
  *     call launches nothing and leaves every buffer untouched.
  *   - Supported shapes: N % 32 == 0, K % 64 == 0, group % 32 == 0, K % group == 0,
  *     1 <= M <= 2^20, N <= 2^23, K <= 2^22. x, y, qweight and scales 16-byte aligned.
- *     x and y must not overlap. The tensor-core paths (M > 8, or M >= 2 with automatic plans)
- *     also need K % 128 == 0 and group dividing 128 or a multiple of it (32, 64, 128, 256,
- *     384, ...); for M <= 8 the automatic plan takes the CUDA-core GEMV when they do not.
+ *     x and y must not overlap. The tensor-core path (M > 8, or M >= 2 with automatic plans)
+ *     also needs K % 128 == 0 and group dividing 128 or a multiple of it (32, 64, 128, 256,
+ *     384, ...). Shapes that miss that condition run on the CUDA-core GEMV, which needs M <= 8
+ *     and stages its slice of x in shared memory: M*K <= 1,500,000 always fits. Any other
+ *     shape in the set above gets an automatic plan.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -53,22 +55,20 @@ typedef enum {
 /* Which kernel family runs a GEMM. */
 typedef enum {
     W4A16_PATH_AUTO = 0, /* the dispatcher decides from (M, N, K) */
-    W4A16_PATH_GEMV = 1,  /* CUDA-core split-K GEMV, M <= 8 */
-    W4A16_PATH_TC = 2,    /* tcgen05 tensor-core tiles, any M */
-    W4A16_PATH_STREAM = 3, /* persistent tcgen05 streaming kernel, M <= 64 (x resident on chip) */
-    W4A16_PATH_GEMV_TMA = 4 /* CUDA-core GEMV fed by TMA through a shared-memory ring, M <= 4 */
+    W4A16_PATH_GEMV = 1, /* CUDA-core split-K GEMV, M <= 8 */
+    W4A16_PATH_TC = 2    /* tcgen05 tensor-core tiles, any M */
 } w4a16_path;
 
 /* A launch plan. Zero fields mean "choose automatically". */
 typedef struct {
     int path;        /* w4a16_path */
     int split_k;     /* CTAs of one thread-block cluster splitting K (1..16) */
-    int m_tile;      /* TC, STREAM: activation rows per tile: 16, 32, 64 (STREAM), 128, 256 (TC) */
-    int k_chunk;     /* TC, STREAM, GEMV_TMA: K per pipeline stage, 128 or 256 */
-    int stages;      /* TC, STREAM, GEMV_TMA: shared-memory pipeline depth, 2..16 */
-    int tmem_stages; /* TC, STREAM: tensor-memory (dequantised A) pipeline depth, 2..8 */
+    int m_tile;      /* TC: activation rows per tile: 16, 32, 64, 128, 256 */
+    int k_chunk;     /* TC: K per pipeline stage, 128 or 256 */
+    int stages;      /* TC: shared-memory pipeline depth, 2..16 */
+    int tmem_stages; /* TC: tensor-memory (dequantised A) pipeline depth, 2..8 */
     int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
-    int clusters;    /* STREAM: persistent thread-block clusters (each walks every clusters-th tile) */
+    int clusters;    /* reserved, must be 0 */
     int dequant_warps; /* TC: 16, or 8 (m_tile <= 64, k_chunk 128: half-size CTAs, two per SM) */
 } w4a16_plan;
 
@@ -154,10 +154,14 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
 int w4a16_last_dispatch(char* buf, size_t len);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status word. Kernels set it
- * when a bounded wait runs out (W4A16_ERR_DEVICE_TIMEOUT) instead of hanging; the CUDA context
- * stays usable. Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT, or W4A16_ERR_CUDA if the
- * synchronisation itself failed.
+ * Reads and clears the current device's status word, after the work queued on `stream` before the
+ * call. Kernels set the word when a bounded wait runs out (W4A16_ERR_DEVICE_TIMEOUT) instead of
+ * hanging; the CUDA context stays usable. The word is per DEVICE, not per stream: a timeout of a
+ * kernel on any stream of the device is reported by the next read. The read and the clear are one
+ * atomic exchange on the device (queued on `stream`), so a timeout recorded concurrently by a
+ * kernel on another stream is never lost: it is either returned now or by the next call. The call
+ * then synchronises `stream`. Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT, or W4A16_ERR_CUDA if the
+ * launch, copy or synchronisation failed.
  */
 int w4a16_device_status(void* stream);
 

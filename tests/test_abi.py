@@ -156,6 +156,24 @@ def test_every_supported_shape_gets_a_plan(W):
             assert 2 <= p.stages <= 16 and p.m_tile in (16, 32, 64, 128, 256)
 
 
+def test_boundary_shapes_get_plans(W):
+    # the corners of the advertised set: widest N, longest K, most rows, and the GEMV-only shapes
+    # (K % 128 != 0) at the documented M * K <= 1,500,000
+    for (M, N, K, G) in [(1, 1 << 23, 5120, 128), (1, 5120, 1 << 22, 128), (8, 5120, 1 << 22, 128),
+                         (1 << 20, 1 << 23, 1 << 22, 128), (1 << 20, 32, 128, 128), (1, 1 << 23, 1 << 22, 128),
+                         (1, 256, 1_499_968, 64), (8, 256, 187_456, 64), (3, 1 << 23, 1216, 64)]:
+        p = W.w4a16_plan_for(M, N, K, G)
+        assert p.path in (W.PATH_GEMV, W.PATH_TC), (M, N, K, G)
+        if p.path == W.PATH_GEMV:
+            assert M <= 8 and 1 <= p.split_k <= 16
+        else:
+            assert K % p.k_chunk == 0 and -(-M // p.m_tile) <= 65535
+    with pytest.raises(W.W4A16Error):
+        W.w4a16_plan_for(1, (1 << 23) + 32, 5120, 128)
+    with pytest.raises(W.W4A16Error):
+        W.w4a16_plan_for(1, 5120, (1 << 22) + 128, 128)
+
+
 def _plan_in_subprocess(env_value):
     import subprocess
     import sys

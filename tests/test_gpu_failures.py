@@ -41,17 +41,16 @@ def test_bounded_wait_reports_timeout_and_context_survives(W, mode):
     finally:
         assert W.w4a16_set_wait_timeout_ns(2_000_000_000) == W.OK
     x, qw_r, sc_r, y_ref, abs_ref, K, N, G = _small_case(W)
-    for plan in (dict(path=1), dict(path=2), dict(path=3), dict(path=4)):
+    for plan in (dict(path=1), dict(path=2)):
         y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
         assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
 
 
 @pytest.mark.parametrize("plan", [dict(path=1), dict(path=1, split_k=3), dict(path=2), dict(path=2, split_k=3),
-                                  dict(path=2, m_tile=128), dict(path=3), dict(path=3, split_k=2, clusters=2),
-                                  dict(path=4), dict(path=4, split_k=3)],
+                                  dict(path=2, m_tile=128)],
                          ids=lambda p: "-".join(f"{k}{v}" for k, v in p.items()))
 def test_no_writes_outside_y(W, plan):
-    M = 3 if plan["path"] in (1, 4) else 17
+    M = 3 if plan["path"] == 1 else 17
     x, qw_r, sc_r, y_ref, abs_ref, K, N, G = _small_case(W, M=M, seed=52 + M)
     pad = 4096  # fp16 elements (8 KB) of canary on each side
     canary = 0x7BAD  # a finite fp16 bit pattern no kernel produces here

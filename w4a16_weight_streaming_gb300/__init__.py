@@ -29,8 +29,6 @@ ERR_DEVICE_TIMEOUT = 5
 PATH_AUTO = 0
 PATH_GEMV = 1
 PATH_TC = 2
-PATH_STREAM = 3
-PATH_GEMV_TMA = 4
 
 # every symbol include/w4a16.h declares
 EXPORTED = [

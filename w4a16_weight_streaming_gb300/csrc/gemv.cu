@@ -74,8 +74,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     extern __shared__ __align__(16) unsigned char smem[];
     const int KB = K / 32;
     const int NG = K / G;
-    const int rank = blockIdx.x;
-    const int t = blockIdx.y;           // 32-column slice: columns 32t .. 32t + 31
+    // grid.x = slices x split, one cluster of `split` consecutive CTAs per 32-column slice
+    const int rank = static_cast<int>(blockIdx.x) % split;
+    const int t = static_cast<int>(blockIdx.x) / split;  // 32-column slice: columns 32t .. 32t + 31
     const int tile = t / 4;             // 128-column tile of the streaming layout
     const int wt = min(128, N - 128 * tile);
     const int cofs = 32 * (t % 4);      // slice offset inside the tile
@@ -181,7 +182,7 @@ cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const ui
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(split, N / 32, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(split) * static_cast<unsigned>(N / 32), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

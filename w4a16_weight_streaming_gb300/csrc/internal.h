@@ -29,14 +29,7 @@ size_t gemv_smem_bytes(int M, int N, int K, int split);
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                         int N, int K, int G, int split, const LaunchCtx& ctx);
 
-// ---- gemv_tma.cu: TMA-fed CUDA-core GEMV, M <= 4 (k_chunk 128 or 256 rows of k per stage).
-constexpr int kGemvTmaMaxM = 4;
-size_t gemv_tma_smem_bytes(int M, int K, int G, int KC, int split, int stages);
-int gemv_tma_resident_ctas(int M, int N, int K, int G, int KC, int split, int stages);
-cudaError_t launch_gemv_tma(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
-                            int M, int N, int K, int G, int KC, int split, int stages, const LaunchCtx& ctx);
-
-// ---- tc_gemm.cu: the x operand's tensor map (shared by both tensor-core kernels). x viewed as
+// ---- tc_gemm.cu: the x operand's tensor map. x viewed as
 // [K/64 blocks][M rows][64 k]; one box = one stage tile [KC/64][MT][64] in the MMA's 128-byte-swizzle
 // K-major layout; rows >= M read as zero. Falls back to a 2-D map when the driver refuses the 3-D one.
 bool encode_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int MT, int KC, bool* three_d);
@@ -59,25 +52,5 @@ int tc_tmem_cols(const TcConfig& c);
 int tc_resident_ctas(const TcConfig& c, int G);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
-
-// ---- tc_stream.cu: persistent tcgen05 streaming kernel for M <= 64 (x resident in shared memory).
-struct StreamConfig {
-    int m_tile;       // 16, 32 or 64 (>= M)
-    int k_chunk;      // K per stage: 128 or 256
-    int stages;       // shared-memory ring depth, 2..16
-    int tmem_stages;  // TMEM A ring depth, 2..8
-    int split;        // CTAs per cluster along K, 1..16
-    int clusters;     // persistent clusters (grid y)
-    int issuers;      // MMA-issuing threads, each with its own accumulator: 2 or 4
-    int dbuf;         // accumulator buffers (2: the epilogue of a tile overlaps the next tile's MMAs)
-};
-bool stream_instantiated(int m_tile, int k_chunk, int issuers);
-int stream_tmem_columns(const StreamConfig& c);
-bool stream_config_valid(const StreamConfig& c, int M, int N, int K, int G);
-size_t stream_smem_bytes(const StreamConfig& c, int G, int K);
-// Clusters of this config resident on the current device at once (0 if unknown).
-int stream_max_clusters(const StreamConfig& c, int G, int K);
-cudaError_t launch_stream(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
-                          int N, int K, int G, const StreamConfig& c, const LaunchCtx& ctx);
 
 }  // namespace w4a16

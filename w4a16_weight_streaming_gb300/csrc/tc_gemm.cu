@@ -132,7 +132,7 @@ template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW>
 __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
-                   int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
+                   int split, int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
     static_assert(NA == 1 || NA == 2 || NA == 4, "1, 2 or 4 accumulators");
@@ -153,7 +153,6 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    const int split = gridDim.x;
     const SmemPlan P = make_plan(MT, KC, s_stages, a_stages, G, split);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + P.bar_off;
@@ -193,11 +192,12 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(a_stages * kACols);
 
-    const int rank = blockIdx.x;
-    const int tile = blockIdx.y;
+    // grid.x = column tiles x split (one cluster of `split` consecutive CTAs per tile), grid.y = row tiles
+    const int rank = static_cast<int>(blockIdx.x) % split;
+    const int tile = static_cast<int>(blockIdx.x) / split;
     const int n0 = tile * kTileN;
     const int wt = min(kTileN, N - n0);  // columns of this tile (32, 64, 96 or 128)
-    const int m0 = blockIdx.z * MT;
+    const int m0 = static_cast<int>(blockIdx.y) * MT;
     const int KB = K / 32;
     const int NG = K / G;
     const int ngs = groups_per_stage(KC, G);
@@ -449,6 +449,14 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
 
     __syncthreads();
     if (warp == kProducerWarp) {
+        // Every issuer commits dfull after its loop, also when it left early, so this phase
+        // completes once the MMAs in flight (reading the x stages and writing TMEM) have drained.
+        // After an abort the epilogue did not wait for it; wait here, with a private abort flag and
+        // still bounded, before shared memory and TMEM are released.
+        if (lane == 0) {
+            int drain_abort = 0;
+            mbar_wait(dfull_bar, 0, &drain_abort, timeout_ns, status);
+        }
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
@@ -478,7 +486,8 @@ template <int MT, int KC, int NI, bool GI, int DW>
 cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(c.split, (N + kTileN - 1) / kTileN, (M + MT - 1) / MT);
+    cfg.gridDim = dim3(static_cast<unsigned>(c.split) * static_cast<unsigned>((N + kTileN - 1) / kTileN),
+                       static_cast<unsigned>((M + MT - 1) / MT), 1);
     cfg.blockDim = dim3(threads_for(GI, NI, DW), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -501,7 +510,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(c, M, N, smem, ctx.stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
-                              c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
+                              c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
 }
 
 // CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.
@@ -585,9 +594,9 @@ bool tc_instantiated(int m_tile, int k_chunk, int issuers, int dequant_warps) {
 }
 
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
-    (void)M;
     (void)N;
     if (c.m_tile != 16 && c.m_tile != 32 && c.m_tile != 64 && c.m_tile != 128 && c.m_tile != 256) return false;
+    if ((M + c.m_tile - 1) / c.m_tile > 65535) return false;  // row tiles are grid.y
     if (c.k_chunk != 128 && c.k_chunk != 256) return false;
     if (K % c.k_chunk != 0) return false;
     if (c.stages < 2 || c.stages > 16) return false;

@@ -18,9 +18,10 @@
 
 namespace w4a16 {
 
-// The one piece of device state: a status word per device, set by kernels whose bounded waits
-// ran out, read and cleared by w4a16_device_status.
+// The device state: a status word per device, set by kernels whose bounded waits ran out, and
+// the word w4a16_device_status copies its value through (read and cleared in one atomic step).
 __device__ unsigned g_status_word;
+__device__ unsigned g_status_taken;
 
 namespace {
 
@@ -29,6 +30,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool ready = false;
     unsigned* status = nullptr;
+    unsigned* taken = nullptr;
     int sm_count = 0;
 };
 
@@ -46,10 +48,13 @@ bool device_info(DeviceInfo* out) {
     DeviceInfo& d = g_dev[dev];
     if (!d.ready) {
         void* p = nullptr;
+        void* t = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(&t, g_status_taken) != cudaSuccess) return false;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         d.status = static_cast<unsigned*>(p);
+        d.taken = static_cast<unsigned*>(t);
         d.sm_count = sms;
         d.ready = true;
     }
@@ -97,9 +102,7 @@ int check_matrix_shape(int N, int K, int G) {
 struct Choice {
     int path;
     TcConfig tc;
-    StreamConfig st;
     int gemv_split;
-    int gt_kc, gt_stages;  // GEMV_TMA: stage K and ring depth (split in gemv_split)
 };
 
 // Split along K for the CUDA-core GEMV: enough 128-thread CTAs to cover every SM about four
@@ -112,6 +115,8 @@ int gemv_pick_split(int M, int N, int K, int sm_count) {
     while (split < 16 && gemv_smem_bytes(M, N, K, split) > 96 * 1024) split *= 2;
     return std::min(split, std::max(1, KB));
 }
+
+constexpr size_t kGemvMaxSmem = 200 * 1024;  // the GEMV's dynamic shared memory limit
 
 bool group_fits(int KC, int G) { return KC >= G ? KC % G == 0 : G % KC == 0; }
 
@@ -192,105 +197,6 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) 
     c.stages = fill_stages(c, G, 225 * 1024, 8);
     c.split = pick_split(c, M, N, K, G, sm_count, have_device);
     return c;
-}
-
-// ---- persistent streaming kernel (M <= 64)
-int stream_m_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
-
-// MMA issuers: one thread issues a tcgen05.mma only every ~110 cycles while the tensor pipe takes one
-// per ~40; each issuer owns an accumulator of m_tile TMEM columns.
-int stream_default_issuers(int m_tile) { return m_tile <= 32 ? 4 : 2; }
-
-// TMEM A ring depth (at most 7: two named barriers per stage) and accumulator buffering: two buffers (the epilogue
-// of a tile overlaps the next tile's MMAs) when that still leaves a ring of at least 3 (or the
-// requested depth), else one.
-void stream_tmem_layout(StreamConfig* c, int want_stages) {
-    for (int dbuf = 2; dbuf >= 1; --dbuf) {
-        const int room = (512 - dbuf * c->issuers * c->m_tile) / (c->k_chunk / 2);
-        const int a = want_stages > 0 ? want_stages : std::min(7, room);
-        if (a <= room && a >= (want_stages > 0 ? 2 : 3)) {
-            c->dbuf = dbuf;
-            c->tmem_stages = a;
-            return;
-        }
-    }
-    c->dbuf = 1;
-    c->tmem_stages = want_stages > 0 ? want_stages : std::min(7, (512 - c->issuers * c->m_tile) / (c->k_chunk / 2));
-}
-
-// Deepest shared-memory ring (at most `max_stages`) that fits next to the resident x slice and
-// the split-K partial tiles; 0 if not even two stages fit.
-int stream_fill_stages(StreamConfig c, int K, int G, int max_stages) {
-    int best = 0;
-    for (int s = 2; s <= max_stages; ++s) {
-        c.stages = s;
-        if (stream_smem_bytes(c, G, K) <= 225 * 1024) best = s;
-    }
-    return best;
-}
-
-// Split along K and number of persistent clusters. Each cluster walks ceil(tiles / clusters) tiles of
-// ceil(C / split) stages each; the clusters the device holds at once come from the driver's cluster
-// occupancy (clusters live inside one GPC, so some sizes leave SMs idle); without a device, the SM
-// count. A small cost per tile (epilogue hand-off) and per cluster rank (reduction) breaks ties.
-bool stream_pick(StreamConfig* io, int M, int N, int K, int G, int sm_count, bool have_device, int force_split,
-                 int force_stages, int force_clusters) {
-    (void)M;
-    const int tiles = (N + 127) / 128;
-    const int C = K / io->k_chunk;
-    double best = 1e30;
-    StreamConfig best_c = *io;
-    bool found = false;
-    for (int s = 1; s <= 16 && s <= C; ++s) {
-        if (force_split > 0 && s != force_split) continue;
-        StreamConfig c = *io;
-        c.split = s;
-        c.clusters = 1;
-        c.stages = force_stages > 0 ? force_stages : stream_fill_stages(c, K, G, 12);
-        if (c.stages < 2) continue;
-        int slots = have_device ? stream_max_clusters(c, G, K) : sm_count / s;
-        if (slots <= 0) continue;
-        c.clusters = force_clusters > 0 ? force_clusters : std::min(slots, tiles);
-        const int per_cluster = (tiles + c.clusters - 1) / c.clusters;
-        const int per_cta = (C + s - 1) / s;
-        // weight bytes in flight per CTA: below ~96 KB the stream slows down (measured on GB300)
-        const double ring = static_cast<double>(c.stages) * io->k_chunk * 64.0;
-        const double eff = std::min(1.0, ring / 98304.0);
-        const double cost =
-            static_cast<double>(per_cluster) * (per_cta * (io->k_chunk / 256.0) + 0.3) / eff + 0.05 * s;
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_c = c;
-            found = true;
-        }
-    }
-    if (found) *io = best_c;
-    return found;
-}
-
-// ---- TMA-fed GEMV: K-slices per tile from the cluster occupancy (waves x stages per CTA).
-int gemv_tma_pick_split(int M, int N, int K, int G, int KC, int stages, int sm_count, bool have_device,
-                        int force_split) {
-    const int tiles = (N + 127) / 128;
-    const int R = KC / 32;
-    const int C = (K / 32 + R - 1) / R;
-    double best = 1e30;
-    int split = 0;
-    for (int s = 1; s <= 16 && s <= C; ++s) {
-        if (force_split > 0 && s != force_split) continue;
-        if (gemv_tma_smem_bytes(M, K, G, KC, s, stages) > 225 * 1024) continue;
-        int slots = have_device ? gemv_tma_resident_ctas(M, N, K, G, KC, s, stages) : 0;
-        if (slots <= 0) slots = have_device ? 0 : (2 * sm_count / s) * s;
-        if (slots <= 0) continue;
-        const int waves = (tiles * s + slots - 1) / slots;
-        const int per_cta = (C + s - 1) / s;
-        const double cost = static_cast<double>(waves) * (per_cta + 1.5) + 0.1 * s;
-        if (cost < best - 1e-9) {
-            best = cost;
-            split = s;
-        }
-    }
-    return split;
 }
 
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
@@ -381,13 +287,11 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
                           Choice* out) {
     w4a16_plan p = {};
     if (plan) p = *plan;
-    if (p.path < 0 || p.path > 4) return W4A16_ERR_INVALID_ARG;
+    if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
     if (path == W4A16_PATH_AUTO) {
         // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one
-        // activation row; from 3 rows on the tcgen05 tiles. (The persistent streaming kernel is
-        // still slower than the tiles on every measured decode / verify shape and is only run when a
-        // plan asks for it.)
+        // activation row; from 3 rows on the tcgen05 tiles.
         // At two rows the GEMV wins only on the smaller matrices (5120 x 5120, 5120 x 7168); on
         // 5120 x 34816 and 17408 x 5120 the tiles are 1-2 us faster.
         const bool small = static_cast<int64_t>(K) * N < (int64_t{64} << 20);
@@ -395,45 +299,18 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         // The tile kernels run whole 128-k stages and stage whole scale groups per stage; a K that
         // is not a multiple of 128, or a group that neither divides nor is a multiple of 128
         // (96, 160, ...), goes to the GEMV, which works in 32-k rows with one scale each.
-        if (path == W4A16_PATH_TC && (K % 128 != 0 || !group_fits(128, G)) && M <= kGemvMaxM)
-            path = W4A16_PATH_GEMV;
+        const bool tc_ok = K % 128 == 0 && group_fits(128, G);
+        if (path == W4A16_PATH_TC && !tc_ok && M <= kGemvMaxM) path = W4A16_PATH_GEMV;
+        // The GEMV stages its K-slice of x in shared memory: for very long K (even at the largest
+        // split) the tiles, which stream x per stage, take over when they can.
+        if (path == W4A16_PATH_GEMV && tc_ok && gemv_smem_bytes(M, N, K, 16) > kGemvMaxSmem) path = W4A16_PATH_TC;
     }
     out->path = path;
-    if (path == W4A16_PATH_GEMV_TMA) {
-        if (M > kGemvTmaMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        const int kc = p.k_chunk > 0 ? p.k_chunk : 256;
-        const int stages = p.stages > 0 ? p.stages : 4;
-        if (kc != 128 && kc != 256) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        if (stages < 2 || stages > 16) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        const int split = gemv_tma_pick_split(M, N, K, G, kc, stages, sm_count, have_device, p.split_k);
-        if (split < 1) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        out->gemv_split = split;
-        out->gt_kc = kc;
-        out->gt_stages = stages;
-        return W4A16_OK;
-    }
-    if (path == W4A16_PATH_STREAM) {
-        if (M > 64) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        StreamConfig c;
-        c.m_tile = p.m_tile > 0 ? p.m_tile : stream_m_tile(M);
-        c.k_chunk = p.k_chunk > 0 ? p.k_chunk : (K % 256 == 0 && group_fits(256, G) ? 256 : 128);
-        c.issuers = p.mma_issuers > 0 ? p.mma_issuers : stream_default_issuers(c.m_tile);
-        if (!stream_instantiated(c.m_tile, c.k_chunk, c.issuers)) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        stream_tmem_layout(&c, p.tmem_stages);
-        c.stages = 2;
-        c.split = 1;
-        c.clusters = 1;
-        if (!stream_pick(&c, M, N, K, G, sm_count, have_device, p.split_k, p.stages, p.clusters))
-            return W4A16_ERR_UNSUPPORTED_SHAPE;
-        if (!stream_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        out->st = c;
-        return W4A16_OK;
-    }
     if (path == W4A16_PATH_GEMV) {
         if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
         int split = p.split_k > 0 ? p.split_k : gemv_pick_split(M, N, K, sm_count);
         if (split < 1 || split > 16 || split > K / 32) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        if (gemv_smem_bytes(M, N, K, split) > 200 * 1024) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        if (gemv_smem_bytes(M, N, K, split) > kGemvMaxSmem) return W4A16_ERR_UNSUPPORTED_SHAPE;
         out->gemv_split = split;
         return W4A16_OK;
     }
@@ -497,6 +374,10 @@ __global__ void wait_timeout_selftest_kernel(unsigned* status, uint64_t timeout_
     __syncwarp();
 }
 
+// Moves the status word into `taken` and clears it in one atomic exchange, so that a timeout
+// recorded concurrently by a kernel on another stream is either taken now or left for the next read.
+__global__ void take_status_kernel(unsigned* status, unsigned* taken) { *taken = atomicExch(status, 0u); }
+
 }  // namespace
 }  // namespace w4a16
 
@@ -536,35 +417,17 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
     if (ch.path == W4A16_PATH_GEMV) {
         e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                         group, ch.gemv_split, ctx);
-        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%d,%d,1) block=128", M, N, K,
-                 group, ch.gemv_split, ch.gemv_split, N / 32);
-    } else if (ch.path == W4A16_PATH_GEMV_TMA) {
-        e = launch_gemv_tma(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
-                            K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages, ctx);
-        snprintf(desc, sizeof(desc),
-                 "path=gemv_tma M=%d N=%d K=%d group=%d k_chunk=%d stages=%d split_k=%d grid=(%d,%d,1) block=288 "
-                 "smem=%zu",
-                 M, N, K, group, ch.gt_kc, ch.gt_stages, ch.gemv_split, ch.gemv_split, (N + 127) / 128,
-                 gemv_tma_smem_bytes(M, K, group, ch.gt_kc, ch.gemv_split, ch.gt_stages));
-    } else if (ch.path == W4A16_PATH_STREAM) {
-        e = launch_stream(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
-                          K, group, ch.st, ctx);
-        snprintf(desc, sizeof(desc),
-                 "path=stream M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "acc_buffers=%d split_k=%d clusters=%d grid=(%d,%d,1) tmem_cols=%d smem=%zu",
-                 M, N, K, group, ch.st.m_tile, ch.st.k_chunk, ch.st.stages, ch.st.tmem_stages, ch.st.issuers,
-                 ch.st.dbuf, ch.st.split, ch.st.clusters, ch.st.split, ch.st.clusters, stream_tmem_columns(ch.st),
-                 stream_smem_bytes(ch.st, group, K));
+        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128", M, N, K,
+                 group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32));
     } else {
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
                  "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "dequant_warps=%d split_k=%d grid=(%d,%d,%d) tmem_cols=%d smem=%zu",
+                 "dequant_warps=%d split_k=%d grid=(%lld,%d,1) tmem_cols=%d smem=%zu",
                  M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
-                 ch.tc.dequant_warps, ch.tc.split,
-                 ch.tc.split,
-                 (N + 127) / 128, (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
+                 ch.tc.dequant_warps, ch.tc.split, static_cast<long long>(ch.tc.split) * ((N + 127) / 128),
+                 (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -658,19 +521,6 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
         out->m_tile = out->k_chunk = out->stages = out->tmem_stages = out->mma_issuers = 0;
-    } else if (ch.path == W4A16_PATH_GEMV_TMA) {
-        out->split_k = ch.gemv_split;
-        out->k_chunk = ch.gt_kc;
-        out->stages = ch.gt_stages;
-        out->m_tile = out->tmem_stages = out->mma_issuers = 0;
-    } else if (ch.path == W4A16_PATH_STREAM) {
-        out->split_k = ch.st.split;
-        out->m_tile = ch.st.m_tile;
-        out->k_chunk = ch.st.k_chunk;
-        out->stages = ch.st.stages;
-        out->tmem_stages = ch.st.tmem_stages;
-        out->mma_issuers = ch.st.issuers;
-        out->clusters = ch.st.clusters;
     } else {
         out->split_k = ch.tc.split;
         out->m_tile = ch.tc.m_tile;
@@ -732,13 +582,14 @@ int w4a16_device_status(void* stream) {
     DeviceInfo d;
     if (!device_info(&d)) return W4A16_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    take_status_kernel<<<1, 1, 0, s>>>(d.status, d.taken);
+    if (cudaGetLastError() != cudaSuccess) return W4A16_ERR_CUDA;
     unsigned v = 0;
-    if (cudaMemcpy(&v, d.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return W4A16_ERR_CUDA;
-    if (v != 0) {
-        const unsigned zero = 0;
-        if (cudaMemcpy(d.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, d.taken, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
     }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
     return v == 0 ? W4A16_OK : static_cast<int>(v);
 }
 
