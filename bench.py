@@ -6,9 +6,7 @@ fused qkv, 5120 x 5120 o, 5120 x 34816 fused gate+up, 17408 x 5120 down; group 1
 M in {1, 2, 4, ..., 1024}. One step = one pass of the hot path over all 44 (M, matrix) GEMMs, in
 layer order (for each M: qkv, o, gate+up, down), each y = x . dequant(W) through the C ABI.
 `value` = weight bytes streamed per step / step time (effective weight-stream GB/s of the whole
-sweep); `tflops` likewise. Every GEMM goes through w4a16_gemm_ws with one workspace (the library
-allocates nothing; the buffer is allocated once here). `rows` gives every (matrix, M) launch on its
-own: mean us (plain CUDA
+sweep); `tflops` likewise; `rows` gives every (matrix, M) launch on its own: mean us (plain CUDA
 graph), median / p10 / p90 us (per-launch event pairs), weight GB/s, TFLOP/s, roofline fraction,
 bound and plan.
 
@@ -420,14 +418,11 @@ def main():
         it["copy"] = use_count[it["name"]]  # the step's own copy of this matrix for this GEMM
         use_count[it["name"]] += 1
         step_wbytes += mats[it["name"]]["wb"]
-    # one scratch buffer, the largest any row's automatic plan wants, zero-filled once (each call
-    # leaves its counters at zero again)
-    ws = W.new_workspace(max(W.w4a16_workspace_bytes(it["M"], it["N"], it["K"], GROUP) for it in items), dev)
     torch.cuda.synchronize()
 
     def launch(it, copy):
         qr, sr = mats[it["name"]]["copies"][copy]
-        W.gemm(it["xd"], qr, sr, it["N"], it["K"], GROUP, y=it["yd"], workspace=ws)
+        W.gemm(it["xd"], qr, sr, it["N"], it["K"], GROUP, y=it["yd"])
 
     def step():
         for it in items:
@@ -574,8 +569,7 @@ def main():
     for it in items:
         qr, sr = mats[it["name"]]["copies"][it["copy"]]
         calls.append((it["x_host"].data_ptr(), it["xd"].data_ptr(), qr.data_ptr(), sr.data_ptr(),
-                      it["yd"].data_ptr(), it["y_host"].data_ptr(), it["M"], it["N"], it["K"], GROUP,
-                      ws.data_ptr(), ws.numel(), stream))
+                      it["yd"].data_ptr(), it["y_host"].data_ptr(), it["M"], it["N"], it["K"], GROUP, stream))
 
     def e2e_step():
         for c in calls:

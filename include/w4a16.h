@@ -55,21 +55,20 @@ typedef enum {
 /* Which kernel family runs a GEMM. */
 typedef enum {
     W4A16_PATH_AUTO = 0, /* the dispatcher decides from (M, N, K) */
-    W4A16_PATH_GEMV = 1,   /* CUDA-core split-K GEMV, M <= 8 */
-    W4A16_PATH_TC = 2,     /* tcgen05 tensor-core tiles, any M */
-    W4A16_PATH_STREAMK = 3 /* persistent stream-K tcgen05 kernel, M <= 64; needs a workspace (w4a16_gemm_ws) */
+    W4A16_PATH_GEMV = 1, /* CUDA-core split-K GEMV, M <= 8 */
+    W4A16_PATH_TC = 2    /* tcgen05 tensor-core tiles, any M */
 } w4a16_path;
 
 /* A launch plan. Zero fields mean "choose automatically". */
 typedef struct {
     int path;        /* w4a16_path */
-    int split_k;     /* GEMV, TC: CTAs of one thread-block cluster splitting K (1..16) */
-    int m_tile;      /* TC: activation rows per tile: 16, 32, 64, 128, 256; STREAMK: 16, 32, 64 */
-    int k_chunk;     /* TC, STREAMK: K per pipeline stage, 128 or 256 */
-    int stages;      /* TC, STREAMK: shared-memory pipeline depth, 2..16 */
+    int split_k;     /* CTAs of one thread-block cluster splitting K (1..16) */
+    int m_tile;      /* TC: activation rows per tile: 16, 32, 64, 128, 256 */
+    int k_chunk;     /* TC: K per pipeline stage, 128 or 256 */
+    int stages;      /* TC: shared-memory pipeline depth, 2..16 */
     int tmem_stages; /* TC: tensor-memory (dequantised A) pipeline depth, 2..8 */
     int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
-    int ctas;        /* STREAMK: persistent CTAs, one per SM (at most the number of (tile, chunk) units) */
+    int clusters;    /* reserved, must be 0 */
     int dequant_warps; /* TC: 16, or 8 (m_tile <= 64, k_chunk 128: half-size CTAs, two per SM) */
 } w4a16_plan;
 
@@ -120,41 +119,9 @@ int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, u
                int group, void* stream);
 
 /* As w4a16_gemm with an explicit plan (NULL or zero fields = automatic). An invalid plan
- * (e.g. GEMV with M > 8, split_k larger than the K chunks) returns UNSUPPORTED_SHAPE; a STREAMK
- * plan, which needs a workspace, returns INVALID_ARG (use w4a16_gemm_ws). */
+ * (e.g. GEMV with M > 8, split_k larger than the K chunks) returns UNSUPPORTED_SHAPE. */
 int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                   int group, const w4a16_plan* plan, void* stream);
-
-/*
- * Bytes of scratch the automatic plan of w4a16_gemm_ws wants for this shape on the current device
- * (0 when that plan needs none, or the shape is unsupported). Host only.
- */
-size_t w4a16_workspace_bytes(int M, int N, int K, int group);
-
-/*
- * w4a16_gemm with a caller-owned scratch buffer, which lets the dispatcher use the persistent
- * stream-K kernel (M <= 64): every SM streams an equal share of the weights, and tiles shared by
- * two or more CTAs are summed through fp32 partial tiles kept in the workspace. The library still
- * allocates nothing.
- *   plan:            NULL (automatic) or as in w4a16_gemm_ex (STREAMK plans allowed).
- *   workspace:       device buffer of at least w4a16_workspace_bytes(M, N, K, group) bytes for the
- *                    automatic plan, 16-byte aligned, not overlapping x, y, qweight_r or scales_r;
- *                    NULL behaves as w4a16_gemm_ex.
- *                    It must be ZERO-FILLED before its first use (one cudaMemset after
- *                    allocation). Its first 256 KiB hold one counter per 128-column tile, and every
- *                    call that completes leaves those counters at zero again, so one buffer serves
- *                    any number of calls of any shapes in stream order. Calls that may run at the
- *                    same time (different streams) need different workspaces. After a
- *                    W4A16_ERR_DEVICE_TIMEOUT the workspace must be zero-filled again.
- *   workspace_bytes: its size; a plan whose need exceeds it returns INVALID_ARG.
- * The stream-K kernel is launched with programmatic dependent launch: it starts streaming the
- * weights of its first stages while the previous kernel on the stream finishes, and reads x and
- * writes y and the workspace only after that kernel has completed.
- * Errors: as w4a16_gemm, plus INVALID_ARG (workspace too small, overlapping, or a host pointer) and
- * MISALIGNED (workspace not 16-byte aligned).
- */
-int w4a16_gemm_ws(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
-                  int group, const w4a16_plan* plan, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * w4a16_gemm for activations and results in HOST memory, queued on `stream` as three operations:
@@ -165,7 +132,6 @@ int w4a16_gemm_ws(const uint16_t* x, const void* qweight_r, const void* scales_r
  *                   must not overlap. y_host is valid once `stream` has been synchronised.
  *   x_dev, y_dev:   caller-owned device buffers of M*K and M*N fp16 (16-byte aligned); the
  *                   library allocates nothing.
- *   workspace, workspace_bytes: as w4a16_gemm_ws (NULL, 0: the plans of w4a16_gemm).
  *   qweight_r, scales_r, M, N, K, group, stream: as w4a16_gemm.
  * Every check of w4a16_gemm (on x_dev, y_dev and the weights) runs before anything is queued, and
  * x_host / y_host are rejected (INVALID_ARG) when null, overlapping or known to the runtime as
@@ -173,17 +139,15 @@ int w4a16_gemm_ws(const uint16_t* x, const void* qweight_r, const void* scales_r
  * MISALIGNED, CUDA (a copy or launch refused; operations queued before it stay queued).
  */
 int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight_r, const void* scales_r,
-                    uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* workspace,
-                    size_t workspace_bytes, void* stream);
+                    uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* stream);
 
-/* The plan w4a16_gemm (with_workspace = 0) or w4a16_gemm_ws with a workspace (with_workspace = 1)
- * would use for this shape (host only; launches nothing).
+/* The plan w4a16_gemm would use for this shape (host only; launches nothing).
  * Automatic plans (w4a16_gemm, w4a16_gemm_host, w4a16_gemm_ex with NULL or all-zero plan, this
  * call) can be overridden without rebuilding: the environment variable W4A16_PLAN, read once per
  * process, holds "field=value[,field=value...]" with the w4a16_plan field names, no spaces
  * (e.g. "path=2,m_tile=64,split_k=3"). It is then used as the plan of every such call. A malformed
  * W4A16_PLAN makes them return INVALID_ARG; a plan invalid for a shape, UNSUPPORTED_SHAPE. */
-int w4a16_plan_for(int M, int N, int K, int group, int with_workspace, w4a16_plan* out);
+int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
 
 /* Describes the last GEMM this process launched (path, tile, split, grid) into buf (NUL
  * terminated, truncated to len). Host only. Returns W4A16_OK or INVALID_ARG. */

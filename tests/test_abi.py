@@ -88,7 +88,7 @@ def test_gemm_host_rejects_bad_arguments_on_host(W):
         a = list(ok)
         if i is not None:
             a[i] = v
-        return W.w4a16_gemm_host(*a, *(sh or shape), None, 0, None)
+        return W.w4a16_gemm_host(*a, *(sh or shape), None)
 
     assert call(0, 0) == 1                     # null x_host
     assert call(5, 0) == 1                     # null y_host
@@ -119,29 +119,6 @@ def test_plan_for_host_only(W):
             assert 2 <= p.tmem_stages <= 8
     with pytest.raises(W.W4A16Error):
         W.w4a16_plan_for(0, 5120, 5120, 128)
-
-
-def test_workspace_plans_host_only(W):
-    # with a workspace, M <= 64 takes the stream-K kernel (one CTA per SM, 152 without a device);
-    # its scratch is the fixed counter zone plus ctas x 2 partial tiles of m_tile x 128 fp32
-    sms = 152
-    for (M, mt) in [(1, 16), (16, 16), (17, 32), (64, 64)]:
-        p = W.w4a16_plan_for(M, 34816, 5120, 128, with_workspace=True)
-        assert p.path == W.PATH_STREAMK and p.m_tile == mt and p.k_chunk == 256 and p.ctas == sms
-        assert W.w4a16_workspace_bytes(M, 34816, 5120, 128) == 256 * 1024 + sms * 2 * mt * 128 * 4
-    assert W.w4a16_plan_for(16, 34816, 5120, 128).path != W.PATH_STREAMK  # no workspace, no stream-K
-    assert W.w4a16_plan_for(65, 34816, 5120, 128, with_workspace=True).path == W.PATH_TC
-    assert W.w4a16_workspace_bytes(65, 34816, 5120, 128) == 0
-    p = W.w4a16_plan_for(4, 256, 1024, 128, with_workspace=True)  # fewer units than SMs: one CTA each
-    assert p.path == W.PATH_STREAMK and p.ctas == 2 * 4
-    assert W.w4a16_plan_for(4, 256, 1984, 64, with_workspace=True).path == W.PATH_GEMV  # K % 128 != 0
-
-
-def test_gemm_ws_rejects_bad_workspace_on_host(W):
-    a = (FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 4, 1024, 1024, 128)
-    assert W.w4a16_gemm_ws(*a, None, FAKE * 5 + 8, 1 << 20, None) == 3          # misaligned workspace
-    assert W.w4a16_gemm_ws(*a, None, FAKE * 4 + 64, 1 << 20, None) == 1         # workspace overlaps y
-    assert W.w4a16_gemm_ws(*a, None, FAKE + 1024, 1 << 20, None) == 1           # workspace overlaps x
 
 
 def test_plan_for_group_sizes(W):

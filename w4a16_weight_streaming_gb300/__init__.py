@@ -29,14 +29,12 @@ ERR_DEVICE_TIMEOUT = 5
 PATH_AUTO = 0
 PATH_GEMV = 1
 PATH_TC = 2
-PATH_STREAMK = 3
 
 # every symbol include/w4a16.h declares
 EXPORTED = [
     "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
     "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
     "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout", "w4a16_gemm_host",
-    "w4a16_workspace_bytes", "w4a16_gemm_ws",
 ]
 
 
@@ -45,7 +43,7 @@ class Plan(ctypes.Structure):
 
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("m_tile", ctypes.c_int),
                 ("k_chunk", ctypes.c_int), ("stages", ctypes.c_int), ("tmem_stages", ctypes.c_int),
-                ("mma_issuers", ctypes.c_int), ("ctas", ctypes.c_int),
+                ("mma_issuers", ctypes.c_int), ("clusters", ctypes.c_int),
                 ("dequant_warps", ctypes.c_int)]
 
     def as_dict(self):
@@ -76,14 +74,10 @@ def _load() -> ctypes.CDLL:
     lib.w4a16_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
     lib.w4a16_gemm_ex.restype = I
     lib.w4a16_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
-    lib.w4a16_gemm_ws.restype = I
-    lib.w4a16_gemm_ws.argtypes = [P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P, S, P]
-    lib.w4a16_workspace_bytes.restype = S
-    lib.w4a16_workspace_bytes.argtypes = [I, I, I, I]
     lib.w4a16_gemm_host.restype = I
-    lib.w4a16_gemm_host.argtypes = [P, P, P, P, P, P, I, I, I, I, P, S, P]
+    lib.w4a16_gemm_host.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.w4a16_plan_for.restype = I
-    lib.w4a16_plan_for.argtypes = [I, I, I, I, I, ctypes.POINTER(Plan)]
+    lib.w4a16_plan_for.argtypes = [I, I, I, I, ctypes.POINTER(Plan)]
     lib.w4a16_last_dispatch.restype = I
     lib.w4a16_last_dispatch.argtypes = [ctypes.c_char_p, S]
     lib.w4a16_device_status.restype = I
@@ -136,25 +130,14 @@ def w4a16_gemm_ex(x: int, qweight_r: int, scales_r: int, y: int, M: int, N: int,
                              ctypes.byref(plan) if plan is not None else None, stream)
 
 
-def w4a16_gemm_ws(x: int, qweight_r: int, scales_r: int, y: int, M: int, N: int, K: int, group: int,
-                  plan: Plan | None, workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
-    return lib.w4a16_gemm_ws(x, qweight_r, scales_r, y, M, N, K, group,
-                             ctypes.byref(plan) if plan is not None else None, workspace, workspace_bytes, stream)
-
-
-def w4a16_workspace_bytes(M: int, N: int, K: int, group: int) -> int:
-    return lib.w4a16_workspace_bytes(M, N, K, group)
-
-
 def w4a16_gemm_host(x_host: int, x_dev: int, qweight_r: int, scales_r: int, y_dev: int, y_host: int, M: int, N: int,
-                    K: int, group: int, workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
-    return lib.w4a16_gemm_host(x_host, x_dev, qweight_r, scales_r, y_dev, y_host, M, N, K, group, workspace,
-                               workspace_bytes, stream)
+                    K: int, group: int, stream: int | None) -> int:
+    return lib.w4a16_gemm_host(x_host, x_dev, qweight_r, scales_r, y_dev, y_host, M, N, K, group, stream)
 
 
-def w4a16_plan_for(M: int, N: int, K: int, group: int, with_workspace: bool = False) -> Plan:
+def w4a16_plan_for(M: int, N: int, K: int, group: int) -> Plan:
     p = Plan()
-    rc = lib.w4a16_plan_for(M, N, K, group, 1 if with_workspace else 0, ctypes.byref(p))
+    rc = lib.w4a16_plan_for(M, N, K, group, ctypes.byref(p))
     if rc != OK:
         raise W4A16Error(rc, "w4a16_plan_for")
     return p
@@ -201,32 +184,13 @@ def repack(qweight: torch.Tensor, scales: torch.Tensor, group: int = 128, stream
     return qw_r, sc_r
 
 
-def _ws_args(workspace: torch.Tensor | None):
-    if workspace is None:
-        return None, 0
-    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
-
-
-def new_workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A zero-filled device buffer of `nbytes` bytes (at least 256) for w4a16_gemm_ws; zero-filled once
-    here, it stays valid for any number of calls in stream order."""
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
-
-
-def workspace_for(M: int, N: int, K: int, group: int = 128, device=None) -> torch.Tensor:
-    """new_workspace() of the size the automatic plan of w4a16_gemm_ws wants for (M, N, K, group)."""
-    return new_workspace(w4a16_workspace_bytes(M, N, K, group), device)
-
-
 def gemm_host(x_host: torch.Tensor, x_dev: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor,
-              y_dev: torch.Tensor, y_host: torch.Tensor, N: int, K: int, group: int = 128, stream=None,
-              workspace: torch.Tensor | None = None) -> None:
+              y_dev: torch.Tensor, y_host: torch.Tensor, N: int, K: int, group: int = 128, stream=None) -> None:
     """w4a16_gemm_host on tensors: x_host / y_host fp16 on the CPU (pinned), x_dev / y_dev on cuda.
     Queues the three operations on `stream`; y_host is valid after that stream is synchronised."""
     M = x_host.shape[0]
-    wp, wb = _ws_args(workspace)
     _check(w4a16_gemm_host(x_host.data_ptr(), x_dev.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(),
-                           y_dev.data_ptr(), y_host.data_ptr(), M, N, K, group, wp, wb, _stream_handle(stream)),
+                           y_dev.data_ptr(), y_host.data_ptr(), M, N, K, group, _stream_handle(stream)),
            "w4a16_gemm_host")
 
 
@@ -239,16 +203,13 @@ def unrepack(qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, gr
 
 
 def gemm(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, group: int = 128,
-         y: torch.Tensor | None = None, plan: Plan | dict | None = None, stream=None,
-         workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """y[M, N] (float16) = x[M, K] (float16, CUDA) . dequant(W) through w4a16_gemm_ws (w4a16_gemm_ex
-    when no workspace is given)."""
+         y: torch.Tensor | None = None, plan: Plan | dict | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] (float16) = x[M, K] (float16, CUDA) . dequant(W) through w4a16_gemm / w4a16_gemm_ex."""
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     if isinstance(plan, dict):
         plan = Plan(**plan)
-    wp, wb = _ws_args(workspace)
-    _check(w4a16_gemm_ws(x.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K, group, plan,
-                         wp, wb, _stream_handle(stream)), "w4a16_gemm")
+    _check(w4a16_gemm_ex(x.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K, group, plan,
+                         _stream_handle(stream)), "w4a16_gemm")
     return y

@@ -26,6 +26,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ------------------------------------------------------------------------------------ PDL
+// Programmatic dependent launch. griddep_wait blocks until the grids this one depends on have
+// completed and their writes are visible (a no-op when launched without the attribute);
+// griddep_launch_dependents lets the next grid on the stream start launching (the first call by any
+// thread of the CTA counts).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -87,6 +87,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(MR) * klen_max * 2);  // [kWarps][MR][32]
     float* part = red + kWarps * MR * 32;                                                  // [MR][32]
 
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;      // + kb * wt
+    const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;  // + g * wt
+
+    // Programmatic dependent launch: the lane's first batch of weights is pulled into L2 while the
+    // previous grid on the stream finishes; x (possibly its output) is read only after it completed.
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int b = sl.kb_begin + warp + kWarps * u;
+        if (b < sl.kb_end) asm volatile("prefetch.global.L2 [%0];" ::"l"(wcol + static_cast<int64_t>(b) * wt));
+    }
+    griddep_wait();
+
     // Stage x[0:MR][slice] as fp16 (16-byte copies).
     {
         const int vec_per_row = sl.klen / 8;
@@ -99,16 +113,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     }
     __syncthreads();
 
-    const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
     float acc[2][MR][2];
 #pragma unroll
     for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int m = 0; m < MR; ++m) acc[c][m][0] = acc[c][m][1] = 0.f;
 
-    const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;      // + kb * wt
-    const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;  // + g * wt
     // scale row of 32-k block b: b / (G / 32), a shift when G / 32 is a power of two
     const int gb = G / 32;
     const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
@@ -136,6 +146,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         gemv_block<MR>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
     }
 
+    griddep_launch_dependents();
 #pragma unroll
     for (int m = 0; m < MR; ++m)
         red[(warp * MR + m) * 32 + lane] = (acc[0][m][0] + acc[0][m][1]) + (acc[1][m][0] + acc[1][m][1]);
@@ -186,13 +197,20 @@ cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const ui
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (split > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = split;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = split > 1 ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, x, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, N, K, G, split);
 }
 

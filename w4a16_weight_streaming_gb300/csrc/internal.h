@@ -53,21 +53,4 @@ int tc_resident_ctas(const TcConfig& c, int G);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
 
-// ---- tc_streamk.cu: persistent stream-K tcgen05 kernel for M <= 64. Caller-provided workspace:
-// kStreamKCounterBytes of per-tile counters (one uint32 per 128-column tile of the widest supported
-// N, zero between calls), then the fp32 partial tiles [ctas][2][m_tile][128].
-constexpr size_t kStreamKCounterBytes = (size_t{1} << 23) / 128 * 4;
-struct StreamKConfig {
-    int m_tile;   // 16, 32 or 64 (>= M)
-    int k_chunk;  // K per pipeline stage: 128 or 256
-    int stages;   // shared-memory ring depth, 2..16
-    int ctas;     // persistent CTAs (one per SM), <= (128-column tiles) x (K / k_chunk)
-};
-bool streamk_instantiated(int m_tile, int k_chunk);
-bool streamk_config_valid(const StreamKConfig& c, int M, int N, int K, int G);
-size_t streamk_smem_bytes(const StreamKConfig& c, int G);
-size_t streamk_workspace_bytes(const StreamKConfig& c, int N);
-cudaError_t launch_streamk(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
-                           void* workspace, int M, int N, int K, int G, const StreamKConfig& c, const LaunchCtx& ctx);
-
 }  // namespace w4a16

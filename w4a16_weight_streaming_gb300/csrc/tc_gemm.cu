@@ -214,30 +214,42 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
             const uint32_t wbytes = static_cast<uint32_t>(kKB * wt * 16);
             const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
             const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
-            int issued = 0;
-            int s = 0;
-            uint32_t ph = 0;  // phase parity of the current use of stage s
-            for (int i = 0; i < niter; ++i) {
-                // far ahead of the consumers: a suspending wait costs no issue slots and no latency here
-                if (i >= s_stages && !mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, timeout_ns, status)) break;
+            auto issue_w = [&](int i) {  // weights and scales of stage use i (no dependence on x)
+                const int s = i % s_stages;
                 const int k0 = (c_begin + i) * KC;
                 const uint32_t fb = full_bar(s);
                 mbar_arrive_expect_tx(fb, bytes);
                 bulk_g2s(sbase + P.w_off + s * P.w_stage, w_tile + static_cast<int64_t>(k0 / 32) * wt, wbytes, fb, pol);
                 bulk_g2s(sbase + P.s_off + s * P.s_stage, s_tile + static_cast<int64_t>(k0 / G) * wt, sbytes, fb, pol);
+            };
+            auto issue_x = [&](int i) {
+                const int s = i % s_stages;
+                const int k0 = (c_begin + i) * KC;
                 const uint32_t xs = sbase + P.x_off + s * P.x_stage;
                 if (x_3d) {
-                    tma_load_x_3d(xs, &tmap_x, k0, m0, fb);
+                    tma_load_x_3d(xs, &tmap_x, k0, m0, full_bar(s));
                 } else {
 #pragma unroll
-                    for (int a = 0; a < KC / 64; ++a) tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, fb);
+                    for (int a = 0; a < KC / 64; ++a)
+                        tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, full_bar(s));
                 }
+            };
+            // Programmatic dependent launch: the first ring fill of weights goes out before the
+            // previous grid on the stream has finished; x (possibly its output) only after.
+            const int pre = niter < s_stages ? niter : s_stages;
+            for (int i = 0; i < pre; ++i) issue_w(i);
+            griddep_wait();
+            for (int i = 0; i < pre; ++i) issue_x(i);
+            int issued = pre;
+            for (int i = pre; i < niter; ++i) {
+                // far ahead of the consumers: a suspending wait costs no issue slots and no latency here
+                const uint32_t ph = static_cast<uint32_t>(i / s_stages) & 1u;  // parity of this use of the stage
+                if (!mbar_wait(empty_bar(i % s_stages), ph ^ 1u, abort_flag, timeout_ns, status)) break;
+                issue_w(i);
+                issue_x(i);
                 issued = i + 1;
-                if (++s == s_stages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
+            griddep_launch_dependents();
             // Let the copies still in flight land before shared memory can be released.
             int dummy_abort = 0;
             for (int i = issued > s_stages ? issued - s_stages : 0; i < issued; ++i)  // (only after the loop)
@@ -375,6 +387,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         __syncwarp();
 
         // ---------------- epilogue: TMEM -> registers -> y (or the split-K partial tile)
+        griddep_wait();  // y may still be read or written by the previous grid on the stream
         const bool have_d = warp_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
         tc_fence_after();
         if (have_d) {
@@ -418,6 +431,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
 
     if (split > 1) {
         __syncwarp();
+        griddep_wait();  // every thread of the reduction writes y
         cluster_sync_all();
         const int E4 = MT * kTileN / 4;
         const int beg = static_cast<int>((static_cast<int64_t>(rank) * E4) / split);
@@ -491,12 +505,19 @@ cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cud
     cfg.blockDim = dim3(threads_for(GI, NI, DW), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = c.split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (c.split > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = c.split;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = c.split > 1 ? 1 : 0;
+    cfg.numAttrs = n;
     return cfg;
 }
 
@@ -507,7 +528,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
     const size_t smem = launch_smem(MT, KC, G, c);
     cudaError_t e = prepare_kernel(kern, smem, c.split);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(c, M, N, smem, ctx.stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
                               c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
@@ -523,10 +544,16 @@ int resident_ctas_t(const TcConfig& c, int G) {
         return 0;
     }
     cudaLaunchAttribute attr[1];
-    TcConfig one = c;
-    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(one, 1, kTileN, smem, nullptr, attr);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.split, 1, 1);
-    cfg.numAttrs = 1;  // query with the cluster shape even for split 1
+    cfg.blockDim = dim3(threads_for(GI, NI, DW), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;  // the cluster shape, also for split 1
+    attr[0].val.clusterDim.x = c.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
         cudaGetLastError();

@@ -102,7 +102,6 @@ int check_matrix_shape(int N, int K, int G) {
 struct Choice {
     int path;
     TcConfig tc;
-    StreamKConfig sk;
     int gemv_split;
 };
 
@@ -201,11 +200,11 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) 
 }
 
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
-                          bool ws_allowed, Choice* out);
+                          Choice* out);
 
 // Automatic plans are resolved once per (device, M, N, K, group) and cached: the resolution queries
 // the driver's cluster occupancy for every candidate split.
-std::map<std::tuple<int, int, int, int, int, bool>, Choice> g_plan_cache;
+std::map<std::tuple<int, int, int, int, int>, Choice> g_plan_cache;
 
 // W4A16_PLAN: an override of every automatic plan, read once per process. Its value is
 // "field=value[,field=value...]" with the w4a16_plan field names, e.g. "path=2,m_tile=64,split_k=3",
@@ -240,7 +239,7 @@ const EnvPlan& env_plan() {
                          : key == "stages"        ? &r.plan.stages
                          : key == "tmem_stages"   ? &r.plan.tmem_stages
                          : key == "mma_issuers"   ? &r.plan.mma_issuers
-                         : key == "ctas"          ? &r.plan.ctas
+                         : key == "clusters"      ? &r.plan.clusters
                          : key == "dequant_warps" ? &r.plan.dequant_warps
                                                   : nullptr;
             if (!field || n < 0 || n > 4096 || (stop && *stop != '\0')) {
@@ -255,23 +254,19 @@ const EnvPlan& env_plan() {
     return e;
 }
 
-// ws_allowed: the caller passes a workspace, so plans that keep partial tiles in it (stream-K) may
-// be chosen automatically.
-int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, bool ws_allowed,
-                 Choice* out) {
+int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, Choice* out) {
     bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
                                          plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
-                                         plan->mma_issuers == 0 && plan->ctas == 0 && plan->dequant_warps == 0);
+                                         plan->mma_issuers == 0 && plan->clusters == 0 && plan->dequant_warps == 0);
     if (automatic && env_plan().present) {
         if (!env_plan().valid) return W4A16_ERR_INVALID_ARG;
         plan = &env_plan().plan;
         automatic = false;
     }
-    if (!automatic || !have_device)
-        return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, ws_allowed, out);
+    if (!automatic || !have_device) return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, M, N, K, G, ws_allowed);
+    const auto key = std::make_tuple(dev, M, N, K, G);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_plan_cache.find(key);
@@ -280,7 +275,7 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
             return W4A16_OK;
         }
     }
-    const int rc = resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, ws_allowed, out);
+    const int rc = resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
     if (rc == W4A16_OK) {
         std::lock_guard<std::mutex> lock(g_mu);
         if (g_plan_cache.size() < 4096) g_plan_cache[key] = *out;
@@ -288,32 +283,13 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
     return rc;
 }
 
-// Persistent stream-K plan: the smallest row tile holding M, 256-k stages when K and the group allow,
-// the deepest ring that fits, one CTA per SM (fewer when the matrix has fewer units).
-StreamKConfig streamk_default(int M, int N, int K, int G, int sm_count) {
-    StreamKConfig c;
-    c.m_tile = M <= 16 ? 16 : M <= 32 ? 32 : 64;
-    c.k_chunk = (K % 256 == 0 && group_fits(256, G)) ? 256 : 128;
-    c.stages = 2;
-    for (int s = 2; s <= 16; ++s) {
-        StreamKConfig t = c;
-        t.stages = s;
-        if (streamk_smem_bytes(t, G) <= 225 * 1024) c.stages = s;
-    }
-    const long long units = static_cast<long long>((N + 127) / 128) * (K / c.k_chunk);
-    c.ctas = static_cast<int>(std::min<long long>(sm_count, units));
-    return c;
-}
-
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
-                          bool ws_allowed, Choice* out) {
+                          Choice* out) {
     w4a16_plan p = {};
     if (plan) p = *plan;
-    if (p.path < 0 || p.path > 3) return W4A16_ERR_INVALID_ARG;
+    if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
-    if (path == W4A16_PATH_AUTO && ws_allowed && M <= 64 && K % 128 == 0 && group_fits(128, G)) {
-        path = W4A16_PATH_STREAMK;
-    } else if (path == W4A16_PATH_AUTO) {
+    if (path == W4A16_PATH_AUTO) {
         // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one
         // activation row; from 3 rows on the tcgen05 tiles.
         // At two rows the GEMV wins only on the smaller matrices (5120 x 5120, 5120 x 7168); on
@@ -330,26 +306,6 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         if (path == W4A16_PATH_GEMV && tc_ok && gemv_smem_bytes(M, N, K, 16) > kGemvMaxSmem) path = W4A16_PATH_TC;
     }
     out->path = path;
-    if (path == W4A16_PATH_STREAMK) {
-        if (M > 64 || K % 128 != 0) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        StreamKConfig c = streamk_default(M, N, K, G, sm_count);
-        if (p.m_tile > 0) c.m_tile = p.m_tile;
-        if (p.k_chunk > 0) c.k_chunk = p.k_chunk;
-        if (p.stages > 0) {
-            c.stages = p.stages;
-        } else {
-            for (int s2 = 2; s2 <= 16; ++s2) {
-                StreamKConfig t = c;
-                t.stages = s2;
-                if (streamk_smem_bytes(t, G) <= 225 * 1024) c.stages = s2;
-            }
-        }
-        const long long units = static_cast<long long>((N + 127) / 128) * (K / std::max(c.k_chunk, 1));
-        c.ctas = p.ctas > 0 ? p.ctas : static_cast<int>(std::min<long long>(sm_count, units));
-        if (!streamk_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        out->sk = c;
-        return W4A16_OK;
-    }
     if (path == W4A16_PATH_GEMV) {
         if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
         int split = p.split_k > 0 ? p.split_k : gemv_pick_split(M, N, K, sm_count);
@@ -430,10 +386,9 @@ using namespace w4a16;
 namespace w4a16 {
 namespace {
 
-// Every argument check of a GEMM on device buffers, then the plan; launches nothing. A non-null
-// workspace lets automatic plans keep partial tiles in it; a plan that needs it is refused without.
+// Every argument check of a GEMM on device buffers, then the plan; launches nothing.
 int prepare_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
-                 int group, const w4a16_plan* plan, const void* ws, size_t ws_bytes, DeviceInfo* d, Choice* ch) {
+                 int group, const w4a16_plan* plan, DeviceInfo* d, Choice* ch) {
     if (!x || !qweight_r || !scales_r || !y) return W4A16_ERR_INVALID_ARG;
     if (M <= 0) return W4A16_ERR_INVALID_ARG;
     const int sh = check_matrix_shape(N, K, group);
@@ -446,22 +401,12 @@ int prepare_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r,
         return W4A16_ERR_INVALID_ARG;
     if (is_host_pointer(x) || is_host_pointer(qweight_r) || is_host_pointer(scales_r) || is_host_pointer(y))
         return W4A16_ERR_INVALID_ARG;
-    if (ws != nullptr) {
-        if (!aligned16(ws)) return W4A16_ERR_MISALIGNED;
-        if (overlaps(ws, ws_bytes, x, xb) || overlaps(ws, ws_bytes, y, yb) || overlaps(ws, ws_bytes, qweight_r, qb) ||
-            overlaps(ws, ws_bytes, scales_r, sb) || is_host_pointer(ws))
-            return W4A16_ERR_INVALID_ARG;
-    }
     if (!device_info(d)) return W4A16_ERR_CUDA;
-    const int rc = resolve_plan(M, N, K, group, plan, d->sm_count, true, ws != nullptr, ch);
-    if (rc != W4A16_OK) return rc;
-    if (ch->path == W4A16_PATH_STREAMK && (ws == nullptr || ws_bytes < streamk_workspace_bytes(ch->sk, N)))
-        return W4A16_ERR_INVALID_ARG;
-    return W4A16_OK;
+    return resolve_plan(M, N, K, group, plan, d->sm_count, true, ch);
 }
 
 int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M,
-                int N, int K, int group, void* ws, const DeviceInfo& d, void* stream) {
+                int N, int K, int group, const DeviceInfo& d, void* stream) {
     LaunchCtx ctx;
     ctx.stream = static_cast<cudaStream_t>(stream);
     ctx.status = d.status;
@@ -474,14 +419,6 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
                         group, ch.gemv_split, ctx);
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128", M, N, K,
                  group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32));
-    } else if (ch.path == W4A16_PATH_STREAMK) {
-        e = launch_streamk(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, ws, M,
-                           N, K, group, ch.sk, ctx);
-        snprintf(desc, sizeof(desc),
-                 "path=streamk M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d ctas=%d grid=(%d,1,1) block=672 "
-                 "smem=%zu workspace=%zu",
-                 M, N, K, group, ch.sk.m_tile, ch.sk.k_chunk, ch.sk.stages, ch.sk.ctas, ch.sk.ctas,
-                 streamk_smem_bytes(ch.sk, group), streamk_workspace_bytes(ch.sk, N));
     } else {
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
@@ -566,7 +503,7 @@ int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
-int w4a16_plan_for(int M, int N, int K, int group, int with_workspace, w4a16_plan* out) {
+int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     if (!out) return W4A16_ERR_INVALID_ARG;
     if (M <= 0) return W4A16_ERR_INVALID_ARG;
     const int sh = check_matrix_shape(N, K, group);
@@ -576,18 +513,14 @@ int w4a16_plan_for(int M, int N, int K, int group, int with_workspace, w4a16_pla
     const bool dev = device_info(&d);
     const int sms = dev ? d.sm_count : 152;
     Choice ch;
-    const int rc = resolve_plan(M, N, K, group, nullptr, sms, dev, with_workspace != 0, &ch);
+    const int rc = resolve_plan(M, N, K, group, nullptr, sms, dev, &ch);
     if (rc != W4A16_OK) return rc;
-    *out = w4a16_plan{};
     out->path = ch.path;
+    out->clusters = 0;
+    out->dequant_warps = 0;
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
-    } else if (ch.path == W4A16_PATH_STREAMK) {
-        out->m_tile = ch.sk.m_tile;
-        out->k_chunk = ch.sk.k_chunk;
-        out->stages = ch.sk.stages;
-        out->ctas = ch.sk.ctas;
-        out->split_k = 1;
+        out->m_tile = out->k_chunk = out->stages = out->tmem_stages = out->mma_issuers = 0;
     } else {
         out->split_k = ch.tc.split;
         out->m_tile = ch.tc.m_tile;
@@ -600,37 +533,21 @@ int w4a16_plan_for(int M, int N, int K, int group, int with_workspace, w4a16_pla
     return W4A16_OK;
 }
 
-size_t w4a16_workspace_bytes(int M, int N, int K, int group) {
-    if (M <= 0 || M > (1 << 20) || check_matrix_shape(N, K, group) != W4A16_OK) return 0;
-    DeviceInfo d;
-    const bool dev = device_info(&d);
-    Choice ch;
-    if (resolve_plan(M, N, K, group, nullptr, dev ? d.sm_count : 152, dev, true, &ch) != W4A16_OK) return 0;
-    return ch.path == W4A16_PATH_STREAMK ? streamk_workspace_bytes(ch.sk, N) : 0;
-}
-
-int w4a16_gemm_ws(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
-                  int group, const w4a16_plan* plan, void* workspace, size_t workspace_bytes, void* stream) {
-    DeviceInfo d;
-    Choice ch;
-    const int rc = prepare_gemm(x, qweight_r, scales_r, y, M, N, K, group, plan, workspace, workspace_bytes, &d, &ch);
-    if (rc != W4A16_OK) return rc;
-    return launch_gemm(ch, x, qweight_r, scales_r, y, M, N, K, group, workspace, d, stream);
-}
-
 int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                   int group, const w4a16_plan* plan, void* stream) {
-    return w4a16_gemm_ws(x, qweight_r, scales_r, y, M, N, K, group, plan, nullptr, 0, stream);
+    DeviceInfo d;
+    Choice ch;
+    const int rc = prepare_gemm(x, qweight_r, scales_r, y, M, N, K, group, plan, &d, &ch);
+    if (rc != W4A16_OK) return rc;
+    return launch_gemm(ch, x, qweight_r, scales_r, y, M, N, K, group, d, stream);
 }
 
 int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight_r, const void* scales_r,
-                    uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+                    uint16_t* y_dev, uint16_t* y_host, int M, int N, int K, int group, void* stream) {
     if (!x_host || !y_host) return W4A16_ERR_INVALID_ARG;
     DeviceInfo d;
     Choice ch;
-    const int rc = prepare_gemm(x_dev, qweight_r, scales_r, y_dev, M, N, K, group, nullptr, workspace, workspace_bytes,
-                                &d, &ch);
+    const int rc = prepare_gemm(x_dev, qweight_r, scales_r, y_dev, M, N, K, group, nullptr, &d, &ch);
     if (rc != W4A16_OK) return rc;
     const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
     if (overlaps(x_host, xb, y_host, yb) || is_device_pointer(x_host) || is_device_pointer(y_host))
@@ -640,7 +557,7 @@ int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight
         cudaGetLastError();
         return W4A16_ERR_CUDA;
     }
-    const int lr = launch_gemm(ch, x_dev, qweight_r, scales_r, y_dev, M, N, K, group, workspace, d, stream);
+    const int lr = launch_gemm(ch, x_dev, qweight_r, scales_r, y_dev, M, N, K, group, d, stream);
     if (lr != W4A16_OK) return lr;
     if (cudaMemcpyAsync(y_host, y_dev, yb, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
         cudaGetLastError();
@@ -651,7 +568,7 @@ int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight
 
 int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                int group, void* stream) {
-    return w4a16_gemm_ws(x, qweight_r, scales_r, y, M, N, K, group, nullptr, nullptr, 0, stream);
+    return w4a16_gemm_ex(x, qweight_r, scales_r, y, M, N, K, group, nullptr, stream);
 }
 
 int w4a16_last_dispatch(char* buf, size_t len) {
