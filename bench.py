@@ -355,6 +355,68 @@ def run_reference(args, rank: int):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------ the decode-step chain
+CHAIN_LAYERS = 64
+CHAIN_B = [1, 8, 16, 32, 64]
+
+
+def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAYERS, reps=5):
+    """The dense layers of one decode step as one CUDA graph: per layer qkv and o from the layer input,
+    gate+up from o, silu(gate) * up, down -> the next layer's input (attention itself is not part of
+    this path). Every layer streams its own device copy of the four matrices (layers x 170 MB in
+    total, far beyond L2). Each B is timed over `reps` graph replays and set against the pages' step
+    model t_step(B) = max(W / BW, B * F / P) with W the weight bytes and F = 2 x weights per position
+    (no recurrent state or KV traffic in this path)."""
+    import torch
+
+    names = [n for (n, _, _) in inputs.SWEEP_MATRICES]
+    dims = {n: (K, N) for (n, K, N) in inputs.SWEEP_MATRICES}
+    copies = {n: [tuple(t.clone() for t in sources[n]) for _ in range(layers)] for n in names}
+    hidden = dims["o"][0]
+    inter = dims["down"][0]
+    wbytes = layers * sum(weight_bytes(K, N) for (K, N) in dims.values())
+    weights_per_pos = layers * sum(K * N for (K, N) in dims.values())
+    out = []
+    for B in CHAIN_B:
+        h = [torch.zeros((B, hidden), dtype=torch.float16, device=dev) for _ in range(2)]
+        h[0].normal_()
+        qkv = torch.empty((B, dims["qkv"][1]), dtype=torch.float16, device=dev)
+        o = torch.empty((B, hidden), dtype=torch.float16, device=dev)
+        gu = torch.empty((B, 2 * inter), dtype=torch.float16, device=dev)
+        act = torch.empty((B, inter), dtype=torch.float16, device=dev)
+
+        def step():
+            for li in range(layers):
+                x, y = h[li % 2], h[(li + 1) % 2]
+                W.gemm(x, *copies["qkv"][li], dims["qkv"][1], hidden, GROUP, y=qkv)
+                W.gemm(x, *copies["o"][li], hidden, hidden, GROUP, y=o)
+                W.gemm(o, *copies["gate_up"][li], 2 * inter, hidden, GROUP, y=gu)
+                W.silu_mul(gu, act)
+                W.gemm(act, *copies["down"][li], hidden, inter, GROUP, y=y)
+
+        step()  # plans resolved outside the capture
+        torch.cuda.synchronize()
+        g = capture(step)
+        g.replay()
+        torch.cuda.synchronize()
+        ms = timed(g.replay, reps) / reps
+        del g
+        t_mem = wbytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = B * 2.0 * weights_per_pos / (peaks["bf16_tflops"] * 1e12)
+        out.append({"B": B, "us_per_step": ms * 1e3, "tokens_per_s": B / (ms * 1e-3),
+                    "weight_gbs": wbytes / (ms * 1e-3) / 1e9, "model_us": max(t_mem, t_tc) * 1e6,
+                    "model_frac": max(t_mem, t_tc) / (ms * 1e-3), "bound": "hbm" if t_mem >= t_tc else "tensor"})
+    st = W.w4a16_device_status()
+    if st != W.OK:
+        raise RuntimeError(f"device status after the layer chain: {W.status_string(st)}")
+    del copies
+    torch.cuda.empty_cache()
+    return {"layers": layers, "kernels_per_step": 5 * layers, "weight_bytes_per_step": wbytes,
+            "what": "per layer: qkv(h), o(h), gate_up(o), silu(gate)*up, down -> next h; one CUDA graph per step, "
+                    "programmatic dependent launch between the kernels; model t_step(B) = max(W/BW, B*2*weights/P) "
+                    "with the measured peaks", "rows": out}
+
+
 # ------------------------------------------------------------------------------ GPU arm
 def percentile(v, q):
     return float(np.percentile(np.asarray(v, dtype=np.float64), q))
@@ -372,6 +434,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--table", action="store_true", help="also print the per-row table to stderr")
+    ap.add_argument("--no-chain", action="store_true", help="skip the 64-layer decode-step chain")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -600,6 +663,11 @@ def main():
                          f"of the step, {reps} repetitions, {el:.1f} s",
                "single_thread": oracle_single_thread_configs()}
 
+    # ---- the decode-step chain (64 dense layers, one CUDA graph per step), sweep workload only
+    chain = None
+    if args.workload == "sweep" and not args.no_chain:
+        chain = measure_layer_chain(W, dev, {n: m["copies"][0] for n, m in mats.items()}, peaks, timed, capture)
+
     if args.table and rank == 0:
         print(f"{'matrix':8s} {'M':>5s} {'us':>9s} {'med':>8s} {'p10':>8s} {'p90':>8s} {'wGB/s':>7s} "
               f"{'TFLOP/s':>8s} {'roof%':>6s} bound  plan", file=sys.stderr)
@@ -608,6 +676,11 @@ def main():
             print(f"{x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} {f(x['us_median'])} {f(x['us_p10'])} "
                   f"{f(x['us_p90'])} {x['weight_gbs']:7.0f} {x['tflops']:8.1f} {100 * x['roofline_frac']:6.1f} "
                   f"{x['bound']:6s} {x['plan']}", file=sys.stderr)
+        if chain:
+            for c in chain["rows"]:
+                print(f"chain B={c['B']:3d}: {c['us_per_step']:9.1f} us/step {c['tokens_per_s']:9.0f} tok/s "
+                      f"{c['weight_gbs']:6.0f} GB/s model {c['model_us']:8.1f} us ({100 * c['model_frac']:.1f}%, "
+                      f"{c['bound']})", file=sys.stderr)
 
     if rank == 0:
         layer = {}
@@ -629,7 +702,7 @@ def main():
                 "value_is": "weight bytes streamed per step / step time (all GEMMs of the step)",
                 "tflops": world * flops_step / (ms_step * 1e-3) / 1e12,
                 "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
-                "layer_step": layer, "rows": rows, "cold_launch_us": cold,
+                "layer_step": layer, "rows": rows, "cold_launch_us": cold, "decode_step_chain": chain,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps * len(items), "clocks": clocks,
                 "peaks": {k: v for k, v in peaks.items()}}

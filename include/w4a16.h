@@ -149,6 +149,22 @@ int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight
  * W4A16_PLAN makes them return INVALID_ARG; a plan invalid for a shape, UNSUPPORTED_SHAPE. */
 int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
 
+/*
+ * The activation between the fused gate+up projection and the down projection of a dense layer
+ * (the 17,408-wide MLPs of "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s", ai.satyajit.si, section
+ * "Where the line bends"; read as SwiGLU, the plainest reading for that model family):
+ *   act[m][i] = fp16_rne(silu(g) * u),  g = gu[m][i], u = gu[m][I + i],  silu(g) = g / (1 + e^-g),
+ * evaluated in fp32 from the fp16 inputs (error about one fp16 rounding of the result).
+ *   gu:  fp16 [M][2I] row-major, device: the output of w4a16_gemm with the fused 2I-column
+ *        gate+up matrix, gate columns first.
+ *   act: fp16 [M][I] row-major, device, written in full; must not overlap gu.
+ * Supported: I % 8 == 0, 1 <= M <= 2^20, I <= 2^22; both pointers 16-byte aligned. Asynchronous on
+ * `stream`, launched with programmatic dependent launch: it is scheduled while the GEMM before it
+ * finishes and reads gu only after that GEMM completed. Allocates nothing.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+int w4a16_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, void* stream);
+
 /* Describes the last GEMM this process launched (path, tile, split, grid) into buf (NUL
  * terminated, truncated to len). Host only. Returns W4A16_OK or INVALID_ARG. */
 int w4a16_last_dispatch(char* buf, size_t len);

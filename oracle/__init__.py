@@ -15,6 +15,9 @@ Functions and the passage each follows:
 * ``dequant`` / ``unpack`` -- the canonical workload format (8 nibbles per int32 along K, low
   nibble first; fp16 scales per group of G rows; w = fp16_rne((q - 8) * s)). The pages do not
   print the format; this is the plainest reading of the workload definition.
+* ``silu_mul`` -- the activation of the dense layer's MLP between the fused gate+up projection
+  and the down projection, act = silu(gate) * up ("Qwen3.8-27B at 764, 1,035 and 1,623 tok/s",
+  section "Where the line bends": the 17,408-wide MLPs; SwiGLU is the reading taken).
 * ``repack`` / ``unrepack`` -- the library's own device layout, restated from its definition.
 * ``half_to_double`` / ``double_to_half`` -- the binary16 codec, written out bit by bit.
 
@@ -92,6 +95,7 @@ class Oracle:
         for name in ("w4o_repack", "w4o_unrepack"):
             getattr(lib, name).restype = I
             getattr(lib, name).argtypes = [P, P, I, I, I, P, P]
+        lib.w4o_silu_mul.argtypes = [P, I, I, P, P]
         lib.w4o_max_threads.restype = I
         lib.w4o_has_openmp.restype = I
         self.lib = lib
@@ -181,6 +185,20 @@ class Oracle:
             raise ValueError(f"oracle gemm_sampled rejected the input (rc={rc})")
         return y, a
 
+    # ---------------------------------------------------------------------------- activation
+    def silu_mul(self, gu_bits):
+        """(act float64 [M, I], act_half uint16 [M, I]) for fp16 bits gu [M, 2I] (gate, then up):
+        act = silu(gate) * up in double and its fp16 rounding."""
+        gu = _c(gu_bits, np.uint16)
+        M, I2 = gu.shape
+        if I2 % 2:
+            raise ValueError("gu must have an even number of columns")
+        I = I2 // 2
+        act = np.empty((M, I), np.float64)
+        half = np.empty((M, I), np.uint16)
+        self.lib.w4o_silu_mul(_ptr(gu), M, I, _ptr(act), _ptr(half))
+        return act, half
+
     # ---------------------------------------------------------------------------- layout
     def repack(self, qweight, scales, group: int):
         """(wr uint32 [N*K/8], sr uint16 [N*K/G]): the device layout (flat; see w4a16_oracle.c)."""
@@ -259,6 +277,10 @@ def gemm_xf64(x, qweight, scales, group: int, nthreads: int | None = None):
 
 def gemm_sampled(x_bits, qweight, scales, group: int, ms, ns, nthreads: int | None = None):
     return load().gemm_sampled(x_bits, qweight, scales, group, ms, ns, nthreads)
+
+
+def silu_mul(gu_bits):
+    return load().silu_mul(gu_bits)
 
 
 def repack(qweight, scales, group: int):

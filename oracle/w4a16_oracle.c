@@ -294,6 +294,25 @@ int w4o_unrepack(const uint32_t* wr, const uint16_t* sr, int K, int N, int G, in
     return 0;
 }
 
+/* ---------------------------------------------------------------- the dense layer's activation
+ *
+ * act[m][i] = silu(g) * u with g = gu[m][i], u = gu[m][I + i] and silu(g) = g / (1 + e^-g), in
+ * double, plus its fp16 rounding: the activation between the fused gate+up projection and the down
+ * projection of the 17,408-wide MLPs of "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s"
+ * (ai.satyajit.si), section "Where the line bends". The pages do not print the activation;
+ * SwiGLU (gate columns first in the fused matrix) is the plainest reading for that model family. */
+void w4o_silu_mul(const uint16_t* gu, int M, int I, double* act_exact, uint16_t* act_half) {
+    for (int m = 0; m < M; ++m) {
+        for (int i = 0; i < I; ++i) {
+            const double g = w4o_half_to_double(gu[(size_t)m * 2 * I + i]);
+            const double u = w4o_half_to_double(gu[(size_t)m * 2 * I + I + i]);
+            const double v = g / (1.0 + exp(-g)) * u;
+            act_exact[(size_t)m * I + i] = v;
+            act_half[(size_t)m * I + i] = w4o_double_to_half(v);
+        }
+    }
+}
+
 int w4o_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

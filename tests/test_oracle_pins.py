@@ -5,6 +5,7 @@ Sources of truth used here (none of them is the oracle's own code):
   * torch's CPU float16 multiply, which rounds the exact fp32 product once (library routine);
   * exact rational arithmetic (``fractions.Fraction``) on tiny inputs;
   * closed forms: one-hot rows, all-ones rows, zero scales, constant weights, linearity;
+  * for the activation: the identity silu(g) - silu(-g) = g, its limits, and scipy's logistic;
   * handcrafted packed words whose nibble order is known by construction.
 
 The W4A16 definition (4-bit weights, 16-bit activations) follows "RTX 3090 Tested: Qwen's 381
@@ -296,10 +297,51 @@ def pin_repack_roundtrip(o):
     assert np.array_equal(qw2, words) and np.array_equal(sc2, sc)
 
 
+def _gu_bits(g, u):
+    """fp16 bits of [gate | up] for float arrays g, u of the same shape [M, I]."""
+    return np.concatenate([np.asarray(g, np.float16), np.asarray(u, np.float16)], axis=1).view(np.uint16)
+
+
+def pin_silu_identity(o):
+    # silu(g) - silu(-g) = g for every g (from silu(g) = g * sigma(g) and sigma(-g) = 1 - sigma(g)),
+    # and silu(0) = 0: catches a sign error in the exponent and a gate/up swap
+    g = np.linspace(-12.0, 12.0, 401).astype(np.float16).astype(np.float64)
+    u = np.ones_like(g)
+    a_pos, _ = o.silu_mul(_gu_bits(g[None, :], u[None, :]))
+    a_neg, _ = o.silu_mul(_gu_bits(-g[None, :], u[None, :]))
+    assert np.allclose(a_pos[0] - a_neg[0], g, rtol=1e-14, atol=1e-300)
+    assert a_pos[0][g == 0.0].tolist() == [0.0]
+
+
+def pin_silu_against_library(o):
+    # the logistic from scipy (its own implementation), times g and u, on asymmetric data
+    from scipy.special import expit
+
+    rng = np.random.default_rng(RNG_SEED + 10)
+    g = rng.normal(0.0, 3.0, size=(5, 64)).astype(np.float16).astype(np.float64)
+    u = rng.normal(0.0, 2.0, size=(5, 64)).astype(np.float16).astype(np.float64)
+    act, half = o.silu_mul(_gu_bits(g, u))
+    ref = g * expit(g) * u
+    assert np.allclose(act, ref, rtol=1e-13, atol=1e-300)
+    # the fp16 result is numpy's round-to-nearest-even of the double value
+    assert np.array_equal(half, act.astype(np.float16).view(np.uint16))
+
+
+def pin_silu_limits(o):
+    # silu(e) / e -> 1/2 as e -> 0; silu(g) -> g for large g; u scales the result exactly
+    e = 2.0 ** -20
+    act, _ = o.silu_mul(_gu_bits([[e, 20.0]], [[1.0, 1.0]]))
+    assert abs(act[0, 0] / e - 0.5) < 1e-6
+    assert abs(act[0, 1] - 20.0) < 20.0 * 3e-9
+    act2, _ = o.silu_mul(_gu_bits([[1.5, -0.75]], [[2.0, 2.0]]))
+    act1, _ = o.silu_mul(_gu_bits([[1.5, -0.75]], [[1.0, 1.0]]))
+    assert np.array_equal(act2, 2.0 * act1)
+
+
 PINS = [pin_half_decode_all, pin_half_encode, pin_dequant_exhaustive, pin_nibble_order, pin_pack_roundtrip,
         pin_bruteforce_fraction, pin_exact_dyadic, pin_one_hot, pin_all_ones, pin_zero_scales,
         pin_constant_weights, pin_linearity, pin_sampled_matches_full, pin_threads_deterministic,
-        pin_repack_positions, pin_repack_roundtrip]
+        pin_repack_positions, pin_repack_roundtrip, pin_silu_identity, pin_silu_against_library, pin_silu_limits]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -325,6 +367,11 @@ MUTANTS = {
     "abs_not_abs": ("aacc += fabs(p);", "aacc += p;"),
     "layout_positions": ("kPosOfJ[8] = {0, 4, 1, 5, 2, 6, 3, 7};", "kPosOfJ[8] = {0, 1, 2, 3, 4, 5, 6, 7};"),
     "layout_transposed_tile": ("((size_t)b * wt + c) * 4 + w;", "((size_t)c * (K / 32) + b) * 4 + w;"),
+    "silu_exponent_sign": ("g / (1.0 + exp(-g)) * u;", "g / (1.0 + exp(g)) * u;"),
+    "silu_gate_up_swapped": ("gu[(size_t)m * 2 * I + i]);\n            const double u = w4o_half_to_double(gu[(size_t)m * 2 * I + I + i]);",
+                             "gu[(size_t)m * 2 * I + I + i]);\n            const double u = w4o_half_to_double(gu[(size_t)m * 2 * I + i]);"),
+    "silu_without_up": ("g / (1.0 + exp(-g)) * u;", "g / (1.0 + exp(-g));"),
+    "silu_sigmoid_only": ("g / (1.0 + exp(-g)) * u;", "1.0 / (1.0 + exp(-g)) * u;"),
 }
 
 

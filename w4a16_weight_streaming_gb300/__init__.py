@@ -35,6 +35,7 @@ EXPORTED = [
     "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
     "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
     "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout", "w4a16_gemm_host",
+    "w4a16_silu_mul",
 ]
 
 
@@ -76,6 +77,8 @@ def _load() -> ctypes.CDLL:
     lib.w4a16_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
     lib.w4a16_gemm_host.restype = I
     lib.w4a16_gemm_host.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
+    lib.w4a16_silu_mul.restype = I
+    lib.w4a16_silu_mul.argtypes = [P, P, I, I, P]
     lib.w4a16_plan_for.restype = I
     lib.w4a16_plan_for.argtypes = [I, I, I, I, ctypes.POINTER(Plan)]
     lib.w4a16_last_dispatch.restype = I
@@ -133,6 +136,10 @@ def w4a16_gemm_ex(x: int, qweight_r: int, scales_r: int, y: int, M: int, N: int,
 def w4a16_gemm_host(x_host: int, x_dev: int, qweight_r: int, scales_r: int, y_dev: int, y_host: int, M: int, N: int,
                     K: int, group: int, stream: int | None) -> int:
     return lib.w4a16_gemm_host(x_host, x_dev, qweight_r, scales_r, y_dev, y_host, M, N, K, group, stream)
+
+
+def w4a16_silu_mul(gu: int, act: int, M: int, I: int, stream: int | None) -> int:
+    return lib.w4a16_silu_mul(gu, act, M, I, stream)
 
 
 def w4a16_plan_for(M: int, N: int, K: int, group: int) -> Plan:
@@ -200,6 +207,15 @@ def unrepack(qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, gr
     _check(w4a16_unrepack(qweight_r.data_ptr(), scales_r.data_ptr(), qw.data_ptr(), sc.data_ptr(), N, K, group,
                           _stream_handle(stream)), "w4a16_unrepack")
     return qw, sc
+
+
+def silu_mul(gu: torch.Tensor, act: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """act[M, I] = silu(gu[:, :I]) * gu[:, I:] (float16, CUDA) through w4a16_silu_mul."""
+    M, I = gu.shape[0], gu.shape[1] // 2
+    if act is None:
+        act = torch.empty((M, I), dtype=torch.float16, device=gu.device)
+    _check(w4a16_silu_mul(gu.data_ptr(), act.data_ptr(), M, I, _stream_handle(stream)), "w4a16_silu_mul")
+    return act
 
 
 def gemm(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, group: int = 128,

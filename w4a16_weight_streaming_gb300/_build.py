@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libw4a16.so")
 
-SOURCES = ["w4a16_api.cu", "repack.cu", "gemv.cu", "tc_gemm.cu"]
+SOURCES = ["w4a16_api.cu", "repack.cu", "gemv.cu", "tc_gemm.cu", "act.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "internal.h"), os.path.join(INCLUDE, "w4a16.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

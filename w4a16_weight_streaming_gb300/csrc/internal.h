@@ -53,4 +53,7 @@ int tc_resident_ctas(const TcConfig& c, int G);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
 
+// ---- act.cu: SwiGLU activation of a fused gate+up output, act = silu(gate) * up.
+cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int sm_count, cudaStream_t s);
+
 }  // namespace w4a16

@@ -571,6 +571,21 @@ int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, u
     return w4a16_gemm_ex(x, qweight_r, scales_r, y, M, N, K, group, nullptr, stream);
 }
 
+int w4a16_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, void* stream) {
+    if (!gu || !act || M <= 0 || I <= 0) return W4A16_ERR_INVALID_ARG;
+    if (I % 8 != 0 || M > (1 << 20) || I > (1 << 22)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(gu) || !aligned16(act)) return W4A16_ERR_MISALIGNED;
+    const size_t gb = static_cast<size_t>(M) * I * 4, ab = static_cast<size_t>(M) * I * 2;
+    if (overlaps(gu, gb, act, ab) || is_host_pointer(gu) || is_host_pointer(act)) return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    if (launch_silu_mul(gu, act, M, I, d.sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+}
+
 int w4a16_last_dispatch(char* buf, size_t len) {
     if (!buf || len == 0) return W4A16_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mu);
