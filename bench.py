@@ -224,19 +224,34 @@ def describe(workload: str):
     return cfg, workload_rows(mats)
 
 
-def host_inputs(workload: str, cols: int | None = None):
+def parse_only(spec: str | None):
+    """--only "name:M,name:M": the sweep rows to keep (None = all)."""
+    if not spec:
+        return None
+    keep = set()
+    for item in spec.split(","):
+        name, m = item.split(":")
+        keep.add((name.strip(), int(m)))
+    return keep
+
+
+def host_inputs(workload: str, cols: int | None = None, only=None):
     """Host-side inputs of every row: list of dict(name, M, K, N, x, qweight, scales) with the
     weights restricted to the first `cols` columns when given (bounded oracle samples)."""
     out = []
     if workload == "sweep":
         weights = {}
         for (name, K, N) in inputs.SWEEP_MATRICES:
+            if only is not None and not any(n == name for (n, _) in only):
+                continue
             qw, sc = inputs.generate_weights(K, N, GROUP, seed=inputs.SWEEP_SEED)
             if cols is not None:
                 qw, sc = np.ascontiguousarray(qw[:, :cols]), np.ascontiguousarray(sc[:, :cols])
             weights[name] = (qw, sc)
         xs = {}
         for (name, M, K, N) in sweep_rows():
+            if only is not None and (name, M) not in only:
+                continue
             if (M, K) not in xs:
                 xs[(M, K)] = inputs.generate_x(M, K, seed=1000 + M)
             qw, sc = weights[name]
@@ -435,6 +450,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--table", action="store_true", help="also print the per-row table to stderr")
     ap.add_argument("--no-chain", action="store_true", help="skip the 64-layer decode-step chain")
+    ap.add_argument("--only", default=None, help='sweep rows to run, e.g. "o:16,gate_up:256" (profiling)')
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -459,7 +475,10 @@ def main():
     # ---- inputs: canonical weights on the host -> repacked device copies per matrix. Every launch
     # of the step reads its own copy, and a matrix has enough copies that its copies cycle through
     # more than 4 x L2 bytes: no launch finds its weights in L2.
-    items = host_inputs(args.workload)
+    only = parse_only(args.only) if args.workload == "sweep" else None
+    if only is not None:
+        cfg = dict(cfg, only=sorted(f"{n}:{m}" for (n, m) in only))
+    items = host_inputs(args.workload, only=only)
     mats = {}
     for it in items:
         if it["name"] in mats:
@@ -595,7 +614,7 @@ def main():
     flush = torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
     cold = {}
     for it in items:
-        if it["M"] != 1 and args.workload == "sweep":
+        if it["M"] != 1 and args.workload == "sweep" and only is None:
             continue
         flush.fill_(1)
         torch.cuda.synchronize()
@@ -665,7 +684,7 @@ def main():
 
     # ---- the decode-step chain (64 dense layers, one CUDA graph per step), sweep workload only
     chain = None
-    if args.workload == "sweep" and not args.no_chain:
+    if args.workload == "sweep" and not args.no_chain and only is None:
         chain = measure_layer_chain(W, dev, {n: m["copies"][0] for n, m in mats.items()}, peaks, timed, capture)
 
     if args.table and rank == 0:
@@ -684,7 +703,7 @@ def main():
 
     if rank == 0:
         layer = {}
-        if args.workload == "sweep":
+        if args.workload == "sweep" and only is None:
             total_wb = sum(weight_bytes(K, N) for (_, K, N) in inputs.SWEEP_MATRICES)
             for M in inputs.SWEEP_M:
                 us = sum(x["us"] for x in rows if x["M"] == M)
