@@ -49,7 +49,8 @@ typedef enum {
     W4A16_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
     W4A16_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
     W4A16_ERR_CUDA = 4,              /* the CUDA runtime refused a launch or query */
-    W4A16_ERR_DEVICE_TIMEOUT = 5     /* a kernel gave up a bounded wait (reported by w4a16_device_status) */
+    W4A16_ERR_DEVICE_TIMEOUT = 5,    /* a kernel gave up a bounded wait (reported by w4a16_device_status) */
+    W4A16_ERR_BOUNDS = 6             /* a kernel index check failed: the debug-bounds build only (see below) */
 } w4a16_status;
 
 /* Which kernel family runs a GEMM. */
@@ -74,6 +75,16 @@ typedef struct {
 
 /* Library version: major*10000 + minor*100 + patch. */
 int w4a16_version(void);
+
+/*
+ * 1 in the debug-bounds build of the library (libw4a16_debug.so, compiled with W4A16_DEBUG_BOUNDS),
+ * 0 in the normal one. In the debug-bounds build every kernel checks each global-memory index (and
+ * each bulk-copy source range) against the size of its buffer before the access; a bad index is
+ * not accessed and records W4A16_ERR_BOUNDS in the device status word, which w4a16_device_status
+ * reports (the first error of a launch is kept). Nothing traps: the context stays usable. It
+ * stands in for a memory checker on hardware where none can be run. Same entry points, slower.
+ */
+int w4a16_debug_bounds(void);
 
 /* Human-readable name of a w4a16_status value (static string; never NULL). */
 const char* w4a16_status_string(int code);
@@ -176,8 +187,8 @@ int w4a16_last_dispatch(char* buf, size_t len);
  * kernel on any stream of the device is reported by the next read. The read and the clear are one
  * atomic exchange on the device (queued on `stream`), so a timeout recorded concurrently by a
  * kernel on another stream is never lost: it is either returned now or by the next call. The call
- * then synchronises `stream`. Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT, or W4A16_ERR_CUDA if the
- * launch, copy or synchronisation failed.
+ * then synchronises `stream`. Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT, W4A16_ERR_BOUNDS (debug-bounds
+ * build), or W4A16_ERR_CUDA if the launch, copy or synchronisation failed.
  */
 int w4a16_device_status(void* stream);
 

@@ -43,9 +43,17 @@ def test_library_exports_every_declared_symbol(W):
     assert sorted(W.EXPORTED) == declared_functions()
 
 
+def test_debug_bounds_build_exports_the_same_symbols(W):
+    dbg = W.load_debug_bounds()
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"{name} missing from the debug-bounds build"
+    assert dbg.w4a16_debug_bounds() == 1 and W.lib.w4a16_debug_bounds() == 0
+    assert dbg.w4a16_status_string(6).decode().startswith("W4A16_ERR_BOUNDS")
+
+
 def test_version_and_status_strings(W):
     assert W.w4a16_version() >= 100
-    for code in range(6):
+    for code in range(7):
         assert W.status_string(code).startswith("W4A16_")
     assert W.status_string(99) == "W4A16_ERR_UNKNOWN"
 

@@ -18,6 +18,7 @@ import torch
 from . import _build
 
 LIB_PATH = _build.LIB_PATH
+DEBUG_LIB_PATH = _build.DEBUG_LIB_PATH
 
 OK = 0
 ERR_INVALID_ARG = 1
@@ -25,6 +26,7 @@ ERR_UNSUPPORTED_SHAPE = 2
 ERR_MISALIGNED = 3
 ERR_CUDA = 4
 ERR_DEVICE_TIMEOUT = 5
+ERR_BOUNDS = 6
 
 PATH_AUTO = 0
 PATH_GEMV = 1
@@ -35,7 +37,7 @@ EXPORTED = [
     "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
     "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
     "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout", "w4a16_gemm_host",
-    "w4a16_silu_mul",
+    "w4a16_silu_mul", "w4a16_debug_bounds",
 ]
 
 
@@ -57,12 +59,13 @@ class W4A16Error(RuntimeError):
         super().__init__(f"{where}: {status_string(code)}")
 
 
-def _load() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libw4a16.so is not built ({LIB_PATH}); run __graft_entry__.build() first")
-    lib = ctypes.CDLL(LIB_PATH)
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{os.path.basename(path)} is not built ({path}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
     P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.w4a16_version.restype = I
+    lib.w4a16_debug_bounds.restype = I
     lib.w4a16_status_string.restype = ctypes.c_char_p
     lib.w4a16_status_string.argtypes = [I]
     for n in ("w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes"):
@@ -93,6 +96,13 @@ def _load() -> ctypes.CDLL:
 
 
 lib = _load()
+
+
+def load_debug_bounds() -> ctypes.CDLL:
+    """The debug-bounds build (libw4a16_debug.so) as a second, independent handle with the same C
+    entry points: every kernel checks its indices and reports W4A16_ERR_BOUNDS instead of accessing
+    out of range."""
+    return _load(DEBUG_LIB_PATH)
 
 
 # ------------------------------------------------------------------------------ raw C ABI

@@ -11,7 +11,7 @@ namespace {
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ gu, uint4* __restrict__ act, int M,
-                                                       int I) {
+                                                       int I, unsigned* status) {
     griddep_wait();  // gu is the previous kernel's output
     const int v_per_row = I / 8;
     const int64_t total = static_cast<int64_t>(M) * v_per_row;
@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
          v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t m = v / v_per_row;
         const int64_t c = v - m * v_per_row;
+        if (!in_bounds(m * 2 * v_per_row + v_per_row + c < 2 * total && v < total, status)) continue;
         const uint4 g4 = gu[m * 2 * v_per_row + c];
         const uint4 u4 = gu[m * 2 * v_per_row + v_per_row + c];
         const uint32_t g2[4] = {g4.x, g4.y, g4.z, g4.w};
@@ -40,7 +41,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
 
 }  // namespace
 
-cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int sm_count, cudaStream_t s) {
+cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int sm_count, cudaStream_t s,
+                            unsigned* status) {
     const int64_t total = static_cast<int64_t>(M) * (I / 8);
     const int64_t blocks_needed = (total + 255) / 256;
     const int blocks = static_cast<int>(blocks_needed < 8LL * sm_count ? blocks_needed : 8LL * sm_count);
@@ -54,7 +56,7 @@ cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, silu_mul_kernel, reinterpret_cast<const uint4*>(gu), reinterpret_cast<uint4*>(act),
-                              M, I);
+                              M, I, status);
 }
 
 }  // namespace w4a16

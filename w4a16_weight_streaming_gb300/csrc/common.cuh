@@ -14,6 +14,24 @@ namespace w4a16 {
 
 // Status codes written into the per-device status word (mirror w4a16_status).
 constexpr unsigned kErrTimeout = 5u;
+constexpr unsigned kErrBounds = 6u;
+
+// Records an error code in the status word unless an earlier error is already there (the first
+// error of a launch is the one reported).
+__device__ __forceinline__ void record_error(unsigned* status, unsigned code) { atomicCAS(status, 0u, code); }
+
+// Index checks of the debug-bounds build (compiled with W4A16_DEBUG_BOUNDS): the kernels test
+// every global-memory index against the size of its buffer before the access; a bad index records
+// kErrBounds and the access is skipped (no trap: the context stays usable). In the normal build the
+// test compiles away.
+#ifdef W4A16_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned* status) {
+    if (!ok) record_error(status, kErrBounds);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool in_bounds(bool, unsigned*) { return true; }
+#endif
 
 // ------------------------------------------------------------------------------------ misc
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -84,7 +102,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if ((spin & 31u) == 0u) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) {
-                atomicExch(status, kErrTimeout);
+                record_error(status, kErrTimeout);
                 *abort_flag = 1;
                 return false;
             }
@@ -116,7 +134,7 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatil
         if ((spin & 255u) == 0u) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) {
-                atomicExch(status, kErrTimeout);
+                record_error(status, kErrTimeout);
                 *abort_flag = 1;
                 return false;
             }
@@ -150,7 +168,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         if ((spin & 255u) == 0u) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) {
-                atomicExch(status, kErrTimeout);
+                record_error(status, kErrTimeout);
                 *abort_flag = 1;
                 return false;
             }

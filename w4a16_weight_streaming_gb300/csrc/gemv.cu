@@ -70,7 +70,7 @@ template <int MR>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restrict__ x,
                                                         const uint4* __restrict__ wr,
                                                         const uint16_t* __restrict__ sr, uint16_t* __restrict__ y,
-                                                        int N, int K, int G, int split) {
+                                                        int N, int K, int G, int split, unsigned* status) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int KB = K / 32;
     const int NG = K / G;
@@ -107,7 +107,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         for (int i = threadIdx.x; i < MR * vec_per_row; i += kThreads) {
             const int m = i / vec_per_row;
             const int c = i % vec_per_row;
-            const uint4 v = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(m) * K + sl.kb_begin * 32 + 8 * c);
+            const int64_t xi = static_cast<int64_t>(m) * K + sl.kb_begin * 32 + 8 * c;
+            const uint4 v = in_bounds(xi + 8 <= static_cast<int64_t>(MR) * K, status)
+                                ? *reinterpret_cast<const uint4*>(x + xi)
+                                : make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(xs + m * sl.klen + 8 * c) = v;
         }
     }
@@ -124,6 +127,19 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
     auto group_of = [&](int b) { return gshift >= 0 ? (b >> gshift) : b / gb; };
 
+    // index checks of the debug-bounds build: vector and scale indices within the whole buffers
+    const int64_t w_total = static_cast<int64_t>(N) * KB, s_total = static_cast<int64_t>(NG) * N;
+    const int64_t w_base = wcol - wr, s_base = scol - sr;
+    auto load_w = [&](int b) {
+        return in_bounds(w_base + static_cast<int64_t>(b) * wt < w_total, status)
+                   ? ldg_stream(wcol + static_cast<int64_t>(b) * wt)
+                   : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto load_s = [&](int b) {
+        return in_bounds(s_base + static_cast<int64_t>(group_of(b)) * wt < s_total, status)
+                   ? ldg_u16(scol + static_cast<int64_t>(group_of(b)) * wt)
+                   : static_cast<uint16_t>(0);
+    };
     int kb = sl.kb_begin + warp;
     for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
         uint4 v[kUnroll];
@@ -131,8 +147,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int b = kb + kWarps * u;
-            v[u] = ldg_stream(wcol + static_cast<int64_t>(b) * wt);
-            sb[u] = ldg_u16(scol + static_cast<int64_t>(group_of(b)) * wt);
+            v[u] = load_w(b);
+            sb[u] = load_s(b);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -141,8 +157,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         }
     }
     for (; kb < sl.kb_end; kb += kWarps) {
-        const uint4 v = ldg_stream(wcol + static_cast<int64_t>(kb) * wt);
-        const uint16_t sb = ldg_u16(scol + static_cast<int64_t>(group_of(kb)) * wt);
+        const uint4 v = load_w(kb);
+        const uint16_t sb = load_s(kb);
         gemv_block<MR>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
     }
 
@@ -159,7 +175,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
             float s = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) s += red[(w * MR + m) * 32 + l];
-            y[static_cast<int64_t>(m) * N + 32 * t + l] = __half_as_ushort(__float2half_rn(s));
+            const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
+            if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s));
         }
         return;
     }
@@ -177,14 +194,15 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         float s = 0.f;
         for (int p = 0; p < split; ++p) s += ld_dsmem_f1(map_peer(local, p));
         const int m = e / 32, l = e % 32;
-        y[static_cast<int64_t>(m) * N + 32 * t + l] = __half_as_ushort(__float2half_rn(s));
+        const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
+        if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s));
     }
     cluster_sync_all();
 }
 
 template <int MR>
 cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
-                          int N, int K, int G, int split, size_t smem, cudaStream_t s) {
+                          int N, int K, int G, int split, size_t smem, cudaStream_t s, unsigned* status) {
     auto kern = gemv_kernel<MR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -211,7 +229,8 @@ cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const ui
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kern, x, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, N, K, G, split);
+    return cudaLaunchKernelEx(&cfg, kern, x, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, N, K, G, split,
+                              status);
 }
 
 }  // namespace
@@ -227,14 +246,14 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint
                         int N, int K, int G, int split, const LaunchCtx& ctx) {
     const size_t smem = gemv_smem_bytes(M, N, K, split);
     switch (M) {
-        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
-        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream);
+        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -19,9 +19,9 @@ struct LaunchCtx {
 
 // ---- repack.cu
 cudaError_t launch_repack(const int32_t* qweight, const uint16_t* scales, uint32_t* qweight_r, uint16_t* scales_r,
-                          int N, int K, int G, cudaStream_t s);
+                          int N, int K, int G, cudaStream_t s, unsigned* status);
 cudaError_t launch_unrepack(const uint32_t* qweight_r, const uint16_t* scales_r, int32_t* qweight, uint16_t* scales,
-                            int N, int K, int G, cudaStream_t s);
+                            int N, int K, int G, cudaStream_t s, unsigned* status);
 
 // ---- gemv.cu: CUDA-core split-K GEMV, M <= 8.
 constexpr int kGemvMaxM = 8;
@@ -54,6 +54,7 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
 
 // ---- act.cu: SwiGLU activation of a fused gate+up output, act = silu(gate) * up.
-cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int sm_count, cudaStream_t s);
+cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int sm_count, cudaStream_t s,
+                            unsigned* status);
 
 }  // namespace w4a16

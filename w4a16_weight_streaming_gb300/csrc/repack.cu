@@ -35,30 +35,34 @@ __device__ __forceinline__ int tile_width(int N, int t) { return min(128, N - 12
 // One thread per 16-byte vector (k-block b, column n), v = b * N + n: reads the four canonical
 // words qweight[4b + i][n] (consecutive n -> consecutive addresses) and writes the vector at
 // tile t = n / 128, position b * w_t + (n - 128t) of that tile's [K/32][w_t] block.
-__global__ void repack_weights_kernel(const uint32_t* __restrict__ qw, uint4* __restrict__ out, int N, int K) {
+__global__ void repack_weights_kernel(const uint32_t* __restrict__ qw, uint4* __restrict__ out, int N, int K,
+                                      unsigned* status) {
     const int64_t total = static_cast<int64_t>(N) * (K / 32);
     for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
          v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(v % N);
         const int b = static_cast<int>(v / N);
         const int t = n / 128;
+        const int64_t o = static_cast<int64_t>(t) * 128 * (K / 32) + static_cast<int64_t>(b) * tile_width(N, t) + (n - 128 * t);
+        if (!in_bounds(o < total && static_cast<int64_t>(4 * b + 3) * N + n < 4 * total, status)) continue;
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) w[i] = interleave_word(qw[static_cast<int64_t>(4 * b + i) * N + n]);
-        out[static_cast<int64_t>(t) * 128 * (K / 32) + static_cast<int64_t>(b) * tile_width(N, t) + (n - 128 * t)] =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        out[o] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-__global__ void unrepack_weights_kernel(const uint4* __restrict__ in, uint32_t* __restrict__ qw, int N, int K) {
+__global__ void unrepack_weights_kernel(const uint4* __restrict__ in, uint32_t* __restrict__ qw, int N, int K,
+                                        unsigned* status) {
     const int64_t total = static_cast<int64_t>(N) * (K / 32);
     for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
          v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(v % N);
         const int b = static_cast<int>(v / N);
         const int t = n / 128;
-        const uint4 x =
-            in[static_cast<int64_t>(t) * 128 * (K / 32) + static_cast<int64_t>(b) * tile_width(N, t) + (n - 128 * t)];
+        const int64_t o = static_cast<int64_t>(t) * 128 * (K / 32) + static_cast<int64_t>(b) * tile_width(N, t) + (n - 128 * t);
+        if (!in_bounds(o < total && static_cast<int64_t>(4 * b + 3) * N + n < 4 * total, status)) continue;
+        const uint4 x = in[o];
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) qw[static_cast<int64_t>(4 * b + i) * N + n] = deinterleave_word(w[i]);
@@ -68,7 +72,7 @@ __global__ void unrepack_weights_kernel(const uint4* __restrict__ in, uint32_t* 
 // scales [K/G][N] <-> scales_r (tile t: [K/G][w_t] at element 128t * K/G); one thread per
 // canonical element i = g * N + n.
 __global__ void scales_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int N, int NG,
-                              bool to_tiles) {
+                              bool to_tiles, unsigned* status) {
     const int64_t total = static_cast<int64_t>(N) * NG;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -76,6 +80,7 @@ __global__ void scales_kernel(const uint16_t* __restrict__ in, uint16_t* __restr
         const int g = static_cast<int>(i / N);
         const int t = n / 128;
         const int64_t tiled = static_cast<int64_t>(t) * 128 * NG + static_cast<int64_t>(g) * tile_width(N, t) + (n - 128 * t);
+        if (!in_bounds(tiled < total, status)) continue;
         if (to_tiles)
             out[tiled] = in[i];
         else
@@ -91,26 +96,26 @@ int grid_for(int64_t total, int block) {
 }  // namespace
 
 cudaError_t launch_repack(const int32_t* qweight, const uint16_t* scales, uint32_t* qweight_r, uint16_t* scales_r,
-                          int N, int K, int G, cudaStream_t s) {
+                          int N, int K, int G, cudaStream_t s, unsigned* status) {
     const int64_t vec = static_cast<int64_t>(N) * (K / 32);
     repack_weights_kernel<<<grid_for(vec, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(qweight),
-                                                              reinterpret_cast<uint4*>(qweight_r), N, K);
+                                                              reinterpret_cast<uint4*>(qweight_r), N, K, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t ns = static_cast<int64_t>(N) * (K / G);
-    scales_kernel<<<grid_for(ns, 256), 256, 0, s>>>(scales, scales_r, N, K / G, true);
+    scales_kernel<<<grid_for(ns, 256), 256, 0, s>>>(scales, scales_r, N, K / G, true, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_unrepack(const uint32_t* qweight_r, const uint16_t* scales_r, int32_t* qweight, uint16_t* scales,
-                            int N, int K, int G, cudaStream_t s) {
+                            int N, int K, int G, cudaStream_t s, unsigned* status) {
     const int64_t vec = static_cast<int64_t>(N) * (K / 32);
     unrepack_weights_kernel<<<grid_for(vec, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(qweight_r),
-                                                                reinterpret_cast<uint32_t*>(qweight), N, K);
+                                                                reinterpret_cast<uint32_t*>(qweight), N, K, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t ns = static_cast<int64_t>(N) * (K / G);
-    scales_kernel<<<grid_for(ns, 256), 256, 0, s>>>(scales_r, scales, N, K / G, false);
+    scales_kernel<<<grid_for(ns, 256), 256, 0, s>>>(scales_r, scales, N, K / G, false, status);
     return cudaGetLastError();
 }
 

@@ -214,17 +214,25 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
             const uint32_t wbytes = static_cast<uint32_t>(kKB * wt * 16);
             const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
             const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
+            // (debug-bounds build: every copy's source range inside its buffer; a copy that is not
+            // issued leaves its stage incomplete, so the kernel also reports the wait's timeout)
+            const int64_t w_bytes_all = static_cast<int64_t>(N) * K / 2, s_bytes_all = static_cast<int64_t>(NG) * N * 2;
             auto issue_w = [&](int i) {  // weights and scales of stage use i (no dependence on x)
                 const int s = i % s_stages;
                 const int k0 = (c_begin + i) * KC;
                 const uint32_t fb = full_bar(s);
+                const uint4* wsrc = w_tile + static_cast<int64_t>(k0 / 32) * wt;
+                const uint16_t* ssrc = s_tile + static_cast<int64_t>(k0 / G) * wt;
                 mbar_arrive_expect_tx(fb, bytes);
-                bulk_g2s(sbase + P.w_off + s * P.w_stage, w_tile + static_cast<int64_t>(k0 / 32) * wt, wbytes, fb, pol);
-                bulk_g2s(sbase + P.s_off + s * P.s_stage, s_tile + static_cast<int64_t>(k0 / G) * wt, sbytes, fb, pol);
+                if (in_bounds((wsrc - wr) * 16 + wbytes <= w_bytes_all, status))
+                    bulk_g2s(sbase + P.w_off + s * P.w_stage, wsrc, wbytes, fb, pol);
+                if (in_bounds((ssrc - sr) * 2 + sbytes <= s_bytes_all, status))
+                    bulk_g2s(sbase + P.s_off + s * P.s_stage, ssrc, sbytes, fb, pol);
             };
             auto issue_x = [&](int i) {
                 const int s = i % s_stages;
                 const int k0 = (c_begin + i) * KC;
+                in_bounds(k0 + KC <= K && m0 < M, status);  // rows >= M of the box are zero-filled by the copy
                 const uint32_t xs = sbase + P.x_off + s * P.x_stage;
                 if (x_3d) {
                     tma_load_x_3d(xs, &tmap_x, k0, m0, full_bar(s));
@@ -414,7 +422,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
 #pragma unroll
                         for (int j = 0; j < kCols; ++j) {
                             const int m = m0 + mbase + c + j;
-                            if (m < M)
+                            if (m < M && in_bounds(static_cast<int64_t>(m) * N + n < static_cast<int64_t>(M) * N, status))
                                 y[static_cast<int64_t>(m) * N + n] =
                                     __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
                         }
@@ -449,7 +457,8 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
             const int e = 4 * e4;
             const int m = m0 + e / kTileN;
             const int c = e % kTileN;
-            if (m < M && c < wt) {
+            if (m < M && c < wt &&
+                in_bounds(static_cast<int64_t>(m) * N + n0 + c + 4 <= static_cast<int64_t>(M) * N, status)) {
                 const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
                                     (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
                 const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |

@@ -445,7 +445,15 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
 
 extern "C" {
 
-int w4a16_version(void) { return 100; }
+int w4a16_version(void) { return 200; }
+
+int w4a16_debug_bounds(void) {
+#ifdef W4A16_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 const char* w4a16_status_string(int code) {
     switch (code) {
@@ -455,6 +463,7 @@ const char* w4a16_status_string(int code) {
         case W4A16_ERR_MISALIGNED: return "W4A16_ERR_MISALIGNED: a pointer is not 16-byte aligned";
         case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA: the CUDA runtime refused the call";
         case W4A16_ERR_DEVICE_TIMEOUT: return "W4A16_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
+        case W4A16_ERR_BOUNDS: return "W4A16_ERR_BOUNDS: a kernel index check failed (debug-bounds build)";
         default: return "W4A16_ERR_UNKNOWN";
     }
 }
@@ -487,9 +496,11 @@ int w4a16_repack(const int32_t* qweight, const uint16_t* scales, void* qweight_r
                  int group, void* stream) {
     const int rc = repack_common_checks(qweight, scales, qweight_r, scales_r, N, K, group);
     if (rc != W4A16_OK) return rc;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
     const cudaError_t e = launch_repack(qweight, scales, static_cast<uint32_t*>(qweight_r),
                                         static_cast<uint16_t*>(scales_r), N, K, group,
-                                        static_cast<cudaStream_t>(stream));
+                                        static_cast<cudaStream_t>(stream), d.status);
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
@@ -497,9 +508,11 @@ int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight
                    int group, void* stream) {
     const int rc = repack_common_checks(qweight_r, scales_r, qweight, scales, N, K, group);
     if (rc != W4A16_OK) return rc;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
     const cudaError_t e = launch_unrepack(static_cast<const uint32_t*>(qweight_r),
                                           static_cast<const uint16_t*>(scales_r), qweight, scales, N, K, group,
-                                          static_cast<cudaStream_t>(stream));
+                                          static_cast<cudaStream_t>(stream), d.status);
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
@@ -579,7 +592,7 @@ int w4a16_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, void* stream
     if (overlaps(gu, gb, act, ab) || is_host_pointer(gu) || is_host_pointer(act)) return W4A16_ERR_INVALID_ARG;
     DeviceInfo d;
     if (!device_info(&d)) return W4A16_ERR_CUDA;
-    if (launch_silu_mul(gu, act, M, I, d.sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    if (launch_silu_mul(gu, act, M, I, d.sm_count, static_cast<cudaStream_t>(stream), d.status) != cudaSuccess) {
         cudaGetLastError();
         return W4A16_ERR_CUDA;
     }
