@@ -192,12 +192,16 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(a_stages * kACols);
 
-    // grid.x = column tiles x split (one cluster of `split` consecutive CTAs per tile), grid.y = row tiles
+    // grid.x = column tiles x row tiles x split: one cluster of `split` consecutive CTAs per (column
+    // tile, row tile), the row tile varying fastest, so that the CTAs streaming the same weight
+    // tile for different rows of x run side by side and all but the first find it in L2
+    const int mtiles = (M + MT - 1) / MT;
     const int rank = static_cast<int>(blockIdx.x) % split;
-    const int tile = static_cast<int>(blockIdx.x) / split;
+    const int rest = static_cast<int>(blockIdx.x) / split;
+    const int tile = rest / mtiles;
     const int n0 = tile * kTileN;
     const int wt = min(kTileN, N - n0);  // columns of this tile (32, 64, 96 or 128)
-    const int m0 = static_cast<int>(blockIdx.y) * MT;
+    const int m0 = (rest % mtiles) * MT;
     const int KB = K / 32;
     const int NG = K / G;
     const int ngs = groups_per_stage(KC, G);
@@ -509,8 +513,9 @@ template <int MT, int KC, int NI, bool GI, int DW>
 cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(c.split) * static_cast<unsigned>((N + kTileN - 1) / kTileN),
-                       static_cast<unsigned>((M + MT - 1) / MT), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(c.split) * static_cast<unsigned>((N + kTileN - 1) / kTileN) *
+                           static_cast<unsigned>((M + MT - 1) / MT),
+                       1, 1);
     cfg.blockDim = dim3(threads_for(GI, NI, DW), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -630,9 +635,10 @@ bool tc_instantiated(int m_tile, int k_chunk, int issuers, int dequant_warps) {
 }
 
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
-    (void)N;
     if (c.m_tile != 16 && c.m_tile != 32 && c.m_tile != 64 && c.m_tile != 128 && c.m_tile != 256) return false;
-    if ((M + c.m_tile - 1) / c.m_tile > 65535) return false;  // row tiles are grid.y
+    // grid.x = split x column tiles x row tiles must stay below 2^31
+    if (static_cast<int64_t>(c.split) * ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile) > 0x7fffffffLL)
+        return false;
     if (c.k_chunk != 128 && c.k_chunk != 256) return false;
     if (K % c.k_chunk != 0) return false;
     if (c.stages < 2 || c.stages > 16) return false;

@@ -148,6 +148,7 @@ int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, b
     double best = 1e30;
     int split = 1;
     for (int s = 1; s <= 16 && s <= C; ++s) {
+        if (static_cast<int64_t>(tiles) * s > 0x7fffffffLL) break;  // the grid's x extent
         TcConfig c = base;
         c.split = s;
         int slots = have_device ? tc_resident_ctas(c, G) : 0;
@@ -424,10 +425,11 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
                  "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "dequant_warps=%d split_k=%d grid=(%lld,%d,1) tmem_cols=%d smem=%zu",
+                 "dequant_warps=%d split_k=%d grid=(%lld,1,1) tmem_cols=%d smem=%zu",
                  M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
-                 ch.tc.dequant_warps, ch.tc.split, static_cast<long long>(ch.tc.split) * ((N + 127) / 128),
-                 (M + ch.tc.m_tile - 1) / ch.tc.m_tile, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
+                 ch.tc.dequant_warps, ch.tc.split,
+                 static_cast<long long>(ch.tc.split) * ((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile),
+                 tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
