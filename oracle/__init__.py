@@ -19,6 +19,12 @@ Functions and the passage each follows:
   and the down projection, act = silu(gate) * up ("Qwen3.8-27B at 764, 1,035 and 1,623 tok/s",
   section "Where the line bends": the 17,408-wide MLPs; SwiGLU is the reading taken).
 * ``repack`` / ``unrepack`` -- the library's own device layout, restated from its definition.
+* ``e2m1_to_double`` / ``e4m3_to_double`` / ``dequant_nvfp4`` / ``gemm_nvfp4`` /
+  ``gemm_nvfp4_sampled`` / ``repack_nvfp4`` / ``unrepack_nvfp4`` -- NVFP4 weights (the RTX 5090
+  runs of "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s", section "One weight read, shared by every
+  stream"): E2M1 codes, one E4M3 scale per 16 weights along K, one fp32 tensor scale g, fp16
+  activations; y = g * sum_k x * e2m1 * e4m3. The pages print no format: the reading is the
+  published NVFP4 definition.
 * ``half_to_double`` / ``double_to_half`` -- the binary16 codec, written out bit by bit.
 
 Parity status of each function is recorded in the test suite that pins it
@@ -96,6 +102,18 @@ class Oracle:
             getattr(lib, name).restype = I
             getattr(lib, name).argtypes = [P, P, I, I, I, P, P]
         lib.w4o_silu_mul.argtypes = [P, I, I, P, P]
+        D = ctypes.c_double
+        lib.w4o_e2m1_to_double.restype = D
+        lib.w4o_e2m1_to_double.argtypes = [I]
+        lib.w4o_e4m3_to_double_array.argtypes = [P, P, L]
+        lib.w4o_dequant_nvfp4.argtypes = [P, P, I, I, P]
+        lib.w4o_gemm_nvfp4.restype = I
+        lib.w4o_gemm_nvfp4.argtypes = [P, P, P, D, I, I, I, P, P, I]
+        lib.w4o_gemm_nvfp4_sampled.restype = I
+        lib.w4o_gemm_nvfp4_sampled.argtypes = [P, P, P, D, I, I, I, P, P, L, P, P]
+        for name in ("w4o_repack_nvfp4", "w4o_unrepack_nvfp4"):
+            getattr(lib, name).restype = I
+            getattr(lib, name).argtypes = [P, P, I, I, P, P]
         lib.w4o_max_threads.restype = I
         lib.w4o_has_openmp.restype = I
         self.lib = lib
@@ -184,6 +202,85 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle gemm_sampled rejected the input (rc={rc})")
         return y, a
+
+    # ---------------------------------------------------------------------------- NVFP4
+    def e2m1_to_double(self, codes) -> np.ndarray:
+        """float64 values of 4-bit E2M1 codes."""
+        c = np.asarray(codes)
+        return np.array([self.lib.w4o_e2m1_to_double(int(v)) for v in c.reshape(-1)], np.float64).reshape(c.shape)
+
+    def e4m3_to_double(self, bits) -> np.ndarray:
+        """float64 values of E4M3 bit patterns (NaN for the NaN patterns)."""
+        b = _c(bits, np.uint8)
+        out = np.empty(b.shape, np.float64)
+        self.lib.w4o_e4m3_to_double_array(_ptr(b), _ptr(out), b.size)
+        return out
+
+    def dequant_nvfp4(self, qweight, scales8) -> np.ndarray:
+        """float64 w[K, N] = e2m1(q) * e4m3(s[k/16]) (without the tensor scale)."""
+        qw = _c(qweight, np.int32)
+        sc = _c(scales8, np.uint8)
+        K, N = qw.shape[0] * 8, qw.shape[1]
+        out = np.empty((K, N), np.float64)
+        self.lib.w4o_dequant_nvfp4(_ptr(qw), _ptr(sc), K, N, _ptr(out))
+        return out
+
+    def gemm_nvfp4(self, x_bits, qweight, scales8, g: float, nthreads: int | None = None):
+        """(y, absy) float64 [M, N]: y = g * sum_k x*w, absy = |g| * sum_k |x*w|."""
+        x = _c(x_bits, np.uint16)
+        qw = _c(qweight, np.int32)
+        sc = _c(scales8, np.uint8)
+        M, K = x.shape
+        N = qw.shape[1]
+        if qw.shape[0] * 8 != K or sc.shape != (K // 16, N):
+            raise ValueError("qweight must be [K/8, N] and scales8 [K/16, N]")
+        y = np.empty((M, N), np.float64)
+        a = np.empty((M, N), np.float64)
+        rc = self.lib.w4o_gemm_nvfp4(_ptr(x), _ptr(qw), _ptr(sc), float(g), M, N, K, _ptr(y), _ptr(a),
+                                     nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle gemm_nvfp4 rejected the shape (rc={rc})")
+        return y, a
+
+    def gemm_nvfp4_sampled(self, x_bits, qweight, scales8, g: float, ms, ns):
+        """(y, absy) float64 [count] for the listed (m, n) pairs only."""
+        x = _c(x_bits, np.uint16)
+        qw = _c(qweight, np.int32)
+        sc = _c(scales8, np.uint8)
+        msa = _c(ms, np.int64)
+        nsa = _c(ns, np.int64)
+        M, K = x.shape
+        N = qw.shape[1]
+        y = np.empty(msa.shape, np.float64)
+        a = np.empty(msa.shape, np.float64)
+        rc = self.lib.w4o_gemm_nvfp4_sampled(_ptr(x), _ptr(qw), _ptr(sc), float(g), M, N, K, _ptr(msa), _ptr(nsa),
+                                             msa.size, _ptr(y), _ptr(a))
+        if rc != 0:
+            raise ValueError(f"oracle gemm_nvfp4_sampled rejected the input (rc={rc})")
+        return y, a
+
+    def repack_nvfp4(self, qweight, scales8):
+        """(wr uint32 [N*K/8], sr uint16 [N*K/16]): the NVFP4 device layout (flat)."""
+        qw = _c(qweight, np.int32)
+        sc = _c(scales8, np.uint8)
+        K, N = qw.shape[0] * 8, qw.shape[1]
+        wr = np.empty(N * K // 8, np.uint32)
+        sr = np.empty(N * (K // 16), np.uint16)
+        rc = self.lib.w4o_repack_nvfp4(_ptr(qw), _ptr(sc), K, N, _ptr(wr), _ptr(sr))
+        if rc != 0:
+            raise ValueError(f"oracle repack_nvfp4 rejected the shape (rc={rc})")
+        return wr, sr
+
+    def unrepack_nvfp4(self, wr, sr, K: int, N: int):
+        """Inverse of ``repack_nvfp4``: (qweight int32 [K/8, N], scales8 uint8 [K/16, N])."""
+        w = _c(wr, np.uint32)
+        s = _c(sr, np.uint16)
+        qw = np.empty((K // 8, N), np.int32)
+        sc = np.empty((K // 16, N), np.uint8)
+        rc = self.lib.w4o_unrepack_nvfp4(_ptr(w), _ptr(s), K, N, _ptr(qw), _ptr(sc))
+        if rc != 0:
+            raise ValueError(f"oracle unrepack_nvfp4 rejected the input (rc={rc})")
+        return qw, sc
 
     # ---------------------------------------------------------------------------- activation
     def silu_mul(self, gu_bits):
@@ -289,6 +386,34 @@ def repack(qweight, scales, group: int):
 
 def unrepack(wr, sr, K: int, N: int, group: int):
     return load().unrepack(wr, sr, K, N, group)
+
+
+def e2m1_to_double(codes):
+    return load().e2m1_to_double(codes)
+
+
+def e4m3_to_double(bits):
+    return load().e4m3_to_double(bits)
+
+
+def dequant_nvfp4(qweight, scales8):
+    return load().dequant_nvfp4(qweight, scales8)
+
+
+def gemm_nvfp4(x_bits, qweight, scales8, g: float, nthreads: int | None = None):
+    return load().gemm_nvfp4(x_bits, qweight, scales8, g, nthreads)
+
+
+def gemm_nvfp4_sampled(x_bits, qweight, scales8, g: float, ms, ns):
+    return load().gemm_nvfp4_sampled(x_bits, qweight, scales8, g, ms, ns)
+
+
+def repack_nvfp4(qweight, scales8):
+    return load().repack_nvfp4(qweight, scales8)
+
+
+def unrepack_nvfp4(wr, sr, K: int, N: int):
+    return load().unrepack_nvfp4(wr, sr, K, N)
 
 
 # ------------------------------------------------------------------------------------ check

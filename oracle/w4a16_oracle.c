@@ -328,3 +328,158 @@ int w4o_has_openmp(void) {
     return 0;
 #endif
 }
+
+/* ---------------------------------------------------------------- NVFP4 weights
+ *
+ * The RTX 5090 runs of "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s" (ai.satyajit.si), section
+ * "One weight read, shared by every stream", store the weights as NVFP4; the pages print no
+ * format. Reading taken (the published NVFP4 definition): every weight is a 4-bit E2M1 code, every
+ * 16 consecutive weights along K share one E4M3 scale, and the tensor has one fp32 scale g.
+ * Activations stay fp16 (the W4A16 contract of this library):
+ *
+ *   qweight int32 [K/8][N]: nibble (k mod 8) of qweight[k/8][n] is the E2M1 code of w[k][n]
+ *     (the container of the 4-bit format above);
+ *   scales8 uint8 [K/16][N]: E4M3 bit patterns;
+ *   w[k][n] = e2m1(code) * e4m3(scales8[k/16][n])   (at most 2 x 4 significant bits: exact in
+ *     double, and exact in fp16 for every finite scale);
+ *   y[m][n] = g * sum_k x[m][k] * w[k][n], summed here in fp64 in ascending k.
+ */
+
+/* E2M1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0 is subnormal
+ * (m * 2^-1). Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double w4o_e2m1_to_double(int code) {
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* E4M3: sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0; exponent 0 is subnormal
+ * (m/8 * 2^-6); exponent 15 with mantissa 7 is NaN (no infinities). Largest finite value 448. */
+double w4o_e4m3_to_double(uint8_t b) {
+    int s = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp(m / 8.0, -6);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+void w4o_e4m3_to_double_array(const uint8_t* b, double* out, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) out[i] = w4o_e4m3_to_double(b[i]);
+}
+
+double w4o_weight_nvfp4(const int32_t* qweight, const uint8_t* scales8, int N, int k, int n) {
+    return w4o_e2m1_to_double(w4o_nibble(qweight, N, k, n)) *
+           w4o_e4m3_to_double(scales8[(size_t)(k / 16) * (size_t)N + (size_t)n]);
+}
+
+void w4o_dequant_nvfp4(const int32_t* qweight, const uint8_t* scales8, int K, int N, double* w_out) {
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) w_out[(size_t)k * N + n] = w4o_weight_nvfp4(qweight, scales8, N, k, n);
+}
+
+/* y = g * sum_k x w and absy = |g| * sum_k |x w| (the tolerance scale of the effective weights
+ * g * w), for x given as fp16 bits [M][K]. */
+int w4o_gemm_nvfp4(const uint16_t* x, const int32_t* qweight, const uint8_t* scales8, double g, int M, int N,
+                   int K, double* y, double* absy, int nthreads) {
+    if (M < 0 || N <= 0 || K <= 0 || K % 16 != 0) return 1;
+    if (nthreads < 1) nthreads = 1;
+    double* xd = (double*)malloc(sizeof(double) * ((size_t)M * K + 1));
+    if (!xd) return 2;
+    w4o_half_to_double_array(x, xd, (int64_t)M * K);
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double* col = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!col) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 8)
+#endif
+            for (int n = 0; n < N; ++n) {
+                for (int k = 0; k < K; ++k) col[k] = w4o_weight_nvfp4(qweight, scales8, N, k, n);
+                for (int m = 0; m < M; ++m) {
+                    double s = 0.0, a = 0.0;
+                    column_dot(xd + (size_t)m * K, K, col, &s, &a);
+                    y[(size_t)m * N + n] = g * s;
+                    absy[(size_t)m * N + n] = fabs(g) * a;
+                }
+            }
+            free(col);
+        }
+    }
+    free(xd);
+    return failed ? 2 : 0;
+}
+
+/* The same for a list of (m, n) pairs. */
+int w4o_gemm_nvfp4_sampled(const uint16_t* x, const int32_t* qweight, const uint8_t* scales8, double g, int M,
+                           int N, int K, const int64_t* ms, const int64_t* ns, int64_t count, double* y,
+                           double* absy) {
+    if (M < 0 || N <= 0 || K <= 0 || K % 16 != 0) return 1;
+    for (int64_t i = 0; i < count; ++i) {
+        if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N) return 1;
+        double s = 0.0, a = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double p = w4o_half_to_double(x[(size_t)ms[i] * K + k]) *
+                       w4o_weight_nvfp4(qweight, scales8, N, k, (int)ns[i]);
+            s += p;
+            a += fabs(p);
+        }
+        y[i] = g * s;
+        absy[i] = fabs(g) * a;
+    }
+    return 0;
+}
+
+/* The library's NVFP4 device layout: the weight words sit where the int4 layout puts them
+ * (weight_word_index) but keep the canonical nibble order (k mod 8 at nibble k mod 8), and each
+ * E4M3 scale is stored as the fp16 number of equal value (exact: an E4M3 value has 4 significant
+ * bits and lies within the fp16 range) at scale_index with a group of 16. */
+int w4o_repack_nvfp4(const int32_t* qweight, const uint8_t* scales8, int K, int N, uint32_t* wr, uint16_t* sr) {
+    if (!layout_ok(N, K, 16)) return 1;
+    size_t nwords = (size_t)N * K / 8;
+    memset(wr, 0, nwords * sizeof(uint32_t));
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < N; ++n) {
+            uint32_t q = (uint32_t)w4o_nibble(qweight, N, k, n);
+            wr[weight_word_index(K, N, k, n)] |= q << (4 * (k % 8));
+        }
+    }
+    for (int g = 0; g < K / 16; ++g)
+        for (int n = 0; n < N; ++n)
+            sr[scale_index(K, N, 16, g, n)] = w4o_double_to_half(w4o_e4m3_to_double(scales8[(size_t)g * N + n]));
+    return 0;
+}
+
+/* Inverse of w4o_repack_nvfp4. An fp16 scale maps back to the E4M3 pattern of equal value (the
+ * positive pattern for zero); a value no E4M3 pattern has is an error (rc 2). */
+int w4o_unrepack_nvfp4(const uint32_t* wr, const uint16_t* sr, int K, int N, int32_t* qweight, uint8_t* scales8) {
+    if (!layout_ok(N, K, 16)) return 1;
+    size_t nwords = (size_t)N * K / 8;
+    memset(qweight, 0, nwords * sizeof(int32_t));
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < N; ++n) {
+            uint32_t q = (wr[weight_word_index(K, N, k, n)] >> (4 * (k % 8))) & 0xFu;
+            uint32_t* dst = (uint32_t*)&qweight[(size_t)(k / 8) * N + n];
+            *dst |= q << (4 * (k % 8));
+        }
+    }
+    for (int g = 0; g < K / 16; ++g) {
+        for (int n = 0; n < N; ++n) {
+            double v = w4o_half_to_double(sr[scale_index(K, N, 16, g, n)]);
+            int found = -1;
+            for (int b = 0; b < 256 && found < 0; ++b)
+                if (w4o_e4m3_to_double((uint8_t)b) == v && !(v == 0.0 && b != 0)) found = b;
+            if (found < 0) return 2;
+            scales8[(size_t)g * N + n] = (uint8_t)found;
+        }
+    }
+    return 0;
+}

@@ -6,7 +6,10 @@ Sources of truth used here (none of them is the oracle's own code):
   * exact rational arithmetic (``fractions.Fraction``) on tiny inputs;
   * closed forms: one-hot rows, all-ones rows, zero scales, constant weights, linearity;
   * for the activation: the identity silu(g) - silu(-g) = g, its limits, and scipy's logistic;
-  * handcrafted packed words whose nibble order is known by construction.
+  * handcrafted packed words whose nibble order is known by construction;
+  * for NVFP4 weights: torch's float8_e4m3fn -> float conversion (a library routine) for every
+    E4M3 pattern, the literal 16-value E2M1 table of the format definition, exact rationals, and
+    closed forms (one-hot rows, zero scales, sign flips, the tensor scale's linearity).
 
 The W4A16 definition (4-bit weights, 16-bit activations) follows "RTX 3090 Tested: Qwen's 381
 tok/s Myth Busted" (kongchang.com), section "What Exactly Is This Stack"; the product of one
@@ -338,10 +341,148 @@ def pin_silu_limits(o):
     assert np.array_equal(act2, 2.0 * act1)
 
 
+# ------------------------------------------------------------------------------ NVFP4 weights
+# The 16 E2M1 values as the NVFP4 / OCP microscaling format definition lists them (sign bit 3,
+# then exponent and mantissa): a literal table, not derived from the oracle's decoder.
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def pin_e2m1_table(o):
+    got = o.e2m1_to_double(np.arange(16))
+    assert np.array_equal(got, np.array(E2M1_VALUES))
+    assert np.array_equal(np.signbit(got), np.arange(16) >= 8)
+
+
+def pin_e4m3_all_patterns(o):
+    # every E4M3 pattern against torch's float8_e4m3fn -> float32 conversion (a library routine)
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).float().double().numpy()
+    got = o.e4m3_to_double(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got)) and set(np.flatnonzero(nan)) == {0x7F, 0xFF}
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def _nvfp4_case(rng, M, K, N):
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    s8 = rng.integers(0, 0x7F, size=(K // 16, N)).astype(np.uint8)  # all finite positive patterns
+    x = rng.normal(0.0, 1.0, size=(M, K)).astype(np.float16)
+    return q, s8, x
+
+
+def _frac_e2m1(c):
+    return Fraction(E2M1_VALUES[c]) if c not in (0, 8) else Fraction(0)
+
+
+def _frac_e4m3(b):
+    return Fraction(torch.tensor([b], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item())
+
+
+def pin_nvfp4_bruteforce_fraction(o):
+    # y = g * sum_k x * e2m1 * e4m3(s[k // 16]) in exact rationals; the oracle's fp64 sum of exact
+    # products over K = 32..64 terms is within a few ulps
+    rng = np.random.default_rng(RNG_SEED + 40)
+    for (M, K, N, g) in [(1, 32, 2, 0.25), (2, 48, 3, 1.0), (3, 64, 2, 3.0)]:
+        q, s8, x = _nvfp4_case(rng, M, K, N)
+        qw = inputs.pack_nibbles(q)
+        y, a = o.gemm_nvfp4(x.view(np.uint16), qw, s8, g)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(Fraction(float(x[m, k])) * _frac_e2m1(int(q[k, n])) * _frac_e4m3(int(s8[k // 16, n]))
+                            for k in range(K))
+                exact *= Fraction(g)
+                absx = Fraction(g) * sum(abs(Fraction(float(x[m, k])) * _frac_e2m1(int(q[k, n])) *
+                                             _frac_e4m3(int(s8[k // 16, n]))) for k in range(K))
+                assert abs(Fraction(y[m, n]) - exact) <= Fraction(2) ** -48 * (absx + 1)
+                assert abs(Fraction(a[m, n]) - absx) <= Fraction(2) ** -48 * (absx + 1)
+
+
+def pin_nvfp4_one_hot(o):
+    # x = e_k returns g * e2m1(q[k, :]) * e4m3(s[k // 16, :]) exactly, at block edges too
+    rng = np.random.default_rng(RNG_SEED + 41)
+    K, N, g = 64, 16, 0.5
+    q, s8, _ = _nvfp4_case(rng, 1, K, N)
+    qw = inputs.pack_nibbles(q)
+    ks = [0, 7, 8, 15, 16, 17, 31, 32, 63]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    y, _ = o.gemm_nvfp4(x.view(np.uint16), qw, s8, g)
+    val = np.array(E2M1_VALUES)
+    s_ref = torch.from_numpy(s8.copy()).view(torch.float8_e4m3fn).double().numpy()
+    for i, k in enumerate(ks):
+        assert np.array_equal(y[i], g * val[q[k]] * s_ref[k // 16])
+
+
+def pin_nvfp4_zero_scales_sign_and_tensor_scale(o):
+    rng = np.random.default_rng(RNG_SEED + 42)
+    K, N = 96, 8
+    q, s8, x = _nvfp4_case(rng, 3, K, N)
+    qw = inputs.pack_nibbles(q)
+    xb = x.view(np.uint16)
+    y0, _ = o.gemm_nvfp4(xb, qw, np.zeros_like(s8), 1.0)
+    assert np.all(y0 == 0.0)
+    y1, a1 = o.gemm_nvfp4(xb, qw, s8, 1.0)
+    yn, an = o.gemm_nvfp4(xb, inputs.pack_nibbles(q ^ 8), s8, 1.0)  # every sign bit flipped
+    assert np.array_equal(yn, -y1) and np.array_equal(an, a1)
+    y3, a3 = o.gemm_nvfp4(xb, qw, s8, 3.0)
+    assert np.array_equal(y3, 3.0 * y1) and np.array_equal(a3, 3.0 * a1)
+    yq, _ = o.gemm_nvfp4(xb, qw, s8, -0.25)
+    assert np.array_equal(yq, -0.25 * y1)
+
+
+def pin_nvfp4_dequant_and_sampled(o):
+    rng = np.random.default_rng(RNG_SEED + 43)
+    K, N = 128, 24
+    q, s8, x = _nvfp4_case(rng, 4, K, N)
+    qw = inputs.pack_nibbles(q)
+    w = o.dequant_nvfp4(qw, s8)
+    s_ref = torch.from_numpy(s8.copy()).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(w, np.array(E2M1_VALUES)[q] * np.repeat(s_ref, 16, axis=0))
+    # every weight is exactly an fp16 number (the product of 2 and 4 significant bits)
+    assert np.array_equal(w.astype(np.float16).astype(np.float64), w)
+    y, a = o.gemm_nvfp4(x.view(np.uint16), qw, s8, 0.125)
+    ms = np.array([0, 3, 1, 2, 3]); ns = np.array([0, 23, 5, 11, 17])
+    ys, as_ = o.gemm_nvfp4_sampled(x.view(np.uint16), qw, s8, 0.125, ms, ns)
+    assert np.array_equal(ys, y[ms, ns]) and np.array_equal(as_, a[ms, ns])
+
+
+def pin_nvfp4_repack(o):
+    # natural nibble order inside the words of the int4 device layout, scales as equal-valued fp16
+    K, N = 64, 160
+    q = np.zeros((K, N), np.uint8)
+    s8 = np.zeros((K // 16, N), np.uint8)
+    for (k, n, v) in [(0, 0, 1), (1, 0, 2), (7, 0, 3), (8, 0, 4), (33, 5, 5), (63, 127, 6), (9, 130, 7)]:
+        q[k, n] = v
+    s8[1, 3] = 0x38
+    s8[3, 150] = 0x01
+    wr, sr = o.repack_nvfp4(inputs.pack_nibbles(q), s8)
+    # tile 0 (128 wide): word ((b * 128 + c) * 4 + w), nibble k % 8
+    assert wr[0] == (1 | 2 << 4 | 3 << 28) and wr[1] == 4
+    assert wr[(1 * 128 + 5) * 4 + 0] == 5 << 4
+    assert wr[(1 * 128 + 127) * 4 + 3] == 6 << 28
+    # tile 1 (32 wide) starts at word 16 * 1 * K
+    assert wr[16 * K + (0 * 32 + 2) * 4 + 1] == 7 << 4
+    # scales: tile 0 [K/16][128], tile 1 [K/16][32] after 128 * K/16 entries
+    assert sr[1 * 128 + 3] == np.float16(1.0).view(np.uint16)
+    assert sr[128 * (K // 16) + 3 * 32 + 22] == np.float16(2.0 ** -9).view(np.uint16)
+    qw2, s82 = o.unrepack_nvfp4(wr, sr, K, N)
+    assert np.array_equal(qw2, inputs.pack_nibbles(q)) and np.array_equal(s82, s8)
+    rng = np.random.default_rng(RNG_SEED + 44)
+    q, s8, _ = _nvfp4_case(rng, 1, 256, 96)
+    qw = inputs.pack_nibbles(q)
+    wr, sr = o.repack_nvfp4(qw, s8)
+    qw2, s82 = o.unrepack_nvfp4(wr, sr, 256, 96)
+    assert np.array_equal(qw2, qw) and np.array_equal(s82, s8)
+
+
 PINS = [pin_half_decode_all, pin_half_encode, pin_dequant_exhaustive, pin_nibble_order, pin_pack_roundtrip,
         pin_bruteforce_fraction, pin_exact_dyadic, pin_one_hot, pin_all_ones, pin_zero_scales,
         pin_constant_weights, pin_linearity, pin_sampled_matches_full, pin_threads_deterministic,
-        pin_repack_positions, pin_repack_roundtrip, pin_silu_identity, pin_silu_against_library, pin_silu_limits]
+        pin_repack_positions, pin_repack_roundtrip, pin_silu_identity, pin_silu_against_library, pin_silu_limits,
+        pin_e2m1_table, pin_e4m3_all_patterns, pin_nvfp4_bruteforce_fraction, pin_nvfp4_one_hot,
+        pin_nvfp4_zero_scales_sign_and_tensor_scale, pin_nvfp4_dequant_and_sampled, pin_nvfp4_repack]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -372,6 +513,14 @@ MUTANTS = {
                              "gu[(size_t)m * 2 * I + I + i]);\n            const double u = w4o_half_to_double(gu[(size_t)m * 2 * I + i]);"),
     "silu_without_up": ("g / (1.0 + exp(-g)) * u;", "g / (1.0 + exp(-g));"),
     "silu_sigmoid_only": ("g / (1.0 + exp(-g)) * u;", "1.0 / (1.0 + exp(-g)) * u;"),
+    "e2m1_subnormal_as_normal": ("double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                                 "double v = ldexp(1.0 + 0.5 * m, e - 1);"),
+    "e4m3_wrong_bias": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "nvfp4_block_of_32": ("scales8[(size_t)(k / 16) * (size_t)N + (size_t)n]);",
+                          "scales8[(size_t)(k / 32) * (size_t)N + (size_t)n]);"),
+    "nvfp4_tensor_scale_dropped": ("y[(size_t)m * N + n] = g * s;", "y[(size_t)m * N + n] = s;"),
+    "nvfp4_repack_permuted": ("wr[weight_word_index(K, N, k, n)] |= q << (4 * (k % 8));",
+                              "wr[weight_word_index(K, N, k, n)] |= q << (4 * kPosOfJ[k % 8]);"),
 }
 
 

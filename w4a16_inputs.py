@@ -65,6 +65,23 @@ def generate_weights(K: int, N: int, group: int = GROUP, seed: int = 0, gen: tor
     return pack_nibbles(q.numpy()), half_bits(scales)
 
 
+# NVFP4 weights: 4-bit E2M1 codes, one E4M3 scale pattern per 16 weights along K, one fp32 tensor
+# scale. Codes are drawn uniformly from all 16 patterns; scale patterns uniformly from
+# [0x30, 0x40) (values 0.5 .. 1.875: every exponent/mantissa combination of that binade pair);
+# the tensor scale is 1/256, so that |g * w| <= 6 * 1.875 / 256 ~ 0.044, the range of the int4
+# workload's weights.
+NVFP4_BLOCK = 16
+NVFP4_TENSOR_SCALE = 1.0 / 256.0
+
+
+def generate_nvfp4_weights(K: int, N: int, seed: int = 0, gen: torch.Generator | None = None):
+    """(qweight int32 [K/8, N] of E2M1 codes, scales8 uint8 [K/16, N] of E4M3 patterns, g float)."""
+    g = gen if gen is not None else torch.Generator("cpu").manual_seed(seed)
+    q = torch.randint(0, 16, (K, N), generator=g, dtype=torch.uint8)
+    s8 = torch.randint(0x30, 0x40, (K // NVFP4_BLOCK, N), generator=g, dtype=torch.uint8)
+    return pack_nibbles(q.numpy()), s8.numpy().copy(), NVFP4_TENSOR_SCALE
+
+
 def generate(M: int, K: int, N: int, group: int = GROUP, seed: int = 0):
     """dict(x uint16 [M, K], qweight int32 [K/8, N], scales uint16 [K/G, N]) for one matrix."""
     g = torch.Generator("cpu").manual_seed(seed)
