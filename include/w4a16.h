@@ -176,6 +176,50 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out);
  */
 int w4a16_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, void* stream);
 
+/*
+ * NVFP4 weights (the RTX 5090 runs of "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s", section "One
+ * weight read, shared by every stream", keep their weights in NVFP4; the pages print no format, so
+ * the published NVFP4 definition is the reading). Activations stay fp16, as for every call here:
+ *   qweight  int32 [K/8][N]: nibble (k mod 8) of qweight[k/8][n] is the 4-bit E2M1 code of w[k][n]
+ *            (sign bit 3; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6);
+ *   scales8  uint8 [K/16][N]: E4M3 bit patterns (bias 7, subnormals, no infinities), one per 16
+ *            consecutive k of a column;
+ *   tensor_scale: one fp32 per matrix;
+ *   y[m][n] = fp16_rne(tensor_scale * sum_k x[m][k] * e2m1(q[k][n]) * e4m3(s[k/16][n])),
+ *            fp32 accumulation. e2m1 * e4m3 is exact in fp16, so the dequantised weight is exact.
+ * Acceptance bound per element, as for int4: |y - y_ref| <= 2^-10 |y_ref| + 2^-10 sum_k |x g w|.
+ * Shapes: N % 32 == 0, K % 64 == 0, N <= 2^23, K <= 2^22 (K % 128 for the tensor-core tiles; the
+ * CUDA-core GEMV takes M <= 8 for the other K). Errors as for w4a16_gemm; a non-finite
+ * tensor_scale is W4A16_ERR_INVALID_ARG.
+ */
+
+/* Bytes of the repacked NVFP4 scale buffer: (K/16) * N * 2 (fp16); the repacked weights take
+ * K * N / 2 bytes. 0 for an unsupported shape. */
+size_t w4a16_repacked_nvfp4_scales_bytes(int N, int K);
+
+/* One-time re-layout of canonical NVFP4 weights into the device layout: the weight words move as
+ * in w4a16_repack but keep the canonical nibble order (byte i of a word = codes of k offsets 2i
+ * and 2i+1); every E4M3 scale becomes the fp16 number of equal value (exact) in the tiled
+ * [K/16][w_t] layout of w4a16_repack. Device pointers, 16-byte aligned, no overlaps. */
+int w4a16_repack_nvfp4(const int32_t* qweight, const uint8_t* scales8, void* qweight_r, void* scales_r, int N, int K,
+                       void* stream);
+
+/* Exact inverse of w4a16_repack_nvfp4 (each fp16 scale back to its E4M3 pattern). */
+int w4a16_unrepack_nvfp4(const void* qweight_r, const void* scales_r, int32_t* qweight, uint8_t* scales8, int N,
+                         int K, void* stream);
+
+/* y[M,N] = x[M,K] . dequant(W) for repacked NVFP4 weights; the same kernels, dispatcher and
+ * plans as w4a16_gemm (x, y fp16 device buffers). */
+int w4a16_gemm_nvfp4(const uint16_t* x, const void* qweight_r, const void* scales_r, float tensor_scale, uint16_t* y,
+                     int M, int N, int K, void* stream);
+
+/* As w4a16_gemm_nvfp4 with an explicit plan (the fields of w4a16_gemm_ex). */
+int w4a16_gemm_nvfp4_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, float tensor_scale,
+                        uint16_t* y, int M, int N, int K, const w4a16_plan* plan, void* stream);
+
+/* The automatic plan of w4a16_gemm_nvfp4 for this shape (host only). */
+int w4a16_plan_for_nvfp4(int M, int N, int K, w4a16_plan* out);
+
 /* Describes the last GEMM this process launched (path, tile, split, grid) into buf (NUL
  * terminated, truncated to len). Host only. Returns W4A16_OK or INVALID_ARG. */
 int w4a16_last_dispatch(char* buf, size_t len);

@@ -216,3 +216,21 @@ def test_selftest_rejects_bad_mode(W):
     # host-side check before any launch
     assert W.w4a16_selftest_wait_timeout(2) == 1
     assert W.w4a16_selftest_wait_timeout(-1) == 1
+
+
+def test_nvfp4_host_checks(W):
+    # argument checks of the NVFP4 entry points, before any device work
+    assert W.w4a16_repacked_nvfp4_scales_bytes(256, 1024) == (1024 // 16) * 256 * 2
+    assert W.w4a16_repacked_nvfp4_scales_bytes(250, 1024) == 0
+    assert W.w4a16_repack_nvfp4(0, FAKE, FAKE * 2, FAKE * 3, 1024, 1024, None) == 1
+    assert W.w4a16_repack_nvfp4(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 1000, 1024, None) == 2
+    assert W.w4a16_repack_nvfp4(FAKE + 2, FAKE * 2, FAKE * 3, FAKE * 4, 1024, 1024, None) == 3
+    assert W.w4a16_unrepack_nvfp4(FAKE, FAKE * 2, FAKE * 3, 0, 1024, 1024, None) == 1
+    assert W.w4a16_gemm_nvfp4(FAKE, FAKE * 2, FAKE * 3, float("nan"), FAKE * 4, 1, 1024, 1024, None) == 1
+    assert W.w4a16_gemm_nvfp4(FAKE, FAKE * 2, FAKE * 3, float("inf"), FAKE * 4, 1, 1024, 1024, None) == 1
+    assert W.w4a16_gemm_nvfp4(FAKE, FAKE * 2, FAKE * 3, 1.0, FAKE * 4, 1, 1024, 1000, None) == 2
+    p = W.w4a16_plan_for_nvfp4(16, 34816, 5120)
+    assert p.path == W.PATH_TC and p.m_tile == 16
+    assert W.w4a16_plan_for_nvfp4(1, 5120, 5120).path == W.PATH_GEMV
+    with pytest.raises(W.W4A16Error):
+        W.w4a16_plan_for_nvfp4(9, 5120, 5120 + 64)  # K % 128 != 0 needs the GEMV, which takes M <= 8

@@ -37,7 +37,8 @@ EXPORTED = [
     "w4a16_version", "w4a16_status_string", "w4a16_repacked_qweight_bytes", "w4a16_repacked_scales_bytes",
     "w4a16_repack", "w4a16_unrepack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_plan_for", "w4a16_last_dispatch",
     "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout", "w4a16_gemm_host",
-    "w4a16_silu_mul", "w4a16_debug_bounds",
+    "w4a16_silu_mul", "w4a16_debug_bounds", "w4a16_repacked_nvfp4_scales_bytes", "w4a16_repack_nvfp4",
+    "w4a16_unrepack_nvfp4", "w4a16_gemm_nvfp4", "w4a16_gemm_nvfp4_ex", "w4a16_plan_for_nvfp4",
 ]
 
 
@@ -92,6 +93,18 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4a16_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.w4a16_selftest_wait_timeout.restype = I
     lib.w4a16_selftest_wait_timeout.argtypes = [I, P]
+    F = ctypes.c_float
+    lib.w4a16_repacked_nvfp4_scales_bytes.restype = S
+    lib.w4a16_repacked_nvfp4_scales_bytes.argtypes = [I, I]
+    for n in ("w4a16_repack_nvfp4", "w4a16_unrepack_nvfp4"):
+        getattr(lib, n).restype = I
+        getattr(lib, n).argtypes = [P, P, P, P, I, I, P]
+    lib.w4a16_gemm_nvfp4.restype = I
+    lib.w4a16_gemm_nvfp4.argtypes = [P, P, P, F, P, I, I, I, P]
+    lib.w4a16_gemm_nvfp4_ex.restype = I
+    lib.w4a16_gemm_nvfp4_ex.argtypes = [P, P, P, F, P, I, I, I, ctypes.POINTER(Plan), P]
+    lib.w4a16_plan_for_nvfp4.restype = I
+    lib.w4a16_plan_for_nvfp4.argtypes = [I, I, I, ctypes.POINTER(Plan)]
     return lib
 
 
@@ -150,6 +163,39 @@ def w4a16_gemm_host(x_host: int, x_dev: int, qweight_r: int, scales_r: int, y_de
 
 def w4a16_silu_mul(gu: int, act: int, M: int, I: int, stream: int | None) -> int:
     return lib.w4a16_silu_mul(gu, act, M, I, stream)
+
+
+def w4a16_repacked_nvfp4_scales_bytes(N: int, K: int) -> int:
+    return lib.w4a16_repacked_nvfp4_scales_bytes(N, K)
+
+
+def w4a16_repack_nvfp4(qweight: int, scales8: int, qweight_r: int, scales_r: int, N: int, K: int,
+                       stream: int | None) -> int:
+    return lib.w4a16_repack_nvfp4(qweight, scales8, qweight_r, scales_r, N, K, stream)
+
+
+def w4a16_unrepack_nvfp4(qweight_r: int, scales_r: int, qweight: int, scales8: int, N: int, K: int,
+                         stream: int | None) -> int:
+    return lib.w4a16_unrepack_nvfp4(qweight_r, scales_r, qweight, scales8, N, K, stream)
+
+
+def w4a16_gemm_nvfp4(x: int, qweight_r: int, scales_r: int, tensor_scale: float, y: int, M: int, N: int, K: int,
+                     stream: int | None) -> int:
+    return lib.w4a16_gemm_nvfp4(x, qweight_r, scales_r, tensor_scale, y, M, N, K, stream)
+
+
+def w4a16_gemm_nvfp4_ex(x: int, qweight_r: int, scales_r: int, tensor_scale: float, y: int, M: int, N: int, K: int,
+                        plan: Plan | None, stream: int | None) -> int:
+    return lib.w4a16_gemm_nvfp4_ex(x, qweight_r, scales_r, tensor_scale, y, M, N, K,
+                                   ctypes.byref(plan) if plan is not None else None, stream)
+
+
+def w4a16_plan_for_nvfp4(M: int, N: int, K: int) -> Plan:
+    p = Plan()
+    rc = lib.w4a16_plan_for_nvfp4(M, N, K, ctypes.byref(p))
+    if rc != OK:
+        raise W4A16Error(rc, "w4a16_plan_for_nvfp4")
+    return p
 
 
 def w4a16_plan_for(M: int, N: int, K: int, group: int) -> Plan:
@@ -238,4 +284,37 @@ def gemm(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor, N: in
         plan = Plan(**plan)
     _check(w4a16_gemm_ex(x.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K, group, plan,
                          _stream_handle(stream)), "w4a16_gemm")
+    return y
+
+
+# ------------------------------------------------------------------------------ NVFP4 weights
+def repack_nvfp4(qweight: torch.Tensor, scales8: torch.Tensor, stream=None):
+    """Device layout from canonical NVFP4 device tensors (int32 [K/8, N] of E2M1 codes, uint8
+    [K/16, N] of E4M3 patterns): (qweight_r int32, scales_r int16 of fp16 bits)."""
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    qw_r = torch.empty(N * K // 8, dtype=torch.int32, device=qweight.device)
+    sc_r = torch.empty(max(w4a16_repacked_nvfp4_scales_bytes(N, K) // 2, 1), dtype=torch.int16, device=qweight.device)
+    _check(w4a16_repack_nvfp4(qweight.data_ptr(), scales8.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), N, K,
+                              _stream_handle(stream)), "w4a16_repack_nvfp4")
+    return qw_r, sc_r
+
+
+def unrepack_nvfp4(qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int, stream=None):
+    qw = torch.empty((K // 8, N), dtype=torch.int32, device=qweight_r.device)
+    s8 = torch.empty((K // 16, N), dtype=torch.uint8, device=qweight_r.device)
+    _check(w4a16_unrepack_nvfp4(qweight_r.data_ptr(), scales_r.data_ptr(), qw.data_ptr(), s8.data_ptr(), N, K,
+                                _stream_handle(stream)), "w4a16_unrepack_nvfp4")
+    return qw, s8
+
+
+def gemm_nvfp4(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor, tensor_scale: float, N: int, K: int,
+               y: torch.Tensor | None = None, plan: Plan | dict | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] (float16) = x[M, K] (float16, CUDA) . dequant(W) for repacked NVFP4 weights."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if isinstance(plan, dict):
+        plan = Plan(**plan)
+    _check(w4a16_gemm_nvfp4_ex(x.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), float(tensor_scale),
+                               y.data_ptr(), M, N, K, plan, _stream_handle(stream)), "w4a16_gemm_nvfp4")
     return y

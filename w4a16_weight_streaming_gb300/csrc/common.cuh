@@ -444,6 +444,25 @@ __device__ __forceinline__ void dequant8(uint32_t word, uint32_t s2, uint32_t ou
     out[3] = hmul2(hfma2(d, kSixteenth, kNeg72), s2);
 }
 
+// NVFP4 weights: out[i] = (w[2i], w[2i+1]) with w = e2m1(code) * s, s2 = (s, s) the fp16 value of
+// the block's E4M3 scale. The word keeps the canonical nibble order (code of k offset j in nibble
+// j), so byte i holds the codes of k offsets 2i and 2i+1 and one hardware conversion turns it into
+// that fp16 pair (E2M1 values are exact in fp16). e2m1 * s has at most 2 + 4 significant bits and
+// lies within the fp16 normal range for every finite E4M3 scale: the multiply is exact.
+__device__ __forceinline__ void dequant8_nvfp4(uint32_t word, uint32_t s2, uint32_t out[4]) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 a0, a1, a2, a3;\n\t"
+        "mov.b32 {a0, a1, a2, a3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, a0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, a1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, a2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, a3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(word));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = hmul2(h[i], s2);
+}
+
 // Two fp32 accumulations acc0 += lo(w2) * lo(x2), acc1 += hi(w2) * hi(x2): fp16 operands, the
 // exact product rounded once into fp32.
 __device__ __forceinline__ void fma2_mixed(float& acc0, float& acc1, uint32_t w2, uint32_t x2) {

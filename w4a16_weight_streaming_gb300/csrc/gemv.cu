@@ -45,16 +45,21 @@ __device__ __forceinline__ GemvSlice slice_of(int rank, int split, int KB) {
     return s;
 }
 
-// acc[c][m][h]: chain c (word parity), row m, half h (even / odd k of a pair).
-template <int MR>
-__device__ __forceinline__ void gemv_block(const uint4 v, uint16_t sbits, const __half* xs_blk, int klen,
+// acc[c][m][h]: chain c (word parity), row m, half h (even / odd k of a pair). sbits: the scale of
+// the block's 32 k (int4), or the scales of its two 16-k halves (NVFP4: lo16 = k 0..15).
+template <int MR, bool FP4>
+__device__ __forceinline__ void gemv_block(const uint4 v, uint32_t sbits, const __half* xs_blk, int klen,
                                            float (&acc)[2][MR][2]) {
-    const uint32_t s2 = static_cast<uint32_t>(sbits) | (static_cast<uint32_t>(sbits) << 16);
+    const uint32_t slo = sbits & 0xFFFFu, shi = FP4 ? (sbits >> 16) : slo;
+    const uint32_t s2a = slo | (slo << 16), s2b = shi | (shi << 16);
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint32_t w2[4];
-        dequant8(words[i], s2, w2);
+        if (FP4)
+            dequant8_nvfp4(words[i], i < 2 ? s2a : s2b, w2);
+        else
+            dequant8(words[i], s2a, w2);
 #pragma unroll
         for (int m = 0; m < MR; ++m) {
             const uint4 xv = *reinterpret_cast<const uint4*>(xs_blk + m * klen + 8 * i);
@@ -66,11 +71,12 @@ __device__ __forceinline__ void gemv_block(const uint4 v, uint16_t sbits, const 
     }
 }
 
-template <int MR>
+template <int MR, bool FP4>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restrict__ x,
                                                         const uint4* __restrict__ wr,
                                                         const uint16_t* __restrict__ sr, uint16_t* __restrict__ y,
-                                                        int N, int K, int G, int split, unsigned* status) {
+                                                        int N, int K, int G, int split, float tensor_scale,
+                                                        unsigned* status) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int KB = K / 32;
     const int NG = K / G;
@@ -122,8 +128,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 #pragma unroll
         for (int m = 0; m < MR; ++m) acc[c][m][0] = acc[c][m][1] = 0.f;
 
-    // scale row of 32-k block b: b / (G / 32), a shift when G / 32 is a power of two
-    const int gb = G / 32;
+    // scale row of 32-k block b: b / (G / 32), a shift when G / 32 is a power of two (int4; NVFP4
+    // has two scale rows per block, 2b and 2b + 1)
+    const int gb = FP4 ? 1 : G / 32;
     const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
     auto group_of = [&](int b) { return gshift >= 0 ? (b >> gshift) : b / gb; };
 
@@ -135,15 +142,21 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
                    ? ldg_stream(wcol + static_cast<int64_t>(b) * wt)
                    : make_uint4(0u, 0u, 0u, 0u);
     };
-    auto load_s = [&](int b) {
+    auto load_s = [&](int b) -> uint32_t {
+        if (FP4) {
+            const int64_t r = 2 * static_cast<int64_t>(b);
+            if (!in_bounds(s_base + (r + 1) * wt < s_total, status)) return 0u;
+            return static_cast<uint32_t>(ldg_u16(scol + r * wt)) |
+                   (static_cast<uint32_t>(ldg_u16(scol + (r + 1) * wt)) << 16);
+        }
         return in_bounds(s_base + static_cast<int64_t>(group_of(b)) * wt < s_total, status)
-                   ? ldg_u16(scol + static_cast<int64_t>(group_of(b)) * wt)
-                   : static_cast<uint16_t>(0);
+                   ? static_cast<uint32_t>(ldg_u16(scol + static_cast<int64_t>(group_of(b)) * wt))
+                   : 0u;
     };
     int kb = sl.kb_begin + warp;
     for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
         uint4 v[kUnroll];
-        uint16_t sb[kUnroll];
+        uint32_t sb[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int b = kb + kWarps * u;
@@ -153,13 +166,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int b = kb + kWarps * u;
-            gemv_block<MR>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
+            gemv_block<MR, FP4>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
         }
     }
     for (; kb < sl.kb_end; kb += kWarps) {
         const uint4 v = load_w(kb);
-        const uint16_t sb = load_s(kb);
-        gemv_block<MR>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
+        const uint32_t sb = load_s(kb);
+        gemv_block<MR, FP4>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
     }
 
     griddep_launch_dependents();
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) s += red[(w * MR + m) * 32 + l];
             const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
-            if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s));
+            if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s * tensor_scale));
         }
         return;
     }
@@ -195,15 +208,17 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
         for (int p = 0; p < split; ++p) s += ld_dsmem_f1(map_peer(local, p));
         const int m = e / 32, l = e % 32;
         const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
-        if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s));
+        if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s * tensor_scale));
     }
     cluster_sync_all();
 }
 
 template <int MR>
 cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
-                          int N, int K, int G, int split, size_t smem, cudaStream_t s, unsigned* status) {
-    auto kern = gemv_kernel<MR>;
+                          int N, int K, int G, int split, size_t smem, const LaunchCtx& ctx) {
+    const cudaStream_t s = ctx.stream;
+    unsigned* status = ctx.status;
+    auto kern = ctx.nvfp4 ? gemv_kernel<MR, true> : gemv_kernel<MR, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (split > 8) {
@@ -230,7 +245,7 @@ cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const ui
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, x, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, N, K, G, split,
-                              status);
+                              ctx.tensor_scale, status);
 }
 
 }  // namespace
@@ -246,14 +261,14 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint
                         int N, int K, int G, int split, const LaunchCtx& ctx) {
     const size_t smem = gemv_smem_bytes(M, N, K, split);
     switch (M) {
-        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
-        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx.stream, ctx.status);
+        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
         default: return cudaErrorInvalidValue;
     }
 }

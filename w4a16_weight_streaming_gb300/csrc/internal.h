@@ -15,6 +15,10 @@ struct LaunchCtx {
     unsigned* status;     // device address of this device's status word
     uint64_t timeout_ns;  // limit of every bounded wait
     int sm_count;
+    // Weight format: 0 = int4 with offset 8 and fp16 group scales; 1 = NVFP4 (E2M1 codes in the
+    // canonical nibble order, fp16 scales per 16 k converted from E4M3, group passed as 16).
+    int nvfp4 = 0;
+    float tensor_scale = 1.0f;  // multiplies every fp32 sum before the fp16 rounding (1 for int4)
 };
 
 // ---- repack.cu
@@ -22,6 +26,12 @@ cudaError_t launch_repack(const int32_t* qweight, const uint16_t* scales, uint32
                           int N, int K, int G, cudaStream_t s, unsigned* status);
 cudaError_t launch_unrepack(const uint32_t* qweight_r, const uint16_t* scales_r, int32_t* qweight, uint16_t* scales,
                             int N, int K, int G, cudaStream_t s, unsigned* status);
+
+// NVFP4: E2M1 codes keep the canonical nibble order; E4M3 scales [K/16][N] become fp16 of equal value.
+cudaError_t launch_repack_nvfp4(const int32_t* qweight, const uint8_t* scales8, uint32_t* qweight_r, uint16_t* scales_r,
+                                int N, int K, cudaStream_t s, unsigned* status);
+cudaError_t launch_unrepack_nvfp4(const uint32_t* qweight_r, const uint16_t* scales_r, int32_t* qweight,
+                                  uint8_t* scales8, int N, int K, cudaStream_t s, unsigned* status);
 
 // ---- gemv.cu: CUDA-core split-K GEMV, M <= 8.
 constexpr int kGemvMaxM = 8;

@@ -130,11 +130,15 @@ __device__ __forceinline__ bool group_sync_and(int id, int nthreads, bool pred) 
     return r != 0u;
 }
 
-template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW>
+// FP4: NVFP4 weights (E2M1 codes in the canonical nibble order, G = 16 fp16 scales: two scale rows
+// per 32-k block) instead of int4 with offset 8. tensor_scale multiplies every fp32 sum before
+// the fp16 rounding (1 for int4).
+template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW, bool FP4>
 __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
-                   int split, int s_stages, int a_stages, int x_3d, unsigned* status, uint64_t timeout_ns) {
+                   int split, int s_stages, int a_stages, int x_3d, float tensor_scale, unsigned* status,
+                   uint64_t timeout_ns) {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
     static_assert(NA == 1 || NA == 2 || NA == 4, "1, 2 or 4 accumulators");
@@ -348,19 +352,29 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                 const uint32_t sst = sst0 + static_cast<uint32_t>(s) * P.s_stage;
                 uint32_t regs[kPartKB * 16];
                 uint4 v[kPartKB];
-                uint32_t sb[kPartKB];
+                uint32_t sb[kPartKB], sb2[kPartKB];
 #pragma unroll
                 for (int u = 0; u < kPartKB; ++u) {
                     v[u] = lds128(wst + 16u * static_cast<uint32_t>(u * wt));
                     sb[u] = lds16(sst + 2u * static_cast<uint32_t>(srow[u] * wt));
+                    // NVFP4: the block's second 16-k half has the next scale row
+                    sb2[u] = FP4 ? lds16(sst + 2u * static_cast<uint32_t>((srow[u] + 1) * wt)) : sb[u];
                 }
 #pragma unroll
                 for (int u = 0; u < kPartKB; ++u) {
                     const uint32_t s2 = sb[u] | (sb[u] << 16);
-                    dequant8(v[u].x, s2, &regs[u * 16 + 0]);
-                    dequant8(v[u].y, s2, &regs[u * 16 + 4]);
-                    dequant8(v[u].z, s2, &regs[u * 16 + 8]);
-                    dequant8(v[u].w, s2, &regs[u * 16 + 12]);
+                    if (FP4) {
+                        const uint32_t s2b = sb2[u] | (sb2[u] << 16);
+                        dequant8_nvfp4(v[u].x, s2, &regs[u * 16 + 0]);
+                        dequant8_nvfp4(v[u].y, s2, &regs[u * 16 + 4]);
+                        dequant8_nvfp4(v[u].z, s2b, &regs[u * 16 + 8]);
+                        dequant8_nvfp4(v[u].w, s2b, &regs[u * 16 + 12]);
+                    } else {
+                        dequant8(v[u].x, s2, &regs[u * 16 + 0]);
+                        dequant8(v[u].y, s2, &regs[u * 16 + 4]);
+                        dequant8(v[u].z, s2, &regs[u * 16 + 8]);
+                        dequant8(v[u].w, s2, &regs[u * 16 + 12]);
+                    }
                 }
                 tmem_st<kPartKB * 16>(a_base + static_cast<uint32_t>(a * kACols), regs);
                 tmem_wait_st();
@@ -430,7 +444,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                             const int m = m0 + mbase + c + j;
                             if (m < M && in_bounds(static_cast<int64_t>(m) * N + n < static_cast<int64_t>(M) * N, status))
                                 y[static_cast<int64_t>(m) * N + n] =
-                                    __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
+                                    __half_as_ushort(__float2half_rn(__uint_as_float(r[j]) * tensor_scale));
                         }
                     }
                 } else {
@@ -460,6 +474,10 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                 acc.z += v.z;
                 acc.w += v.w;
             }
+            acc.x *= tensor_scale;
+            acc.y *= tensor_scale;
+            acc.z *= tensor_scale;
+            acc.w *= tensor_scale;
             const int e = 4 * e4;
             const int m = m0 + e / kTileN;
             const int c = e % kTileN;
@@ -540,20 +558,21 @@ cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cud
 template <int MT, int KC, int NI, bool GI, int DW>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
                         uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW>;
+    auto kern = ctx.nvfp4 ? tc_gemm_kernel<MT, KC, NI, GI, DW, true> : tc_gemm_kernel<MT, KC, NI, GI, DW, false>;
     const size_t smem = launch_smem(MT, KC, G, c);
     cudaError_t e = prepare_kernel(kern, smem, c.split);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(c, M, N, smem, ctx.stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
-                              c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.status, ctx.timeout_ns);
+                              c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.tensor_scale, ctx.status,
+                              ctx.timeout_ns);
 }
 
 // CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.
 template <int MT, int KC, int NI, bool GI, int DW>
 int resident_ctas_t(const TcConfig& c, int G) {
-    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW>;
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW, false>;  // (the NVFP4 variant has the same resources)
     const size_t smem = launch_smem(MT, KC, G, c);
     if (prepare_kernel(kern, smem, c.split) != cudaSuccess) {
         cudaGetLastError();

@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <cmath>
 #include <mutex>
 #include <string>
 #include <tuple>
@@ -97,6 +98,15 @@ int check_matrix_shape(int N, int K, int G) {
     if (N > (1 << 23) || K > (1 << 22)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     return W4A16_OK;
 }
+
+// NVFP4 weights: the same limits, with the format's fixed block of 16 rows per scale.
+int check_matrix_shape_nvfp4(int N, int K) {
+    if (N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+    if (N % 32 != 0 || K % 64 != 0) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (N > (1 << 23) || K > (1 << 22)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    return W4A16_OK;
+}
+constexpr int kNvfp4Block = 16;
 
 // ----------------------------------------------------------------------------- dispatcher
 struct Choice {
@@ -388,11 +398,12 @@ namespace w4a16 {
 namespace {
 
 // Every argument check of a GEMM on device buffers, then the plan; launches nothing.
+// (nvfp4: NVFP4 weights, group = 16.)
 int prepare_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
-                 int group, const w4a16_plan* plan, DeviceInfo* d, Choice* ch) {
+                 int group, const w4a16_plan* plan, DeviceInfo* d, Choice* ch, bool nvfp4 = false) {
     if (!x || !qweight_r || !scales_r || !y) return W4A16_ERR_INVALID_ARG;
     if (M <= 0) return W4A16_ERR_INVALID_ARG;
-    const int sh = check_matrix_shape(N, K, group);
+    const int sh = nvfp4 ? check_matrix_shape_nvfp4(N, K) : check_matrix_shape(N, K, group);
     if (sh != W4A16_OK) return sh;
     if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(x) || !aligned16(qweight_r) || !aligned16(scales_r) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
@@ -407,29 +418,33 @@ int prepare_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r,
 }
 
 int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M,
-                int N, int K, int group, const DeviceInfo& d, void* stream) {
+                int N, int K, int group, const DeviceInfo& d, void* stream, bool nvfp4 = false,
+                float tensor_scale = 1.0f) {
     LaunchCtx ctx;
     ctx.stream = static_cast<cudaStream_t>(stream);
     ctx.status = d.status;
     ctx.timeout_ns = g_timeout_ns.load();
     ctx.sm_count = d.sm_count;
+    ctx.nvfp4 = nvfp4 ? 1 : 0;
+    ctx.tensor_scale = tensor_scale;
     cudaError_t e;
     char desc[256];
     if (ch.path == W4A16_PATH_GEMV) {
         e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                         group, ch.gemv_split, ctx);
-        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128", M, N, K,
-                 group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32));
+        snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128%s", M, N,
+                 K, group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32),
+                 nvfp4 ? " weights=nvfp4" : "");
     } else {
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
                  "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "dequant_warps=%d split_k=%d grid=(%lld,1,1) tmem_cols=%d smem=%zu",
+                 "dequant_warps=%d split_k=%d grid=(%lld,1,1) tmem_cols=%d smem=%zu%s",
                  M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
                  ch.tc.dequant_warps, ch.tc.split,
                  static_cast<long long>(ch.tc.split) * ((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile),
-                 tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group));
+                 tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), nvfp4 ? " weights=nvfp4" : "");
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -518,12 +533,19 @@ int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
+static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out);
+
 int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     if (!out) return W4A16_ERR_INVALID_ARG;
     if (M <= 0) return W4A16_ERR_INVALID_ARG;
     const int sh = check_matrix_shape(N, K, group);
     if (sh != W4A16_OK) return sh;
     if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    return plan_for_group(M, N, K, group, out);
+}
+
+// The automatic plan of a checked shape (also for NVFP4 weights, group 16).
+static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out) {
     DeviceInfo d;
     const bool dev = device_info(&d);
     const int sms = dev ? d.sm_count : 152;
@@ -584,6 +606,78 @@ int w4a16_gemm_host(const uint16_t* x_host, uint16_t* x_dev, const void* qweight
 int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                int group, void* stream) {
     return w4a16_gemm_ex(x, qweight_r, scales_r, y, M, N, K, group, nullptr, stream);
+}
+
+// ---------------------------------------------------------------------------- NVFP4 weights
+size_t w4a16_repacked_nvfp4_scales_bytes(int N, int K) {
+    if (check_matrix_shape_nvfp4(N, K) != W4A16_OK) return 0;
+    return static_cast<size_t>(K / kNvfp4Block) * N * 2;
+}
+
+static int nvfp4_repack_checks(const void* a, const void* b, const void* c, const void* d, int N, int K,
+                               bool canonical_first) {
+    if (!a || !b || !c || !d) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape_nvfp4(N, K);
+    if (sh != W4A16_OK) return sh;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d)) return W4A16_ERR_MISALIGNED;
+    const size_t qb = static_cast<size_t>(N) * K / 2;
+    const size_t s8 = static_cast<size_t>(K / kNvfp4Block) * N, s16 = 2 * s8;
+    // (a, b) = (qweight, scales) of the source, (c, d) of the destination
+    const size_t sb_src = canonical_first ? s8 : s16, sb_dst = canonical_first ? s16 : s8;
+    if (overlaps(a, qb, c, qb) || overlaps(a, qb, d, sb_dst) || overlaps(b, sb_src, c, qb) ||
+        overlaps(b, sb_src, d, sb_dst) || overlaps(c, qb, d, sb_dst))
+        return W4A16_ERR_INVALID_ARG;
+    if (is_host_pointer(a) || is_host_pointer(b) || is_host_pointer(c) || is_host_pointer(d))
+        return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+int w4a16_repack_nvfp4(const int32_t* qweight, const uint8_t* scales8, void* qweight_r, void* scales_r, int N, int K,
+                       void* stream) {
+    const int rc = nvfp4_repack_checks(qweight, scales8, qweight_r, scales_r, N, K, true);
+    if (rc != W4A16_OK) return rc;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    const cudaError_t e = launch_repack_nvfp4(qweight, scales8, static_cast<uint32_t*>(qweight_r),
+                                              static_cast<uint16_t*>(scales_r), N, K,
+                                              static_cast<cudaStream_t>(stream), d.status);
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_unrepack_nvfp4(const void* qweight_r, const void* scales_r, int32_t* qweight, uint8_t* scales8, int N,
+                         int K, void* stream) {
+    const int rc = nvfp4_repack_checks(qweight_r, scales_r, qweight, scales8, N, K, false);
+    if (rc != W4A16_OK) return rc;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    const cudaError_t e = launch_unrepack_nvfp4(static_cast<const uint32_t*>(qweight_r),
+                                                static_cast<const uint16_t*>(scales_r), qweight, scales8, N, K,
+                                                static_cast<cudaStream_t>(stream), d.status);
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_gemm_nvfp4_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, float tensor_scale,
+                        uint16_t* y, int M, int N, int K, const w4a16_plan* plan, void* stream) {
+    if (!std::isfinite(tensor_scale)) return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    Choice ch;
+    const int rc = prepare_gemm(x, qweight_r, scales_r, y, M, N, K, kNvfp4Block, plan, &d, &ch, true);
+    if (rc != W4A16_OK) return rc;
+    return launch_gemm(ch, x, qweight_r, scales_r, y, M, N, K, kNvfp4Block, d, stream, true, tensor_scale);
+}
+
+int w4a16_gemm_nvfp4(const uint16_t* x, const void* qweight_r, const void* scales_r, float tensor_scale, uint16_t* y,
+                     int M, int N, int K, void* stream) {
+    return w4a16_gemm_nvfp4_ex(x, qweight_r, scales_r, tensor_scale, y, M, N, K, nullptr, stream);
+}
+
+int w4a16_plan_for_nvfp4(int M, int N, int K, w4a16_plan* out) {
+    if (!out) return W4A16_ERR_INVALID_ARG;
+    if (M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape_nvfp4(N, K);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    return plan_for_group(M, N, K, kNvfp4Block, out);
 }
 
 int w4a16_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, void* stream) {
