@@ -15,7 +15,9 @@ bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on t
 stream. L2: every weight matrix exists in R device copies and consecutive uses of one copy are at
 least 4 x L2 bytes of other weights apart, so no launch finds its weights in L2. `e2e` repeats
 steps through w4a16_gemm_host with host buffers (x copied in from pinned host memory, y copied
-back, every GEMM of the step).
+back, every GEMM of the step). Two more objects, outside the timed step: `decode_step_chain` (64
+dense layers in one CUDA graph per decode step, at B = 1 .. 64 streams) and `nvfp4` (the same four
+matrices with NVFP4 weights at M = 1, 16, 256).
 
 --workload picks one of the single configurations instead (decode, verify, batched, head, ...):
 the same line for that configuration. --impl reference times the CPU oracle (fp64, oracle/) on a
@@ -435,6 +437,70 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
                     "with the measured peaks", "rows": out}
 
 
+NVFP4_M = [1, 16, 256]
+
+
+def nvfp4_weight_bytes(K: int, N: int) -> int:
+    """Canonical NVFP4 bytes: 4-bit codes + one E4M3 byte per 16 weights (0.5625 B per weight)."""
+    return K * N // 2 + (K // 16) * N
+
+
+def nvfp4_device_bytes(K: int, N: int) -> int:
+    """What the device layout streams: 4-bit codes + one fp16 scale per 16 weights (0.625 B)."""
+    return K * N // 2 + (K // 16) * N * 2
+
+
+def measure_nvfp4(W, dev, peaks, timed, capture, l2, n_launches=100, keep=None):
+    """The dense-layer matrices with NVFP4 weights at M = 1, 16, 256: per row a CUDA graph of
+    `n_launches` launches cycling over enough repacked copies that they exceed 4 x L2; roofline
+    fraction against the canonical NVFP4 bytes (the device layout's fp16 scales add 0.0625 B per
+    weight, reported as device_gbs)."""
+    import torch
+
+    rows = []
+    for (name, K, N) in inputs.SWEEP_MATRICES:
+        if keep is not None and not any(n == name for (n, _) in keep):
+            continue
+        qw, s8, g = inputs.generate_nvfp4_weights(K, N, seed=inputs.SWEEP_SEED)
+        q = torch.from_numpy(qw).to(dev)
+        sc = torch.from_numpy(s8).to(dev)
+        R = max(2, -(-4 * l2 // nvfp4_device_bytes(K, N)))
+        copies = [W.repack_nvfp4(q, sc) for _ in range(R)]
+        del q, sc
+        for M in NVFP4_M:
+            if keep is not None and (name, M) not in keep:
+                continue
+            x = torch.from_numpy(inputs.generate_x(M, K, seed=1000 + M).view(np.int16)).view(torch.float16).to(dev)
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            W.gemm_nvfp4(x, *copies[0], g, N, K, y=y)
+            plan = W.w4a16_last_dispatch()
+            torch.cuda.synchronize()
+            gr = capture(lambda: [W.gemm_nvfp4(x, *copies[i % R], g, N, K, y=y) for i in range(n_launches)])
+            gr.replay()
+            us = timed(gr.replay) / n_launches * 1e3
+            del gr
+            wb = nvfp4_weight_bytes(K, N)
+            t_mem = (wb + activation_bytes(M, K, N)) / (peaks["hbm_gbs"] * 1e9)
+            t_tc = gemm_flops(M, K, N) / (peaks["bf16_tflops"] * 1e12)
+            rows.append(dict(matrix=name, M=M, K=K, N=N, us=us, weight_gbs=wb / (us * 1e-6) / 1e9,
+                             device_gbs=nvfp4_device_bytes(K, N) / (us * 1e-6) / 1e9,
+                             tflops=gemm_flops(M, K, N) / (us * 1e-6) / 1e12,
+                             roofline_frac=max(t_mem, t_tc) / (us * 1e-6), bound="hbm" if t_mem >= t_tc else "tensor",
+                             plan=plan))
+        del copies
+        torch.cuda.empty_cache()
+    st = W.w4a16_device_status()
+    if st != W.OK:
+        raise RuntimeError(f"device status after the NVFP4 rows: {W.status_string(st)}")
+    layer = {}
+    total = sum(nvfp4_weight_bytes(K, N) for (_, K, N) in inputs.SWEEP_MATRICES)
+    for M in NVFP4_M if keep is None else []:
+        us = sum(r["us"] for r in rows if r["M"] == M)
+        layer[str(M)] = {"us": us, "weight_gbs": total / (us * 1e-6) / 1e9}
+    return {"format": "E2M1 codes, one E4M3 scale per 16 k, fp32 tensor scale; fp16 activations",
+            "bytes_per_weight": 0.5625, "device_bytes_per_weight": 0.625, "layer_step": layer, "rows": rows}
+
+
 # ------------------------------------------------------------------------------ GPU arm
 def percentile(v, q):
     return float(np.percentile(np.asarray(v, dtype=np.float64), q))
@@ -453,6 +519,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--table", action="store_true", help="also print the per-row table to stderr")
     ap.add_argument("--no-chain", action="store_true", help="skip the 64-layer decode-step chain")
+    ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4-weight rows")
+    ap.add_argument("--nvfp4-rows", default=None,
+                    help='NVFP4 rows to run, e.g. "gate_up:16" (M in 1, 16, 256; with --only: profiling)')
     ap.add_argument("--only", default=None, help='sweep rows to run, e.g. "o:16,gate_up:256" (profiling)')
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -690,6 +759,11 @@ def main():
     if args.workload == "sweep" and not args.no_chain and only is None:
         chain = measure_layer_chain(W, dev, {n: m["copies"][0] for n, m in mats.items()}, peaks, timed, capture)
 
+    nvfp4 = None
+    nv_keep = parse_only(args.nvfp4_rows)
+    if args.workload == "sweep" and not args.no_nvfp4 and (only is None or nv_keep is not None):
+        nvfp4 = measure_nvfp4(W, dev, peaks, timed, capture, l2, keep=nv_keep)
+
     if args.table and rank == 0:
         print(f"{'matrix':8s} {'M':>5s} {'us':>9s} {'med':>8s} {'p10':>8s} {'p90':>8s} {'wGB/s':>7s} "
               f"{'TFLOP/s':>8s} {'roof%':>6s} bound  plan", file=sys.stderr)
@@ -698,6 +772,10 @@ def main():
             print(f"{x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} {f(x['us_median'])} {f(x['us_p10'])} "
                   f"{f(x['us_p90'])} {x['weight_gbs']:7.0f} {x['tflops']:8.1f} {100 * x['roofline_frac']:6.1f} "
                   f"{x['bound']:6s} {x['plan']}", file=sys.stderr)
+        if nvfp4:
+            for x in nvfp4["rows"]:
+                print(f"nvfp4 {x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} us {x['weight_gbs']:7.0f} GB/s "
+                      f"{x['tflops']:8.1f} TFLOP/s {100 * x['roofline_frac']:6.1f}% {x['bound']}", file=sys.stderr)
         if chain:
             for c in chain["rows"]:
                 print(f"chain B={c['B']:3d}: {c['us_per_step']:9.1f} us/step {c['tokens_per_s']:9.0f} tok/s "
@@ -725,6 +803,7 @@ def main():
                 "tflops": world * flops_step / (ms_step * 1e-3) / 1e12,
                 "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
                 "layer_step": layer, "rows": rows, "cold_launch_us": cold, "decode_step_chain": chain,
+                "nvfp4": nvfp4,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps * len(items), "clocks": clocks,
                 "peaks": {k: v for k, v in peaks.items()}}
