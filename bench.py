@@ -380,13 +380,15 @@ CHAIN_LAYERS = 64
 CHAIN_B = [1, 8, 16, 32, 64]
 
 
-def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAYERS, reps=5):
+def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAYERS, reps=5, nvfp4_scale=None,
+                        batches=None):
     """The dense layers of one decode step as one CUDA graph: per layer qkv and o from the layer input,
     gate+up from o, silu(gate) * up, down -> the next layer's input (attention itself is not part of
     this path). Every layer streams its own device copy of the four matrices (layers x 170 MB in
     total, far beyond L2). Each B is timed over `reps` graph replays and set against the pages' step
     model t_step(B) = max(W / BW, B * F / P) with W the weight bytes and F = 2 x weights per position
-    (no recurrent state or KV traffic in this path)."""
+    (no recurrent state or KV traffic in this path). nvfp4_scale: the sources are repacked NVFP4
+    weights with that tensor scale (weight bytes counted in the canonical NVFP4 format)."""
     import torch
 
     names = [n for (n, _, _) in inputs.SWEEP_MATRICES]
@@ -394,10 +396,17 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
     copies = {n: [tuple(t.clone() for t in sources[n]) for _ in range(layers)] for n in names}
     hidden = dims["o"][0]
     inter = dims["down"][0]
-    wbytes = layers * sum(weight_bytes(K, N) for (K, N) in dims.values())
+    nv = nvfp4_scale is not None
+    wbytes = layers * sum((nvfp4_weight_bytes(K, N) if nv else weight_bytes(K, N)) for (K, N) in dims.values())
     weights_per_pos = layers * sum(K * N for (K, N) in dims.values())
+    def gemm(x, w, N, K, y):
+        if nv:
+            W.gemm_nvfp4(x, *w, nvfp4_scale, N, K, y=y)
+        else:
+            W.gemm(x, *w, N, K, GROUP, y=y)
+
     out = []
-    for B in CHAIN_B:
+    for B in (batches or CHAIN_B):
         h = [torch.zeros((B, hidden), dtype=torch.float16, device=dev) for _ in range(2)]
         h[0].normal_()
         qkv = torch.empty((B, dims["qkv"][1]), dtype=torch.float16, device=dev)
@@ -408,11 +417,11 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
         def step():
             for li in range(layers):
                 x, y = h[li % 2], h[(li + 1) % 2]
-                W.gemm(x, *copies["qkv"][li], dims["qkv"][1], hidden, GROUP, y=qkv)
-                W.gemm(x, *copies["o"][li], hidden, hidden, GROUP, y=o)
-                W.gemm(o, *copies["gate_up"][li], 2 * inter, hidden, GROUP, y=gu)
+                gemm(x, copies["qkv"][li], dims["qkv"][1], hidden, qkv)
+                gemm(x, copies["o"][li], hidden, hidden, o)
+                gemm(o, copies["gate_up"][li], 2 * inter, hidden, gu)
                 W.silu_mul(gu, act)
-                W.gemm(act, *copies["down"][li], hidden, inter, GROUP, y=y)
+                gemm(act, copies["down"][li], hidden, inter, y)
 
         step()  # plans resolved outside the capture
         torch.cuda.synchronize()
@@ -432,6 +441,7 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
     del copies
     torch.cuda.empty_cache()
     return {"layers": layers, "kernels_per_step": 5 * layers, "weight_bytes_per_step": wbytes,
+            "weights": "NVFP4 (E2M1 + E4M3 per 16 k + fp32 tensor scale)" if nv else "int4, fp16 scales per 128 k",
             "what": "per layer: qkv(h), o(h), gate_up(o), silu(gate)*up, down -> next h; one CUDA graph per step, "
                     "programmatic dependent launch between the kernels; model t_step(B) = max(W/BW, B*2*weights/P) "
                     "with the measured peaks", "rows": out}
@@ -763,6 +773,14 @@ def main():
     nv_keep = parse_only(args.nvfp4_rows)
     if args.workload == "sweep" and not args.no_nvfp4 and (only is None or nv_keep is not None):
         nvfp4 = measure_nvfp4(W, dev, peaks, timed, capture, l2, keep=nv_keep)
+        if nv_keep is None and not args.no_chain:
+            src = {}
+            for (name, K, N) in inputs.SWEEP_MATRICES:
+                qw, s8, g = inputs.generate_nvfp4_weights(K, N, seed=inputs.SWEEP_SEED)
+                src[name] = W.repack_nvfp4(torch.from_numpy(qw).to(dev), torch.from_numpy(s8).to(dev))
+            nvfp4["decode_step_chain"] = measure_layer_chain(W, dev, src, peaks, timed, capture, nvfp4_scale=g)
+            del src
+            torch.cuda.empty_cache()
 
     if args.table and rank == 0:
         print(f"{'matrix':8s} {'M':>5s} {'us':>9s} {'med':>8s} {'p10':>8s} {'p90':>8s} {'wGB/s':>7s} "
@@ -776,6 +794,11 @@ def main():
             for x in nvfp4["rows"]:
                 print(f"nvfp4 {x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} us {x['weight_gbs']:7.0f} GB/s "
                       f"{x['tflops']:8.1f} TFLOP/s {100 * x['roofline_frac']:6.1f}% {x['bound']}", file=sys.stderr)
+        if nvfp4 and nvfp4.get("decode_step_chain"):
+            for c in nvfp4["decode_step_chain"]["rows"]:
+                print(f"nvfp4 chain B={c['B']:3d}: {c['us_per_step']:9.1f} us/step {c['tokens_per_s']:9.0f} tok/s "
+                      f"{c['weight_gbs']:6.0f} GB/s model {c['model_us']:8.1f} us ({100 * c['model_frac']:.1f}%)",
+                      file=sys.stderr)
         if chain:
             for c in chain["rows"]:
                 print(f"chain B={c['B']:3d}: {c['us_per_step']:9.1f} us/step {c['tokens_per_s']:9.0f} tok/s "
