@@ -12,6 +12,9 @@ __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)
 
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ gu, uint4* __restrict__ act, int M,
                                                        int I, unsigned* status) {
+    // The next kernel (the down projection) may start now: its weight copies do not depend on act,
+    // and it waits for this grid to complete before it reads act.
+    griddep_launch_dependents();
     griddep_wait();  // gu is the previous kernel's output
     const int v_per_row = I / 8;
     const int64_t total = static_cast<int64_t>(M) * v_per_row;
@@ -36,7 +39,6 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
         }
         act[v] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
     }
-    griddep_launch_dependents();
 }
 
 }  // namespace
