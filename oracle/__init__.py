@@ -25,6 +25,11 @@ Functions and the passage each follows:
   stream"): E2M1 codes, one E4M3 scale per 16 weights along K, one fp32 tensor scale g, fp16
   activations; y = g * sum_k x * e2m1 * e4m3. The pages print no format: the reading is the
   published NVFP4 definition.
+* ``quantize_x_int8`` / ``gemm_w4a8`` / ``gemm_w4a8_sampled`` -- int8 activations (W4A8: the MLP
+  GEMMs past the bend in "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s", section "Where the line
+  bends"): per-token symmetric int8 (sx = fl32(amax / 127), xq = rne(fl32(x / sx))), and
+  y = sx * sum_g s * sum_{k in g} (q - 8) * xq with exact integer group sums. The pages print no
+  quantisation: the reading is the plainest per-token one.
 * ``half_to_double`` / ``double_to_half`` -- the binary16 codec, written out bit by bit.
 
 Parity status of each function is recorded in the test suite that pins it
@@ -114,6 +119,12 @@ class Oracle:
         for name in ("w4o_repack_nvfp4", "w4o_unrepack_nvfp4"):
             getattr(lib, name).restype = I
             getattr(lib, name).argtypes = [P, P, I, I, P, P]
+        lib.w4o_quantize_x_int8.restype = I
+        lib.w4o_quantize_x_int8.argtypes = [P, I, I, P, P]
+        lib.w4o_gemm_w4a8.restype = I
+        lib.w4o_gemm_w4a8.argtypes = [P, P, P, P, I, I, I, I, P, P, I]
+        lib.w4o_gemm_w4a8_sampled.restype = I
+        lib.w4o_gemm_w4a8_sampled.argtypes = [P, P, P, P, I, I, I, I, P, P, L, P, P]
         lib.w4o_max_threads.restype = I
         lib.w4o_has_openmp.restype = I
         self.lib = lib
@@ -257,6 +268,54 @@ class Oracle:
                                              msa.size, _ptr(y), _ptr(a))
         if rc != 0:
             raise ValueError(f"oracle gemm_nvfp4_sampled rejected the input (rc={rc})")
+        return y, a
+
+    # ---------------------------------------------------------------------------- W4A8
+    def quantize_x_int8(self, x_bits):
+        """(xq int8 [M, K], sx float32 [M]): per-token symmetric int8 quantisation of fp16 x."""
+        x = _c(x_bits, np.uint16)
+        M, K = x.shape
+        xq = np.empty((M, K), np.int8)
+        sx = np.empty(M, np.float32)
+        rc = self.lib.w4o_quantize_x_int8(_ptr(x), M, K, _ptr(xq), _ptr(sx))
+        if rc != 0:
+            raise ValueError(f"oracle quantize_x_int8 rejected the shape (rc={rc})")
+        return xq, sx
+
+    def gemm_w4a8(self, xq, sx, qweight, scales, G: int, nthreads: int | None = None):
+        """(y, absy) float64 [M, N]: y = sx * sum_g s * sum (q - 8) xq; absy = sum_k |sx xq (q - 8) s|."""
+        xa = _c(xq, np.int8)
+        sa = _c(sx, np.float32)
+        qw = _c(qweight, np.int32)
+        sc = _c(scales, np.uint16)
+        M, K = xa.shape
+        N = qw.shape[1]
+        if qw.shape[0] * 8 != K or sc.shape != (K // G, N) or sa.shape != (M,):
+            raise ValueError("xq [M, K], sx [M], qweight [K/8, N], scales [K/G, N] expected")
+        y = np.empty((M, N), np.float64)
+        a = np.empty((M, N), np.float64)
+        rc = self.lib.w4o_gemm_w4a8(_ptr(xa), _ptr(sa), _ptr(qw), _ptr(sc), M, N, K, G, _ptr(y), _ptr(a),
+                                    nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle gemm_w4a8 rejected the shape (rc={rc})")
+        return y, a
+
+    def gemm_w4a8_sampled(self, xq, sx, qweight, scales, G: int, ms, ns):
+        """(y, absy) float64 [count] for the listed (m, n) pairs only."""
+        xa = _c(xq, np.int8)
+        sa = _c(sx, np.float32)
+        qw = _c(qweight, np.int32)
+        sc = _c(scales, np.uint16)
+        msa = _c(ms, np.int64)
+        nsa = _c(ns, np.int64)
+        M, K = xa.shape
+        N = qw.shape[1]
+        y = np.empty(msa.shape, np.float64)
+        a = np.empty(msa.shape, np.float64)
+        rc = self.lib.w4o_gemm_w4a8_sampled(_ptr(xa), _ptr(sa), _ptr(qw), _ptr(sc), M, N, K, G, _ptr(msa),
+                                            _ptr(nsa), msa.size, _ptr(y), _ptr(a))
+        if rc != 0:
+            raise ValueError(f"oracle gemm_w4a8_sampled rejected the input (rc={rc})")
         return y, a
 
     def repack_nvfp4(self, qweight, scales8):
@@ -414,6 +473,18 @@ def repack_nvfp4(qweight, scales8):
 
 def unrepack_nvfp4(wr, sr, K: int, N: int):
     return load().unrepack_nvfp4(wr, sr, K, N)
+
+
+def quantize_x_int8(x_bits):
+    return load().quantize_x_int8(x_bits)
+
+
+def gemm_w4a8(xq, sx, qweight, scales, G: int, nthreads: int | None = None):
+    return load().gemm_w4a8(xq, sx, qweight, scales, G, nthreads)
+
+
+def gemm_w4a8_sampled(xq, sx, qweight, scales, G: int, ms, ns):
+    return load().gemm_w4a8_sampled(xq, sx, qweight, scales, G, ms, ns)
 
 
 # ------------------------------------------------------------------------------------ check

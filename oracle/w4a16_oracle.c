@@ -20,6 +20,7 @@
  *     scales fp16 [K/G][N];
  *     w[k][n] = fp16_rne((q[k][n] - 8) * scales[k/G][n]);
  *     y[m][n] = sum_k x[m][k] * w[k][n], summed here in fp64 in ascending k.
+ *   NVFP4 weights and int8 activations (W4A8): the sections of those names below.
  *
  * The fp16 codec is written out bit by bit (sign, exponent, mantissa, subnormals, overflow to
  * infinity, round-to-nearest-even); no compiler half type is used.
@@ -481,5 +482,125 @@ int w4o_unrepack_nvfp4(const uint32_t* wr, const uint16_t* sr, int K, int N, int
             scales8[(size_t)g * N + n] = (uint8_t)found;
         }
     }
+    return 0;
+}
+
+/* ---------------------------------------------------------------- W4A8: int8 activations
+ *
+ * "Qwen3.8-27B at 764, 1,035 and 1,623 tok/s" (ai.satyajit.si), section "Where the line bends",
+ * runs the MLP GEMMs with int8 activations past the bend (a W4A8 path: 4-bit weights, 8-bit
+ * activations), and the technobrother.ru news page on the same project names INT8 arithmetic;
+ * neither prints the quantisation. Reading taken (the plainest one: per-token symmetric int8; the
+ * weights are the W4A16 weights before their fp16 rounding, i.e. integer codes and group scales as
+ * an integer GEMM consumes them):
+ *
+ *   amax[m]  = max_k |x[m][k]|                  (fp16 -> binary32, exact)
+ *   sx[m]    = fl32(amax[m] / 127)              (one IEEE binary32 division, ties to even)
+ *   xq[m][k] = rne(fl32(x[m][k] / sx[m]))       (binary32 division, then to the nearest integer,
+ *                                                ties to even; clamped to [-127, 127], which the
+ *                                                division never leaves); all 0 when amax[m] = 0
+ *   y[m][n]  = sx[m] * sum_g scales[g][n] * sum_{k in group g} (q[k][n] - 8) * xq[m][k]
+ *
+ * The quantisation is a decision taken in floating point: it is written in binary32 exactly as
+ * above so that any implementation taking the same binary32 steps reaches the same integers. The
+ * group sums are integers, exact here in 64 bits; the rest is fp64.
+ */
+int w4o_quantize_x_int8(const uint16_t* x, int M, int K, int8_t* xq, float* sx) {
+    if (M < 0 || K <= 0) return 1;
+    for (int m = 0; m < M; ++m) {
+        const uint16_t* row = x + (size_t)m * K;
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            float v = fabsf((float)w4o_half_to_double(row[k]));
+            if (v > amax) amax = v;
+        }
+        float s = amax / 127.0f;
+        sx[m] = s;
+        for (int k = 0; k < K; ++k) {
+            int v = 0;
+            if (amax > 0.0f) {
+                float r = (float)w4o_half_to_double(row[k]) / s;
+                float t = nearbyintf(r);
+                if (t > 127.0f) t = 127.0f;
+                if (t < -127.0f) t = -127.0f;
+                v = (int)t;
+            }
+            xq[(size_t)m * K + k] = (int8_t)v;
+        }
+    }
+    return 0;
+}
+
+/* One output column n for the rows listed in ms (count rows): the codes of column n are unpacked
+ * once into qcol (K ints), then per row and group the exact integer sum and its absolute value. */
+static void w4a8_column(const int8_t* xq, const float* sx, const uint16_t* scales, int N, int K, int G,
+                        const int* qcol, int n, int m, double* y, double* absy) {
+    double acc = 0.0, aacc = 0.0;
+    for (int g = 0; g < K / G; ++g) {
+        int64_t isum = 0, iabs = 0;
+        for (int k = g * G; k < (g + 1) * G; ++k) {
+            const int64_t d = (int64_t)(qcol[k] - 8) * (int64_t)xq[(size_t)m * K + k];
+            isum += d;
+            iabs += d < 0 ? -d : d;
+        }
+        const double s = w4o_half_to_double(scales[(size_t)g * (size_t)N + (size_t)n]);
+        acc += s * (double)isum;
+        aacc += fabs(s) * (double)iabs;
+    }
+    const double sxm = (double)sx[m];
+    *y = sxm * acc;
+    *absy = fabs(sxm) * aacc;
+}
+
+/* y[m][n] and absy[m][n] = sum_k |(sx[m] xq[m][k]) (q[k][n] - 8) scales[k/G][n]| (the tolerance
+ * scale, with the dequantised activations and unrounded weights) for every m, n. */
+int w4o_gemm_w4a8(const int8_t* xq, const float* sx, const int32_t* qweight, const uint16_t* scales, int M, int N,
+                  int K, int G, double* y, double* absy, int nthreads) {
+    if (M < 0 || N <= 0 || K <= 0 || G <= 0 || K % G != 0 || K % 8 != 0) return 1;
+    if (nthreads < 1) nthreads = 1;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        int* qcol = (int*)malloc(sizeof(int) * (size_t)K);
+        if (!qcol) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 8)
+#endif
+            for (int n = 0; n < N; ++n) {
+                for (int k = 0; k < K; ++k) qcol[k] = w4o_nibble(qweight, N, k, n);
+                for (int m = 0; m < M; ++m) {
+                    const size_t at = (size_t)m * (size_t)N + (size_t)n;
+                    w4a8_column(xq, sx, scales, N, K, G, qcol, n, m, y + at, absy + at);
+                }
+            }
+            free(qcol);
+        }
+    }
+    return failed ? 2 : 0;
+}
+
+/* The same for a list of (m, n) pairs. */
+int w4o_gemm_w4a8_sampled(const int8_t* xq, const float* sx, const int32_t* qweight, const uint16_t* scales, int M,
+                          int N, int K, int G, const int64_t* ms, const int64_t* ns, int64_t count, double* y,
+                          double* absy) {
+    if (M < 0 || N <= 0 || K <= 0 || G <= 0 || K % G != 0 || K % 8 != 0) return 1;
+    int* qcol = (int*)malloc(sizeof(int) * (size_t)K);
+    if (!qcol) return 2;
+    for (int64_t i = 0; i < count; ++i) {
+        if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N) {
+            free(qcol);
+            return 1;
+        }
+        for (int k = 0; k < K; ++k) qcol[k] = w4o_nibble(qweight, N, k, (int)ns[i]);
+        w4a8_column(xq, sx, scales, N, K, G, qcol, (int)ns[i], (int)ms[i], &y[i], &absy[i]);
+    }
+    free(qcol);
     return 0;
 }

@@ -477,12 +477,133 @@ def pin_nvfp4_repack(o):
     assert np.array_equal(qw2, qw) and np.array_equal(s82, s8)
 
 
+# ------------------------------------------------------------------------------ W4A8 (int8 activations)
+def _quantize_numpy(x16):
+    """The per-token decision restated in numpy binary32 (an implementation independent of the C one)."""
+    xf = x16.astype(np.float32)
+    amax = np.max(np.abs(xf), axis=1).astype(np.float32)
+    sx = (amax / np.float32(127)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (xf / sx[:, None]).astype(np.float32)
+    xq = np.where(amax[:, None] > 0, np.clip(np.rint(r), -127, 127), 0).astype(np.int8)
+    return xq, sx
+
+
+def pin_w4a8_quantize(o):
+    K = 16
+    rows = np.zeros((5, K), np.float32)
+    rows[0, :7] = [127, -127, 5, -6, 0, 64, -1]            # amax 127: sx = 1, xq = x
+    rows[1, :9] = [127, 2.5, 3.5, -2.5, 0.5, -0.5, 1.5, -1.5, 126.5]  # ties go to even
+    # rows[2] stays zero: sx = 0, xq = 0
+    rows[3, :4] = [1016, -8, 24, -1000]                     # amax 127 * 8: sx = 8, xq = x / 8
+    rows[4, :3] = [-100, 50, 20]                            # the largest magnitude is negative
+    x16 = rows.astype(np.float16)
+    xq, sx = o.quantize_x_int8(x16.view(np.uint16))
+    assert sx[0] == 1.0 and np.array_equal(xq[0], rows[0].astype(np.int8))
+    assert np.array_equal(xq[1, :9], [127, 2, 4, -2, 0, 0, 2, -2, 126])
+    assert sx[2] == 0.0 and not xq[2].any()
+    assert sx[3] == 8.0 and np.array_equal(xq[3, :4], [127, -1, 3, -125])
+    assert sx[4] == np.float32(100) / np.float32(127) and xq[4, 0] == -127
+    rng = np.random.default_rng(RNG_SEED + 50)
+    for scale in (1.0, 1e-3, 300.0):
+        x = (rng.standard_normal((6, 320)) * scale).astype(np.float16)
+        x[1] = (rng.standard_cauchy(320) * scale).clip(-60000, 60000).astype(np.float16)  # heavy tails
+        xq, sx = o.quantize_x_int8(x.view(np.uint16))
+        xq_ref, sx_ref = _quantize_numpy(x)
+        assert np.array_equal(sx, sx_ref) and np.array_equal(xq, xq_ref)
+
+
+def _w4a8_case(rng, M, K, N, G):
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    # fp16 scales of both signs and several binades (a signed scale checks |s| in the tolerance sum)
+    sc = (rng.uniform(0.5, 1.0, size=(K // G, N)) * rng.choice([-1.0, 1.0], size=(K // G, N)) *
+          2.0 ** rng.integers(-12, 2, size=(K // G, N))).astype(np.float16)
+    xq = rng.integers(-127, 128, size=(M, K), dtype=np.int64).astype(np.int8)
+    sx = rng.uniform(1e-3, 0.1, size=M).astype(np.float32)
+    return q, sc, xq, sx
+
+
+def pin_w4a8_bruteforce_fraction(o):
+    # y = sx * sum_g s_g * sum_{k in g} (q - 8) xq in exact rationals
+    rng = np.random.default_rng(RNG_SEED + 51)
+    for (M, K, N, G) in [(1, 16, 3, 8), (2, 32, 2, 16), (3, 48, 2, 8)]:
+        q, sc, xq, sx = _w4a8_case(rng, M, K, N, G)
+        qw = inputs.pack_nibbles(q)
+        y, a = o.gemm_w4a8(xq, sx, qw, sc.view(np.uint16), G)
+        for m in range(M):
+            for n in range(N):
+                terms = [Fraction(float(sx[m])) * Fraction(float(sc[k // G, n])) * (int(q[k, n]) - 8) * int(xq[m, k])
+                         for k in range(K)]
+                exact, absx = sum(terms), sum(abs(t) for t in terms)
+                assert abs(Fraction(y[m, n]) - exact) <= Fraction(2) ** -48 * (absx + 1)
+                assert abs(Fraction(a[m, n]) - absx) <= Fraction(2) ** -48 * (absx + 1)
+
+
+def pin_w4a8_matches_w4a16_when_exact(o):
+    # power-of-two scales make (q - 8) * s exact in fp16, and x = j / 8 with max |j| = 127 gives
+    # sx = 1/8 exactly and xq = j: then W4A8 and the (separately pinned) W4A16 oracle compute the same
+    # sum of exact dyadic products and must agree to the last bit
+    rng = np.random.default_rng(RNG_SEED + 52)
+    M, K, N, G = 3, 256, 24, 64
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    sc = (2.0 ** rng.integers(-10, -2, size=(K // G, N)) * rng.choice([-1.0, 1.0], size=(K // G, N))).astype(np.float16)
+    j = rng.integers(-126, 127, size=(M, K))
+    j[:, 5] = 127
+    x = (j / 8.0).astype(np.float16)
+    qw = inputs.pack_nibbles(q)
+    xq, sx = o.quantize_x_int8(x.view(np.uint16))
+    assert np.all(sx == 0.125) and np.array_equal(xq, j.astype(np.int8))
+    y8, a8 = o.gemm_w4a8(xq, sx, qw, sc.view(np.uint16), G)
+    y16, a16 = o.gemm(x.view(np.uint16), qw, sc.view(np.uint16), G)
+    assert np.array_equal(y8, y16) and np.array_equal(a8, a16)
+
+
+def pin_w4a8_one_hot(o):
+    # x = e_k: xq = 127 e_k, sx = fl32(1/127), y = sx * s[k/G] * 127 (q[k] - 8)
+    rng = np.random.default_rng(RNG_SEED + 53)
+    K, N, G = 64, 12, 16
+    q, sc, _, _ = _w4a8_case(rng, 1, K, N, G)
+    qw = inputs.pack_nibbles(q)
+    ks = [0, 15, 16, 17, 47, 63]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    xq, sx = o.quantize_x_int8(x.view(np.uint16))
+    assert np.all(sx == np.float32(1) / np.float32(127))
+    y, _ = o.gemm_w4a8(xq, sx, qw, sc.view(np.uint16), G)
+    for i, k in enumerate(ks):
+        assert xq[i, k] == 127 and np.count_nonzero(xq[i]) == 1
+        for n in range(N):
+            exact = Fraction(float(sx[i])) * Fraction(float(sc[k // G, n])) * 127 * (int(q[k, n]) - 8)
+            assert abs(Fraction(y[i, n]) - exact) <= Fraction(2) ** -51 * abs(exact)
+
+
+def pin_w4a8_zero_sign_linearity_sampled(o):
+    rng = np.random.default_rng(RNG_SEED + 54)
+    M, K, N, G = 4, 128, 20, 32
+    q, sc, xq, sx = _w4a8_case(rng, M, K, N, G)
+    qw = inputs.pack_nibbles(q)
+    s16 = sc.view(np.uint16)
+    y0, _ = o.gemm_w4a8(xq, sx, qw, np.zeros_like(s16), G)
+    assert np.all(y0 == 0.0)
+    y, a = o.gemm_w4a8(xq, sx, qw, s16, G)
+    yn, an = o.gemm_w4a8((-xq.astype(np.int16)).astype(np.int8), sx, qw, s16, G)
+    assert np.array_equal(yn, -y) and np.array_equal(an, a)
+    y2, a2 = o.gemm_w4a8(xq, (2 * sx).astype(np.float32), qw, s16, G)
+    assert np.array_equal(y2, 2 * y) and np.array_equal(a2, 2 * a)
+    ms = np.array([0, 3, 1, 2, 3]); ns = np.array([0, 19, 5, 11, 7])
+    ys, as_ = o.gemm_w4a8_sampled(xq, sx, qw, s16, G, ms, ns)
+    assert np.array_equal(ys, y[ms, ns]) and np.array_equal(as_, a[ms, ns])
+
+
 PINS = [pin_half_decode_all, pin_half_encode, pin_dequant_exhaustive, pin_nibble_order, pin_pack_roundtrip,
         pin_bruteforce_fraction, pin_exact_dyadic, pin_one_hot, pin_all_ones, pin_zero_scales,
         pin_constant_weights, pin_linearity, pin_sampled_matches_full, pin_threads_deterministic,
         pin_repack_positions, pin_repack_roundtrip, pin_silu_identity, pin_silu_against_library, pin_silu_limits,
         pin_e2m1_table, pin_e4m3_all_patterns, pin_nvfp4_bruteforce_fraction, pin_nvfp4_one_hot,
-        pin_nvfp4_zero_scales_sign_and_tensor_scale, pin_nvfp4_dequant_and_sampled, pin_nvfp4_repack]
+        pin_nvfp4_zero_scales_sign_and_tensor_scale, pin_nvfp4_dequant_and_sampled, pin_nvfp4_repack,
+        pin_w4a8_quantize, pin_w4a8_bruteforce_fraction, pin_w4a8_matches_w4a16_when_exact, pin_w4a8_one_hot,
+        pin_w4a8_zero_sign_linearity_sampled]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -521,6 +642,14 @@ MUTANTS = {
     "nvfp4_tensor_scale_dropped": ("y[(size_t)m * N + n] = g * s;", "y[(size_t)m * N + n] = s;"),
     "nvfp4_repack_permuted": ("wr[weight_word_index(K, N, k, n)] |= q << (4 * (k % 8));",
                               "wr[weight_word_index(K, N, k, n)] |= q << (4 * kPosOfJ[k % 8]);"),
+    "w4a8_offset_7": ("(int64_t)(qcol[k] - 8)", "(int64_t)(qcol[k] - 7)"),
+    "w4a8_ties_away_from_zero": ("float t = nearbyintf(r);", "float t = roundf(r);"),
+    "w4a8_scale_over_128": ("float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    "w4a8_amax_signed": ("float v = fabsf((float)w4o_half_to_double(row[k]));",
+                         "float v = (float)w4o_half_to_double(row[k]);"),
+    "w4a8_group_index": ("scales[(size_t)g * (size_t)N + (size_t)n]", "scales[(size_t)(g / 2) * (size_t)N + (size_t)n]"),
+    "w4a8_sx_dropped": ("*y = sxm * acc;", "*y = acc;"),
+    "w4a8_signed_scale_in_abs": ("aacc += fabs(s) * (double)iabs;", "aacc += s * (double)iabs;"),
 }
 
 
