@@ -220,6 +220,45 @@ int w4a16_gemm_nvfp4_ex(const uint16_t* x, const void* qweight_r, const void* sc
 /* The automatic plan of w4a16_gemm_nvfp4 for this shape (host only). */
 int w4a16_plan_for_nvfp4(int M, int N, int K, w4a16_plan* out);
 
+/*
+ * W4A8: int8 activations with the int4 weights of w4a16_repack ("Qwen3.8-27B at 764, 1,035 and
+ * 1,623 tok/s" (ai.satyajit.si), section "Where the line bends": the MLP GEMMs run with int8
+ * activations past the bend; the pages print no quantisation, so the reading is per-token
+ * symmetric int8):
+ *   sx[m]    = fl32(max_k |x[m][k]| / 127)               IEEE binary32 division, ties to even
+ *   xq[m][k] = rne(fl32(x[m][k] / sx[m])), in [-127, 127]; 0 for every k when the row is all 0
+ *   y[m][n]  = fp16_rne(sx[m] * sum_g s[g][n] * sum_{k in g} (q[k][n] - 8) * xq[m][k])
+ * The group sums are exact integers (int32 dp4a in the GEMV for M <= 8); the tensor-core tiles
+ * (M > 8) multiply the fp16 copy of xq (exact) by the fp16 W4A16 weights fp16_rne((q - 8) s) and
+ * scale row m by sx[m] at the end. Acceptance bound per element: |y - y_ref| <= 2^-10 |y_ref| +
+ * 2^-10 sum_k |sx xq (q - 8) s| (the weights' fp16 rounding on the tile path is within it). sm_103a
+ * has no int8 tensor-core MMA, so W4A8 is not a faster tensor path on this GPU; its int8 arithmetic
+ * pays in the CUDA-core GEMV.
+ */
+
+/* Per-token symmetric int8 quantisation of x (fp16 [M][K], device): writes xq (int8 [M][K]),
+ * optionally xq_f16 (fp16 [M][K], the same integers; NULL to skip; the tensor-core path of
+ * w4a16_gemm_w4a8 needs it) and sx (fp32 [M]). x must be finite. K % 8 == 0, M <= 2^20,
+ * K <= 2^22. x, xq, xq_f16 16-byte aligned, sx 4-byte aligned, device pointers, no overlaps.
+ * Asynchronous on `stream` (with programmatic dependent launch). Errors: INVALID_ARG, MISALIGNED,
+ * UNSUPPORTED_SHAPE, CUDA. */
+int w4a16_quantize_x_int8(const uint16_t* x, int8_t* xq, uint16_t* xq_f16, float* sx, int M, int K, void* stream);
+
+/* y[M,N] (fp16, device) for int8 activations (xq, xq_f16, sx as written by w4a16_quantize_x_int8)
+ * and repacked int4 weights (w4a16_repack, group `group`). The automatic plan takes the integer
+ * GEMV for M <= 8 and the tensor-core tiles otherwise; xq_f16 may be NULL when the plan is the
+ * GEMV (W4A16_ERR_INVALID_ARG if the tiles would need it). Shapes and errors as w4a16_gemm. */
+int w4a16_gemm_w4a8(const int8_t* xq, const uint16_t* xq_f16, const float* sx, const void* qweight_r,
+                    const void* scales_r, uint16_t* y, int M, int N, int K, int group, void* stream);
+
+/* As w4a16_gemm_w4a8 with an explicit plan (the fields of w4a16_gemm_ex). */
+int w4a16_gemm_w4a8_ex(const int8_t* xq, const uint16_t* xq_f16, const float* sx, const void* qweight_r,
+                       const void* scales_r, uint16_t* y, int M, int N, int K, int group, const w4a16_plan* plan,
+                       void* stream);
+
+/* The automatic plan of w4a16_gemm_w4a8 for this shape (host only). */
+int w4a16_plan_for_w4a8(int M, int N, int K, int group, w4a16_plan* out);
+
 /* Describes the last GEMM this process launched (path, tile, split, grid) into buf (NUL
  * terminated, truncated to len). Host only. Returns W4A16_OK or INVALID_ARG. */
 int w4a16_last_dispatch(char* buf, size_t len);

@@ -234,3 +234,32 @@ def test_nvfp4_host_checks(W):
     assert W.w4a16_plan_for_nvfp4(1, 5120, 5120).path == W.PATH_GEMV
     with pytest.raises(W.W4A16Error):
         W.w4a16_plan_for_nvfp4(9, 5120, 5120 + 64)  # K % 128 != 0 needs the GEMV, which takes M <= 8
+
+
+def test_w4a8_host_checks(W):
+    # argument checks of the int8-activation entry points, before any device work
+    q = W.w4a16_quantize_x_int8
+    assert q(0, FAKE, None, FAKE * 2, 4, 1024, None) == 1            # null x
+    assert q(FAKE, FAKE * 2, None, 0, 4, 1024, None) == 1            # null sx
+    assert q(FAKE, FAKE * 2, None, FAKE * 3, 0, 1024, None) == 1     # M = 0
+    assert q(FAKE, FAKE * 2, None, FAKE * 3, 4, 1001, None) == 2     # K % 8
+    assert q(FAKE + 2, FAKE * 2, None, FAKE * 3, 4, 1024, None) == 3  # x misaligned
+    assert q(FAKE, FAKE * 2, FAKE * 4 + 8, FAKE * 3, 4, 1024, None) == 3  # xq_f16 misaligned
+    assert q(FAKE, FAKE * 2, None, FAKE * 3 + 2, 4, 1024, None) == 3  # sx not 4-byte aligned
+    assert q(FAKE, FAKE + 4096, None, FAKE * 3, 4, 1024, None) == 1   # xq overlaps x (8 KB)
+    g = W.w4a16_gemm_w4a8
+    assert g(0, None, FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 1
+    assert g(FAKE, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE * 4, 0, 1024, 1024, 128, None) == 1
+    assert g(FAKE, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1000, 1024, 128, None) == 2
+    assert g(FAKE + 8, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 3
+    assert g(FAKE, None, FAKE * 5 + 1, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 3
+    assert g(FAKE, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE + 64, 1, 1024, 1024, 128, None) == 1  # y overlaps xq
+    # the automatic plan: the integer GEMV for every M <= 8, the tiles above
+    for M in (1, 2, 5, 8):
+        assert W.w4a16_plan_for_w4a8(M, 5120, 5120).path == W.PATH_GEMV
+        assert W.w4a16_plan_for_w4a8(M, 34816, 5120).path == W.PATH_GEMV
+    p = W.w4a16_plan_for_w4a8(9, 5120, 5120)
+    assert p.path == W.PATH_TC and p.m_tile == 16
+    assert W.w4a16_plan_for_w4a8(256, 34816, 5120).m_tile == 256
+    with pytest.raises(W.W4A16Error):
+        W.w4a16_plan_for_w4a8(9, 5120, 5120 + 64)  # K % 128 != 0: the tiles cannot, the GEMV takes M <= 8

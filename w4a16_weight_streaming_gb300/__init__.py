@@ -39,6 +39,7 @@ EXPORTED = [
     "w4a16_device_status", "w4a16_set_wait_timeout_ns", "w4a16_selftest_wait_timeout", "w4a16_gemm_host",
     "w4a16_silu_mul", "w4a16_debug_bounds", "w4a16_repacked_nvfp4_scales_bytes", "w4a16_repack_nvfp4",
     "w4a16_unrepack_nvfp4", "w4a16_gemm_nvfp4", "w4a16_gemm_nvfp4_ex", "w4a16_plan_for_nvfp4",
+    "w4a16_quantize_x_int8", "w4a16_gemm_w4a8", "w4a16_gemm_w4a8_ex", "w4a16_plan_for_w4a8",
 ]
 
 
@@ -105,6 +106,14 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4a16_gemm_nvfp4_ex.argtypes = [P, P, P, F, P, I, I, I, ctypes.POINTER(Plan), P]
     lib.w4a16_plan_for_nvfp4.restype = I
     lib.w4a16_plan_for_nvfp4.argtypes = [I, I, I, ctypes.POINTER(Plan)]
+    lib.w4a16_quantize_x_int8.restype = I
+    lib.w4a16_quantize_x_int8.argtypes = [P, P, P, P, I, I, P]
+    lib.w4a16_gemm_w4a8.restype = I
+    lib.w4a16_gemm_w4a8.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
+    lib.w4a16_gemm_w4a8_ex.restype = I
+    lib.w4a16_gemm_w4a8_ex.argtypes = [P, P, P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
+    lib.w4a16_plan_for_w4a8.restype = I
+    lib.w4a16_plan_for_w4a8.argtypes = [I, I, I, I, ctypes.POINTER(Plan)]
     return lib
 
 
@@ -247,6 +256,29 @@ def repack(qweight: torch.Tensor, scales: torch.Tensor, group: int = 128, stream
     return qw_r, sc_r
 
 
+def w4a16_quantize_x_int8(x: int, xq: int, xq_f16: int | None, sx: int, M: int, K: int, stream: int | None) -> int:
+    return lib.w4a16_quantize_x_int8(x, xq, xq_f16, sx, M, K, stream)
+
+
+def w4a16_gemm_w4a8(xq: int, xq_f16: int | None, sx: int, qweight_r: int, scales_r: int, y: int, M: int, N: int,
+                    K: int, group: int, stream: int | None) -> int:
+    return lib.w4a16_gemm_w4a8(xq, xq_f16, sx, qweight_r, scales_r, y, M, N, K, group, stream)
+
+
+def w4a16_gemm_w4a8_ex(xq: int, xq_f16: int | None, sx: int, qweight_r: int, scales_r: int, y: int, M: int, N: int,
+                       K: int, group: int, plan: Plan | None, stream: int | None) -> int:
+    return lib.w4a16_gemm_w4a8_ex(xq, xq_f16, sx, qweight_r, scales_r, y, M, N, K, group,
+                                  ctypes.byref(plan) if plan is not None else None, stream)
+
+
+def w4a16_plan_for_w4a8(M: int, N: int, K: int, group: int = 128) -> Plan:
+    p = Plan()
+    rc = lib.w4a16_plan_for_w4a8(M, N, K, group, ctypes.byref(p))
+    if rc != OK:
+        raise W4A16Error(rc, "w4a16_plan_for_w4a8")
+    return p
+
+
 def gemm_host(x_host: torch.Tensor, x_dev: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor,
               y_dev: torch.Tensor, y_host: torch.Tensor, N: int, K: int, group: int = 128, stream=None) -> None:
     """w4a16_gemm_host on tensors: x_host / y_host fp16 on the CPU (pinned), x_dev / y_dev on cuda.
@@ -317,4 +349,35 @@ def gemm_nvfp4(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor,
         plan = Plan(**plan)
     _check(w4a16_gemm_nvfp4_ex(x.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), float(tensor_scale),
                                y.data_ptr(), M, N, K, plan, _stream_handle(stream)), "w4a16_gemm_nvfp4")
+    return y
+
+
+# ------------------------------------------------------------------------------ W4A8 (int8 activations)
+def quantize_x_int8(x: torch.Tensor, with_f16: bool = True, out=None, stream=None):
+    """Per-token symmetric int8 quantisation of x (float16 [M, K], CUDA) through w4a16_quantize_x_int8:
+    (xq int8 [M, K], xq_f16 float16 [M, K] holding the same integers or None, sx float32 [M])."""
+    M, K = x.shape
+    if out is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+        xh = torch.empty((M, K), dtype=torch.float16, device=x.device) if with_f16 else None
+        sx = torch.empty(M, dtype=torch.float32, device=x.device)
+    else:
+        xq, xh, sx = out
+    _check(w4a16_quantize_x_int8(x.data_ptr(), xq.data_ptr(), xh.data_ptr() if xh is not None else None,
+                                 sx.data_ptr(), M, K, _stream_handle(stream)), "w4a16_quantize_x_int8")
+    return xq, xh, sx
+
+
+def gemm_w4a8(xq: torch.Tensor, xq_f16: torch.Tensor | None, sx: torch.Tensor, qweight_r: torch.Tensor,
+              scales_r: torch.Tensor, N: int, K: int, group: int = 128, y: torch.Tensor | None = None,
+              plan: Plan | dict | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] (float16) for int8 activations (from quantize_x_int8) and repacked int4 weights."""
+    M = xq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=xq.device)
+    if isinstance(plan, dict):
+        plan = Plan(**plan)
+    _check(w4a16_gemm_w4a8_ex(xq.data_ptr(), xq_f16.data_ptr() if xq_f16 is not None else None, sx.data_ptr(),
+                              qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K, group, plan,
+                              _stream_handle(stream)), "w4a16_gemm_w4a8")
     return y

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(PKG, "libw4a16.so")
 # the same library with every kernel's index checks compiled in (W4A16_DEBUG_BOUNDS)
 DEBUG_LIB_PATH = os.path.join(PKG, "libw4a16_debug.so")
 
-SOURCES = ["w4a16_api.cu", "repack.cu", "gemv.cu", "tc_gemm.cu", "act.cu"]
+SOURCES = ["w4a16_api.cu", "repack.cu", "gemv.cu", "tc_gemm.cu", "act.cu", "w4a8.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "internal.h"), os.path.join(INCLUDE, "w4a16.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

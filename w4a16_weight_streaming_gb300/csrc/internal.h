@@ -19,6 +19,9 @@ struct LaunchCtx {
     // canonical nibble order, fp16 scales per 16 k converted from E4M3, group passed as 16).
     int nvfp4 = 0;
     float tensor_scale = 1.0f;  // multiplies every fp32 sum before the fp16 rounding (1 for int4)
+    // Tile kernel only: when not null, the sums of output row m are then multiplied by row_scale[m]
+    // (the per-token scale of int8 activations, W4A8).
+    const float* row_scale = nullptr;
 };
 
 // ---- repack.cu
@@ -62,6 +65,16 @@ int tc_tmem_cols(const TcConfig& c);
 int tc_resident_ctas(const TcConfig& c, int G);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
                       int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx);
+
+// ---- w4a8.cu: int8 activations (W4A8).
+// Per-token symmetric quantisation: sx[m] = amax / 127, xq = rne(x / sx) (binary32), optionally
+// also written as fp16 integers (xq_f16 may be null).
+cudaError_t launch_quantize_x_int8(const uint16_t* x, int8_t* xq, uint16_t* xq_f16, float* sx, int M, int K,
+                                   cudaStream_t s, unsigned* status);
+// Integer (dp4a) split-K GEMV, M <= 8: y = fp16(sx[m] * sum_blocks s * sum (q - 8) xq).
+size_t gemv_w4a8_smem_bytes(int M, int K, int split);
+cudaError_t launch_gemv_w4a8(const int8_t* xq, const float* sx, const uint32_t* qweight_r, const uint16_t* scales_r,
+                             uint16_t* y, int M, int N, int K, int G, int split, const LaunchCtx& ctx);
 
 // ---- act.cu: SwiGLU activation of a fused gate+up output, act = silu(gate) * up.
 cudaError_t launch_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, int sm_count, cudaStream_t s,

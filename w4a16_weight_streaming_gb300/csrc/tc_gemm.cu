@@ -132,13 +132,14 @@ __device__ __forceinline__ bool group_sync_and(int id, int nthreads, bool pred) 
 
 // FP4: NVFP4 weights (E2M1 codes in the canonical nibble order, G = 16 fp16 scales: two scale rows
 // per 32-k block) instead of int4 with offset 8. tensor_scale multiplies every fp32 sum before
-// the fp16 rounding (1 for int4).
+// the fp16 rounding (1 for int4); row_scale, when not null, then multiplies the sums of output row
+// m by row_scale[m] (the int8 activations' per-token scale).
 template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW, bool FP4>
 __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
-                   int split, int s_stages, int a_stages, int x_3d, float tensor_scale, unsigned* status,
-                   uint64_t timeout_ns) {
+                   int split, int s_stages, int a_stages, int x_3d, float tensor_scale,
+                   const float* __restrict__ row_scale, unsigned* status, uint64_t timeout_ns) {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
     static_assert(NA == 1 || NA == 2 || NA == 4, "1, 2 or 4 accumulators");
@@ -442,9 +443,11 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
 #pragma unroll
                         for (int j = 0; j < kCols; ++j) {
                             const int m = m0 + mbase + c + j;
-                            if (m < M && in_bounds(static_cast<int64_t>(m) * N + n < static_cast<int64_t>(M) * N, status))
-                                y[static_cast<int64_t>(m) * N + n] =
-                                    __half_as_ushort(__float2half_rn(__uint_as_float(r[j]) * tensor_scale));
+                            if (m < M && in_bounds(static_cast<int64_t>(m) * N + n < static_cast<int64_t>(M) * N, status)) {
+                                float v = __uint_as_float(r[j]) * tensor_scale;
+                                if (row_scale != nullptr) v *= row_scale[m];
+                                y[static_cast<int64_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
+                            }
                         }
                     }
                 } else {
@@ -483,6 +486,13 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
             const int c = e % kTileN;
             if (m < M && c < wt &&
                 in_bounds(static_cast<int64_t>(m) * N + n0 + c + 4 <= static_cast<int64_t>(M) * N, status)) {
+                if (row_scale != nullptr) {
+                    const float rs = row_scale[m];
+                    acc.x *= rs;
+                    acc.y *= rs;
+                    acc.z *= rs;
+                    acc.w *= rs;
+                }
                 const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
                                     (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
                 const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |
@@ -565,8 +575,8 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(c, M, N, smem, ctx.stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
-                              c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.tensor_scale, ctx.status,
-                              ctx.timeout_ns);
+                              c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.tensor_scale, ctx.row_scale,
+                              ctx.status, ctx.timeout_ns);
 }
 
 // CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.

@@ -211,11 +211,11 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) 
 }
 
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
-                          Choice* out);
+                          Choice* out, bool w4a8);
 
-// Automatic plans are resolved once per (device, M, N, K, group) and cached: the resolution queries
-// the driver's cluster occupancy for every candidate split.
-std::map<std::tuple<int, int, int, int, int>, Choice> g_plan_cache;
+// Automatic plans are resolved once per (device, M, N, K, group, activation type) and cached: the
+// resolution queries the driver's cluster occupancy for every candidate split.
+std::map<std::tuple<int, int, int, int, int, int>, Choice> g_plan_cache;
 
 // W4A16_PLAN: an override of every automatic plan, read once per process. Its value is
 // "field=value[,field=value...]" with the w4a16_plan field names, e.g. "path=2,m_tile=64,split_k=3",
@@ -265,7 +265,9 @@ const EnvPlan& env_plan() {
     return e;
 }
 
-int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, Choice* out) {
+// (w4a8: int8 activations; the GEMV path is then the integer GEMV of w4a8.cu.)
+int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device, Choice* out,
+                 bool w4a8 = false) {
     bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
                                          plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
                                          plan->mma_issuers == 0 && plan->clusters == 0 && plan->dequant_warps == 0);
@@ -274,10 +276,10 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
         plan = &env_plan().plan;
         automatic = false;
     }
-    if (!automatic || !have_device) return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
+    if (!automatic || !have_device) return resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out, w4a8);
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, M, N, K, G);
+    const auto key = std::make_tuple(dev, M, N, K, G, w4a8 ? 1 : 0);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_plan_cache.find(key);
@@ -286,7 +288,7 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
             return W4A16_OK;
         }
     }
-    const int rc = resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out);
+    const int rc = resolve_plan_uncached(M, N, K, G, plan, sm_count, have_device, out, w4a8);
     if (rc == W4A16_OK) {
         std::lock_guard<std::mutex> lock(g_mu);
         if (g_plan_cache.size() < 4096) g_plan_cache[key] = *out;
@@ -295,12 +297,18 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
 }
 
 int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, int sm_count, bool have_device,
-                          Choice* out) {
+                          Choice* out, bool w4a8) {
     w4a16_plan p = {};
     if (plan) p = *plan;
     if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
-    if (path == W4A16_PATH_AUTO) {
+    if (path == W4A16_PATH_AUTO && w4a8) {
+        // int8 activations: the integer GEMV takes every M it supports (its arithmetic per weight
+        // is a fraction of the fp16 path's); the tiles need whole 128-k stages.
+        const bool tc_ok = K % 128 == 0 && group_fits(128, G);
+        path = M <= kGemvMaxM ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+        if (path == W4A16_PATH_GEMV && tc_ok && gemv_w4a8_smem_bytes(M, K, 16) > kGemvMaxSmem) path = W4A16_PATH_TC;
+    } else if (path == W4A16_PATH_AUTO) {
         // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one
         // activation row; from 3 rows on the tcgen05 tiles.
         // At two rows the GEMV wins only on the smaller matrices (5120 x 5120, 5120 x 7168); on
@@ -321,7 +329,8 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
         int split = p.split_k > 0 ? p.split_k : gemv_pick_split(M, N, K, sm_count);
         if (split < 1 || split > 16 || split > K / 32) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        if (gemv_smem_bytes(M, N, K, split) > kGemvMaxSmem) return W4A16_ERR_UNSUPPORTED_SHAPE;
+        const size_t smem = w4a8 ? gemv_w4a8_smem_bytes(M, K, split) : gemv_smem_bytes(M, N, K, split);
+        if (smem > kGemvMaxSmem) return W4A16_ERR_UNSUPPORTED_SHAPE;
         out->gemv_split = split;
         return W4A16_OK;
     }
@@ -417,9 +426,11 @@ int prepare_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r,
     return resolve_plan(M, N, K, group, plan, d->sm_count, true, ch);
 }
 
+// W4A8 (sx not null): x is the fp16 copy of the int8 activations (tile path), xq the int8 ones
+// (GEMV path) and sx their per-token scales.
 int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M,
                 int N, int K, int group, const DeviceInfo& d, void* stream, bool nvfp4 = false,
-                float tensor_scale = 1.0f) {
+                float tensor_scale = 1.0f, const int8_t* xq = nullptr, const float* sx = nullptr) {
     LaunchCtx ctx;
     ctx.stream = static_cast<cudaStream_t>(stream);
     ctx.status = d.status;
@@ -427,14 +438,19 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
     ctx.sm_count = d.sm_count;
     ctx.nvfp4 = nvfp4 ? 1 : 0;
     ctx.tensor_scale = tensor_scale;
+    ctx.row_scale = sx;
+    const char* fmt = nvfp4 ? " weights=nvfp4" : sx != nullptr ? " activations=int8" : "";
     cudaError_t e;
     char desc[256];
     if (ch.path == W4A16_PATH_GEMV) {
-        e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
-                        group, ch.gemv_split, ctx);
+        if (sx != nullptr)
+            e = launch_gemv_w4a8(xq, sx, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r),
+                                 y, M, N, K, group, ch.gemv_split, ctx);
+        else
+            e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
+                            K, group, ch.gemv_split, ctx);
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128%s", M, N,
-                 K, group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32),
-                 nvfp4 ? " weights=nvfp4" : "");
+                 K, group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32), fmt);
     } else {
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
@@ -444,7 +460,7 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
                  M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
                  ch.tc.dequant_warps, ch.tc.split,
                  static_cast<long long>(ch.tc.split) * ((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile),
-                 tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), nvfp4 ? " weights=nvfp4" : "");
+                 tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), fmt);
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -533,7 +549,7 @@ int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
-static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out);
+static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out, bool w4a8 = false);
 
 int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     if (!out) return W4A16_ERR_INVALID_ARG;
@@ -544,13 +560,13 @@ int w4a16_plan_for(int M, int N, int K, int group, w4a16_plan* out) {
     return plan_for_group(M, N, K, group, out);
 }
 
-// The automatic plan of a checked shape (also for NVFP4 weights, group 16).
-static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out) {
+// The automatic plan of a checked shape (also for NVFP4 weights, group 16; w4a8: int8 activations).
+static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out, bool w4a8) {
     DeviceInfo d;
     const bool dev = device_info(&d);
     const int sms = dev ? d.sm_count : 152;
     Choice ch;
-    const int rc = resolve_plan(M, N, K, group, nullptr, sms, dev, &ch);
+    const int rc = resolve_plan(M, N, K, group, nullptr, sms, dev, &ch, w4a8);
     if (rc != W4A16_OK) return rc;
     out->path = ch.path;
     out->clusters = 0;
@@ -678,6 +694,69 @@ int w4a16_plan_for_nvfp4(int M, int N, int K, w4a16_plan* out) {
     if (sh != W4A16_OK) return sh;
     if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     return plan_for_group(M, N, K, kNvfp4Block, out);
+}
+
+// ---------------------------------------------------------------------------- W4A8 (int8 activations)
+int w4a16_quantize_x_int8(const uint16_t* x, int8_t* xq, uint16_t* xq_f16, float* sx, int M, int K, void* stream) {
+    if (!x || !xq || !sx || M <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+    if (K % 8 != 0 || M > (1 << 20) || K > (1 << 22)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(xq) || (xq_f16 && !aligned16(xq_f16)) || (reinterpret_cast<uintptr_t>(sx) & 3u))
+        return W4A16_ERR_MISALIGNED;
+    const size_t xb = static_cast<size_t>(M) * K * 2, qb = static_cast<size_t>(M) * K, sb = static_cast<size_t>(M) * 4;
+    if (overlaps(x, xb, xq, qb) || overlaps(x, xb, sx, sb) || overlaps(xq, qb, sx, sb) ||
+        (xq_f16 && (overlaps(xq_f16, xb, x, xb) || overlaps(xq_f16, xb, xq, qb) || overlaps(xq_f16, xb, sx, sb))))
+        return W4A16_ERR_INVALID_ARG;
+    if (is_host_pointer(x) || is_host_pointer(xq) || is_host_pointer(sx) || (xq_f16 && is_host_pointer(xq_f16)))
+        return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    if (launch_quantize_x_int8(x, xq, xq_f16, sx, M, K, static_cast<cudaStream_t>(stream), d.status) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+}
+
+int w4a16_gemm_w4a8_ex(const int8_t* xq, const uint16_t* xq_f16, const float* sx, const void* qweight_r,
+                       const void* scales_r, uint16_t* y, int M, int N, int K, int group, const w4a16_plan* plan,
+                       void* stream) {
+    if (!xq || !sx || !qweight_r || !scales_r || !y || M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(xq) || (xq_f16 && !aligned16(xq_f16)) || (reinterpret_cast<uintptr_t>(sx) & 3u) ||
+        !aligned16(qweight_r) || !aligned16(scales_r) || !aligned16(y))
+        return W4A16_ERR_MISALIGNED;
+    const size_t qxb = static_cast<size_t>(M) * K, hb = qxb * 2, sb = static_cast<size_t>(M) * 4;
+    const size_t yb = static_cast<size_t>(M) * N * 2, wb = static_cast<size_t>(N) * K / 2;
+    const size_t scb = static_cast<size_t>(K / group) * N * 2;
+    if (overlaps(xq, qxb, y, yb) || (xq_f16 && overlaps(xq_f16, hb, y, yb)) || overlaps(sx, sb, y, yb) ||
+        overlaps(qweight_r, wb, y, yb) || overlaps(scales_r, scb, y, yb))
+        return W4A16_ERR_INVALID_ARG;
+    if (is_host_pointer(xq) || (xq_f16 && is_host_pointer(xq_f16)) || is_host_pointer(sx) ||
+        is_host_pointer(qweight_r) || is_host_pointer(scales_r) || is_host_pointer(y))
+        return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    Choice ch;
+    const int rc = resolve_plan(M, N, K, group, plan, d.sm_count, true, &ch, true);
+    if (rc != W4A16_OK) return rc;
+    if (ch.path == W4A16_PATH_TC && xq_f16 == nullptr) return W4A16_ERR_INVALID_ARG;  // the tiles read fp16
+    return launch_gemm(ch, xq_f16, qweight_r, scales_r, y, M, N, K, group, d, stream, false, 1.0f, xq, sx);
+}
+
+int w4a16_gemm_w4a8(const int8_t* xq, const uint16_t* xq_f16, const float* sx, const void* qweight_r,
+                    const void* scales_r, uint16_t* y, int M, int N, int K, int group, void* stream) {
+    return w4a16_gemm_w4a8_ex(xq, xq_f16, sx, qweight_r, scales_r, y, M, N, K, group, nullptr, stream);
+}
+
+int w4a16_plan_for_w4a8(int M, int N, int K, int group, w4a16_plan* out) {
+    if (!out) return W4A16_ERR_INVALID_ARG;
+    if (M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    return plan_for_group(M, N, K, group, out, true);
 }
 
 int w4a16_silu_mul(const uint16_t* gu, uint16_t* act, int M, int I, void* stream) {
