@@ -15,9 +15,11 @@ bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on t
 stream. L2: every weight matrix exists in R device copies and consecutive uses of one copy are at
 least 4 x L2 bytes of other weights apart, so no launch finds its weights in L2. `e2e` repeats
 steps through w4a16_gemm_host with host buffers (x copied in from pinned host memory, y copied
-back, every GEMM of the step). Two more objects, outside the timed step: `decode_step_chain` (64
-dense layers in one CUDA graph per decode step, at B = 1 .. 64 streams) and `nvfp4` (the same four
-matrices with NVFP4 weights at M = 1, 16, 256).
+back, every GEMM of the step). More objects, outside the timed step: `decode_step_chain` (64
+dense layers in one CUDA graph per decode step, at B = 1 .. 64 streams), `nvfp4` (the same four
+matrices with NVFP4 weights at M = 1, 16, 256, and their chain) and `w4a8` (the same int4 weights
+with int8 activations at M = 1, 8, 16, 256, the quantisation timed beside each row, and their chain
+with the quantisation inside the step).
 
 --workload picks one of the single configurations instead (decode, verify, batched, head, ...):
 the same line for that configuration. --impl reference times the CPU oracle (fp64, oracle/) on a
@@ -381,14 +383,16 @@ CHAIN_B = [1, 8, 16, 32, 64]
 
 
 def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAYERS, reps=5, nvfp4_scale=None,
-                        batches=None):
+                        batches=None, w4a8=False):
     """The dense layers of one decode step as one CUDA graph: per layer qkv and o from the layer input,
     gate+up from o, silu(gate) * up, down -> the next layer's input (attention itself is not part of
     this path). Every layer streams its own device copy of the four matrices (layers x 170 MB in
     total, far beyond L2). Each B is timed over `reps` graph replays and set against the pages' step
     model t_step(B) = max(W / BW, B * F / P) with W the weight bytes and F = 2 x weights per position
     (no recurrent state or KV traffic in this path). nvfp4_scale: the sources are repacked NVFP4
-    weights with that tensor scale (weight bytes counted in the canonical NVFP4 format)."""
+    weights with that tensor scale (weight bytes counted in the canonical NVFP4 format). w4a8: int4
+    weights with int8 activations: every GEMM input is quantised per token first (h once for qkv and
+    o, then o and act), inside the timed step."""
     import torch
 
     names = [n for (n, _, _) in inputs.SWEEP_MATRICES]
@@ -414,9 +418,29 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
         gu = torch.empty((B, 2 * inter), dtype=torch.float16, device=dev)
         act = torch.empty((B, inter), dtype=torch.float16, device=dev)
 
+        def qbuf(K, consumers):  # int8 activations, their fp16 copy (tile path only), per-token scales
+            tiles = any(W.w4a16_plan_for_w4a8(B, N, K, GROUP).path == W.PATH_TC for N in consumers)
+            return (torch.empty((B, K), dtype=torch.int8, device=dev),
+                    torch.empty((B, K), dtype=torch.float16, device=dev) if tiles else None,
+                    torch.empty(B, dtype=torch.float32, device=dev))
+        if w4a8:
+            qh = qbuf(hidden, (dims["qkv"][1], hidden))
+            qo = qbuf(hidden, (2 * inter,))
+            qa = qbuf(inter, (hidden,))
+
         def step():
             for li in range(layers):
                 x, y = h[li % 2], h[(li + 1) % 2]
+                if w4a8:
+                    W.quantize_x_int8(x, out=qh)
+                    W.gemm_w4a8(*qh, *copies["qkv"][li], dims["qkv"][1], hidden, GROUP, y=qkv)
+                    W.gemm_w4a8(*qh, *copies["o"][li], hidden, hidden, GROUP, y=o)
+                    W.quantize_x_int8(o, out=qo)
+                    W.gemm_w4a8(*qo, *copies["gate_up"][li], 2 * inter, hidden, GROUP, y=gu)
+                    W.silu_mul(gu, act)
+                    W.quantize_x_int8(act, out=qa)
+                    W.gemm_w4a8(*qa, *copies["down"][li], hidden, inter, GROUP, y=y)
+                    continue
                 gemm(x, copies["qkv"][li], dims["qkv"][1], hidden, qkv)
                 gemm(x, copies["o"][li], hidden, hidden, o)
                 gemm(o, copies["gate_up"][li], 2 * inter, hidden, gu)
@@ -440,8 +464,9 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
         raise RuntimeError(f"device status after the layer chain: {W.status_string(st)}")
     del copies
     torch.cuda.empty_cache()
-    return {"layers": layers, "kernels_per_step": 5 * layers, "weight_bytes_per_step": wbytes,
+    return {"layers": layers, "kernels_per_step": (8 if w4a8 else 5) * layers, "weight_bytes_per_step": wbytes,
             "weights": "NVFP4 (E2M1 + E4M3 per 16 k + fp32 tensor scale)" if nv else "int4, fp16 scales per 128 k",
+            "activations": "int8 per token (quantised in the step)" if w4a8 else "fp16",
             "what": "per layer: qkv(h), o(h), gate_up(o), silu(gate)*up, down -> next h; one CUDA graph per step, "
                     "programmatic dependent launch between the kernels; model t_step(B) = max(W/BW, B*2*weights/P) "
                     "with the measured peaks", "rows": out}
@@ -511,6 +536,66 @@ def measure_nvfp4(W, dev, peaks, timed, capture, l2, n_launches=100, keep=None):
             "bytes_per_weight": 0.5625, "device_bytes_per_weight": 0.625, "layer_step": layer, "rows": rows}
 
 
+W4A8_M = [1, 8, 16, 256]
+
+
+def measure_w4a8(W, dev, peaks, timed, capture, l2, n_launches=100, keep=None):
+    """The dense-layer matrices with int4 weights and int8 activations at M = 1, 8, 16, 256: per row
+    a CUDA graph of `n_launches` GEMM launches cycling over enough repacked copies that they exceed
+    4 x L2, and beside it the per-token quantisation of that row's input ([M, K], its own graph).
+    Roofline bytes: the weights plus int8 x and fp16 y."""
+    import torch
+
+    rows = []
+    for (name, K, N) in inputs.SWEEP_MATRICES:
+        if keep is not None and not any(n == name for (n, _) in keep):
+            continue
+        qw, sc = inputs.generate_weights(K, N, GROUP, seed=inputs.SWEEP_SEED)
+        q = torch.from_numpy(qw).to(dev)
+        s = torch.from_numpy(sc.view(np.int16)).to(dev)
+        R = max(2, -(-4 * l2 // weight_bytes(K, N)))
+        copies = [W.repack(q, s, GROUP) for _ in range(R)]
+        del q, s
+        for M in W4A8_M:
+            if keep is not None and (name, M) not in keep:
+                continue
+            x = torch.from_numpy(inputs.generate_x(M, K, seed=1000 + M).view(np.int16)).view(torch.float16).to(dev)
+            act = W.quantize_x_int8(x, with_f16=W.w4a16_plan_for_w4a8(M, N, K, GROUP).path == W.PATH_TC)
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            W.gemm_w4a8(*act, *copies[0], N, K, GROUP, y=y)
+            plan = W.w4a16_last_dispatch()
+            torch.cuda.synchronize()
+            gr = capture(lambda: [W.gemm_w4a8(*act, *copies[i % R], N, K, GROUP, y=y) for i in range(n_launches)])
+            gr.replay()
+            us = timed(gr.replay) / n_launches * 1e3
+            del gr
+            gq = capture(lambda: [W.quantize_x_int8(x, out=act) for _ in range(n_launches)])
+            gq.replay()
+            us_q = timed(gq.replay) / n_launches * 1e3
+            del gq
+            wb = weight_bytes(K, N)
+            ab = M * K + 2 * M * N
+            t_mem = (wb + ab) / (peaks["hbm_gbs"] * 1e9)
+            t_tc = gemm_flops(M, K, N) / (peaks["bf16_tflops"] * 1e12)
+            rows.append(dict(matrix=name, M=M, K=K, N=N, us=us, us_quantize=us_q, weight_gbs=wb / (us * 1e-6) / 1e9,
+                             tflops=gemm_flops(M, K, N) / (us * 1e-6) / 1e12,
+                             roofline_frac=max(t_mem, t_tc) / (us * 1e-6), bound="hbm" if t_mem >= t_tc else "tensor",
+                             plan=plan))
+        del copies
+        torch.cuda.empty_cache()
+    st = W.w4a16_device_status()
+    if st != W.OK:
+        raise RuntimeError(f"device status after the W4A8 rows: {W.status_string(st)}")
+    layer = {}
+    total = sum(weight_bytes(K, N) for (_, K, N) in inputs.SWEEP_MATRICES)
+    for M in W4A8_M if keep is None else []:
+        us = sum(r["us"] for r in rows if r["M"] == M)
+        layer[str(M)] = {"us": us, "weight_gbs": total / (us * 1e-6) / 1e9}
+    return {"format": "int4 weights (fp16 scales per 128 k), int8 activations per token",
+            "quantisation": "sx = amax / 127, xq = rne(x / sx) in binary32; us_quantize times it alone",
+            "layer_step": layer, "rows": rows}
+
+
 # ------------------------------------------------------------------------------ GPU arm
 def percentile(v, q):
     return float(np.percentile(np.asarray(v, dtype=np.float64), q))
@@ -530,6 +615,8 @@ def main():
     ap.add_argument("--table", action="store_true", help="also print the per-row table to stderr")
     ap.add_argument("--no-chain", action="store_true", help="skip the 64-layer decode-step chain")
     ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4-weight rows")
+    ap.add_argument("--no-w4a8", action="store_true", help="skip the int8-activation rows")
+    ap.add_argument("--w4a8-rows", default=None, help='int8-activation rows to run, e.g. "down:1" (profiling)')
     ap.add_argument("--nvfp4-rows", default=None,
                     help='NVFP4 rows to run, e.g. "gate_up:16" (M in 1, 16, 256; with --only: profiling)')
     ap.add_argument("--only", default=None, help='sweep rows to run, e.g. "o:16,gate_up:256" (profiling)')
@@ -782,6 +869,15 @@ def main():
             del src
             torch.cuda.empty_cache()
 
+    w4a8 = None
+    a8_keep = parse_only(args.w4a8_rows)
+    if args.workload == "sweep" and not args.no_w4a8 and (only is None or a8_keep is not None):
+        w4a8 = measure_w4a8(W, dev, peaks, timed, capture, l2, keep=a8_keep)
+        if a8_keep is None and not args.no_chain:
+            w4a8["decode_step_chain"] = measure_layer_chain(W, dev, {n: m["copies"][0] for n, m in mats.items()},
+                                                            peaks, timed, capture, w4a8=True)
+            torch.cuda.empty_cache()
+
     if args.table and rank == 0:
         print(f"{'matrix':8s} {'M':>5s} {'us':>9s} {'med':>8s} {'p10':>8s} {'p90':>8s} {'wGB/s':>7s} "
               f"{'TFLOP/s':>8s} {'roof%':>6s} bound  plan", file=sys.stderr)
@@ -797,6 +893,16 @@ def main():
         if nvfp4 and nvfp4.get("decode_step_chain"):
             for c in nvfp4["decode_step_chain"]["rows"]:
                 print(f"nvfp4 chain B={c['B']:3d}: {c['us_per_step']:9.1f} us/step {c['tokens_per_s']:9.0f} tok/s "
+                      f"{c['weight_gbs']:6.0f} GB/s model {c['model_us']:8.1f} us ({100 * c['model_frac']:.1f}%)",
+                      file=sys.stderr)
+        if w4a8:
+            for x in w4a8["rows"]:
+                print(f"w4a8 {x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} us (quantise {x['us_quantize']:5.2f} us) "
+                      f"{x['weight_gbs']:7.0f} GB/s {x['tflops']:8.1f} TFLOP/s {100 * x['roofline_frac']:6.1f}% "
+                      f"{x['bound']}", file=sys.stderr)
+        if w4a8 and w4a8.get("decode_step_chain"):
+            for c in w4a8["decode_step_chain"]["rows"]:
+                print(f"w4a8 chain B={c['B']:3d}: {c['us_per_step']:9.1f} us/step {c['tokens_per_s']:9.0f} tok/s "
                       f"{c['weight_gbs']:6.0f} GB/s model {c['model_us']:8.1f} us ({100 * c['model_frac']:.1f}%)",
                       file=sys.stderr)
         if chain:
@@ -826,7 +932,7 @@ def main():
                 "tflops": world * flops_step / (ms_step * 1e-3) / 1e12,
                 "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
                 "layer_step": layer, "rows": rows, "cold_launch_us": cold, "decode_step_chain": chain,
-                "nvfp4": nvfp4,
+                "nvfp4": nvfp4, "w4a8": w4a8,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps * len(items), "clocks": clocks,
                 "peaks": {k: v for k, v in peaks.items()}}

@@ -254,10 +254,15 @@ def test_w4a8_host_checks(W):
     assert g(FAKE + 8, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 3
     assert g(FAKE, None, FAKE * 5 + 1, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 3
     assert g(FAKE, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE + 64, 1, 1024, 1024, 128, None) == 1  # y overlaps xq
-    # the automatic plan: the integer GEMV for every M <= 8, the tiles above
-    for M in (1, 2, 5, 8):
+    # the automatic plan: the integer GEMV at M <= 2, at M <= 4 while its grid fits in one wave
+    for M in (1, 2):
         assert W.w4a16_plan_for_w4a8(M, 5120, 5120).path == W.PATH_GEMV
         assert W.w4a16_plan_for_w4a8(M, 34816, 5120).path == W.PATH_GEMV
+    for M in (3, 4):
+        assert W.w4a16_plan_for_w4a8(M, 5120, 5120).path == W.PATH_GEMV
+        assert W.w4a16_plan_for_w4a8(M, 34816, 5120).path == W.PATH_TC
+    assert W.w4a16_plan_for_w4a8(5, 5120, 5120).path == W.PATH_TC
+    assert W.w4a16_plan_for_w4a8(8, 5120, 5120 + 64, 64).path == W.PATH_GEMV  # K % 128 != 0: only the GEMV can
     p = W.w4a16_plan_for_w4a8(9, 5120, 5120)
     assert p.path == W.PATH_TC and p.m_tile == 16
     assert W.w4a16_plan_for_w4a8(256, 34816, 5120).m_tile == 256

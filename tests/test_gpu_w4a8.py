@@ -137,9 +137,9 @@ def test_quantize_then_gemm_automatic(W, M):
     x = inputs.generate_x(M, K, seed=501 + M)
     xq_ref, sx_ref = oracle.quantize_x_int8(x)
     y_ref, a_ref = oracle.gemm_w4a8(xq_ref, sx_ref, qw, sc, G)
-    act = W.quantize_x_int8(x_to_dev(x), with_f16=M > 8)
+    act = W.quantize_x_int8(x_to_dev(x))
     y = _run(W, act, r, N, K, G)
-    assert ("path=gemv" in W.w4a16_last_dispatch()) == (M <= 8)
+    assert ("path=gemv" in W.w4a16_last_dispatch()) == (W.w4a16_plan_for_w4a8(M, N, K, G).path == W.PATH_GEMV)
     assert_parity(y_f64(y), y_ref, a_ref, W.w4a16_last_dispatch())
 
 
@@ -177,7 +177,7 @@ def test_full_size_every_element(W, M, K, N):
     x = inputs.generate_x(M, K, seed=801 + M)
     xq, sx = oracle.quantize_x_int8(x)
     y_ref, a_ref = oracle.gemm_w4a8(xq, sx, qw, sc, G)
-    act = W.quantize_x_int8(x_to_dev(x), with_f16=M > 8)
+    act = W.quantize_x_int8(x_to_dev(x))
     torch.cuda.synchronize()
     assert np.array_equal(act[0].cpu().numpy(), xq)
     y = _run(W, act, r, N, K, G)

@@ -98,36 +98,6 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;      // + kb * wt
     const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;  // + g * wt
 
-    // Programmatic dependent launch: the lane's first batch of weights is pulled into L2 while the
-    // previous grid on the stream finishes; x (possibly its output) is read only after it completed.
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-        const int b = sl.kb_begin + warp + kWarps * u;
-        if (b < sl.kb_end) asm volatile("prefetch.global.L2 [%0];" ::"l"(wcol + static_cast<int64_t>(b) * wt));
-    }
-    griddep_wait();
-
-    // Stage x[0:MR][slice] as fp16 (16-byte copies).
-    {
-        const int vec_per_row = sl.klen / 8;
-        for (int i = threadIdx.x; i < MR * vec_per_row; i += kThreads) {
-            const int m = i / vec_per_row;
-            const int c = i % vec_per_row;
-            const int64_t xi = static_cast<int64_t>(m) * K + sl.kb_begin * 32 + 8 * c;
-            const uint4 v = in_bounds(xi + 8 <= static_cast<int64_t>(MR) * K, status)
-                                ? *reinterpret_cast<const uint4*>(x + xi)
-                                : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(xs + m * sl.klen + 8 * c) = v;
-        }
-    }
-    __syncthreads();
-
-    float acc[2][MR][2];
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int m = 0; m < MR; ++m) acc[c][m][0] = acc[c][m][1] = 0.f;
-
     // scale row of 32-k block b: b / (G / 32), a shift when G / 32 is a power of two (int4; NVFP4
     // has two scale rows per block, 2b and 2b + 1)
     const int gb = FP4 ? 1 : G / 32;
@@ -153,7 +123,49 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
                    ? static_cast<uint32_t>(ldg_u16(scol + static_cast<int64_t>(group_of(b)) * wt))
                    : 0u;
     };
+
+    // Programmatic dependent launch: the warp's first batch of weights and scales is loaded while the
+    // previous grid on the stream finishes; x (possibly its output) is read only after it completed.
     int kb = sl.kb_begin + warp;
+    const bool first = kb + kWarps * (kUnroll - 1) < sl.kb_end;
+    uint4 v0[kUnroll];
+    uint32_t s0[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        v0[u] = first ? load_w(kb + kWarps * u) : make_uint4(0u, 0u, 0u, 0u);
+        s0[u] = first ? load_s(kb + kWarps * u) : 0u;
+    }
+    griddep_wait();
+
+    // Stage x[0:MR][slice] as fp16 (16-byte copies).
+    {
+        const int vec_per_row = sl.klen / 8;
+        for (int i = threadIdx.x; i < MR * vec_per_row; i += kThreads) {
+            const int m = i / vec_per_row;
+            const int c = i % vec_per_row;
+            const int64_t xi = static_cast<int64_t>(m) * K + sl.kb_begin * 32 + 8 * c;
+            const uint4 v = in_bounds(xi + 8 <= static_cast<int64_t>(MR) * K, status)
+                                ? *reinterpret_cast<const uint4*>(x + xi)
+                                : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(xs + m * sl.klen + 8 * c) = v;
+        }
+    }
+    __syncthreads();
+
+    float acc[2][MR][2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[c][m][0] = acc[c][m][1] = 0.f;
+
+    if (first) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = kb + kWarps * u;
+            gemv_block<MR, FP4>(v0[u], s0[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
+        }
+        kb += kWarps * kUnroll;
+    }
     for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
         uint4 v[kUnroll];
         uint32_t sb[kUnroll];

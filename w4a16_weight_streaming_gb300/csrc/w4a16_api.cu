@@ -303,10 +303,20 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
     if (p.path < 0 || p.path > 2) return W4A16_ERR_INVALID_ARG;
     int path = p.path;
     if (path == W4A16_PATH_AUTO && w4a8) {
-        // int8 activations: the integer GEMV takes every M it supports (its arithmetic per weight
-        // is a fraction of the fp16 path's); the tiles need whole 128-k stages.
+        // int8 activations, measured on GB300 (the four dense-layer matrices): the integer GEMV is
+        // faster than the tiles at one and two rows on every matrix (5120 x 34816 at M = 2: 22.7
+        // against 33.9 us); at three and four rows only while its grid fits in one wave (the
+        // 5120-column matrices); from five rows the tiles. The tiles need whole 128-k stages.
         const bool tc_ok = K % 128 == 0 && group_fits(128, G);
-        path = M <= kGemvMaxM ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+        if (M <= 2) {
+            path = W4A16_PATH_GEMV;
+        } else if (M <= 4) {
+            const int64_t ctas = static_cast<int64_t>(N / 32) * gemv_pick_split(M, N, K, sm_count);
+            path = ctas <= 5 * static_cast<int64_t>(sm_count) ? W4A16_PATH_GEMV : W4A16_PATH_TC;
+        } else {
+            path = W4A16_PATH_TC;
+        }
+        if (path == W4A16_PATH_TC && !tc_ok && M <= kGemvMaxM) path = W4A16_PATH_GEMV;
         if (path == W4A16_PATH_GEMV && tc_ok && gemv_w4a8_smem_bytes(M, K, 16) > kGemvMaxSmem) path = W4A16_PATH_TC;
     } else if (path == W4A16_PATH_AUTO) {
         // Measured on GB300: the CUDA-core GEMV streams faster than the tensor-core tiles for one

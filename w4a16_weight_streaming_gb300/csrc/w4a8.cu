@@ -165,8 +165,12 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) {
     return v;
 }
 
+// CTAs per SM the register budget must allow: the grids are a few waves of 128-thread CTAs, and
+// one CTA fewer per SM can add a whole wave (8 per SM = at most 64 registers per thread).
+__host__ __device__ constexpr int gemv_w4a8_min_ctas(int mr) { return mr <= 2 ? 8 : mr <= 4 ? 6 : 5; }
+
 template <int MR>
-__global__ void __launch_bounds__(kThreads) gemv_w4a8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx,
+__global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR)) gemv_w4a8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx,
                                                              const uint4* __restrict__ wr,
                                                              const uint16_t* __restrict__ sr, uint16_t* __restrict__ y,
                                                              int N, int K, int G, int split, unsigned* status) {
@@ -193,10 +197,32 @@ __global__ void __launch_bounds__(kThreads) gemv_w4a8_kernel(const uint4* __rest
     const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;
     const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;
 
+    const int gb = G / 32;
+    const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
+    auto group_of = [&](int b) { return gshift >= 0 ? (b >> gshift) : b / gb; };
+    const int64_t w_total = static_cast<int64_t>(N) * KB, s_total = static_cast<int64_t>(NG) * N;
+    const int64_t w_base = wcol - wr, s_base = scol - sr;
+    auto load_w = [&](int b) {
+        return in_bounds(w_base + static_cast<int64_t>(b) * wt < w_total, status)
+                   ? ldg_stream(wcol + static_cast<int64_t>(b) * wt)
+                   : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto load_s = [&](int b) -> float {
+        const int64_t r = group_of(b);
+        return in_bounds(s_base + r * wt < s_total, status) ? __half2float(__ushort_as_half(ldg_u16(scol + r * wt)))
+                                                            : 0.f;
+    };
+
+    // Programmatic dependent launch: the warp's first batch of weights and scales is loaded while
+    // the previous grid on the stream (typically the quantisation of x) finishes; xq only after it.
+    int kb = kb_begin + warp;
+    const bool first = kb + kWarps * (kUnroll - 1) < kb_end;
+    uint4 v0[kUnroll];
+    float s0[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-        const int b = kb_begin + warp + kWarps * u;
-        if (b < kb_end) asm volatile("prefetch.global.L2 [%0];" ::"l"(wcol + static_cast<int64_t>(b) * wt));
+        v0[u] = first ? load_w(kb + kWarps * u) : make_uint4(0u, 0u, 0u, 0u);
+        s0[u] = first ? load_s(kb + kWarps * u) : 0.f;
     }
     griddep_wait();
 
@@ -233,22 +259,14 @@ __global__ void __launch_bounds__(kThreads) gemv_w4a8_kernel(const uint4* __rest
 #pragma unroll
     for (int m = 0; m < MR; ++m) acc[m] = 0.f;
 
-    const int gb = G / 32;
-    const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
-    auto group_of = [&](int b) { return gshift >= 0 ? (b >> gshift) : b / gb; };
-    const int64_t w_total = static_cast<int64_t>(N) * KB, s_total = static_cast<int64_t>(NG) * N;
-    const int64_t w_base = wcol - wr, s_base = scol - sr;
-    auto load_w = [&](int b) {
-        return in_bounds(w_base + static_cast<int64_t>(b) * wt < w_total, status)
-                   ? ldg_stream(wcol + static_cast<int64_t>(b) * wt)
-                   : make_uint4(0u, 0u, 0u, 0u);
-    };
-    auto load_s = [&](int b) -> float {
-        const int64_t r = group_of(b);
-        return in_bounds(s_base + r * wt < s_total, status) ? __half2float(__ushort_as_half(ldg_u16(scol + r * wt)))
-                                                            : 0.f;
-    };
-    int kb = kb_begin + warp;
+    if (first) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int jb = kb + kWarps * u - kb_begin;
+            w4a8_block<MR>(v0[u], s0[u], xw + 2 * jb, ofs + jb, nblk_max, acc);
+        }
+        kb += kWarps * kUnroll;
+    }
     for (; kb + kWarps * (kUnroll - 1) < kb_end; kb += kWarps * kUnroll) {
         uint4 v[kUnroll];
         float sb[kUnroll];
