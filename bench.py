@@ -431,15 +431,12 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
         def step():
             for li in range(layers):
                 x, y = h[li % 2], h[(li + 1) % 2]
-                if w4a8:
-                    W.quantize_x_int8(x, out=qh)
-                    W.gemm_w4a8(*qh, *copies["qkv"][li], dims["qkv"][1], hidden, GROUP, y=qkv)
+                if w4a8:  # quantise each input once, in the call of its first GEMM
+                    W.quantize_gemm_w4a8(x, *copies["qkv"][li], dims["qkv"][1], hidden, GROUP, out=qh, y=qkv)
                     W.gemm_w4a8(*qh, *copies["o"][li], hidden, hidden, GROUP, y=o)
-                    W.quantize_x_int8(o, out=qo)
-                    W.gemm_w4a8(*qo, *copies["gate_up"][li], 2 * inter, hidden, GROUP, y=gu)
+                    W.quantize_gemm_w4a8(o, *copies["gate_up"][li], 2 * inter, hidden, GROUP, out=qo, y=gu)
                     W.silu_mul(gu, act)
-                    W.quantize_x_int8(act, out=qa)
-                    W.gemm_w4a8(*qa, *copies["down"][li], hidden, inter, GROUP, y=y)
+                    W.quantize_gemm_w4a8(act, *copies["down"][li], hidden, inter, GROUP, out=qa, y=y)
                     continue
                 gemm(x, copies["qkv"][li], dims["qkv"][1], hidden, qkv)
                 gemm(x, copies["o"][li], hidden, hidden, o)
@@ -464,7 +461,8 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
         raise RuntimeError(f"device status after the layer chain: {W.status_string(st)}")
     del copies
     torch.cuda.empty_cache()
-    return {"layers": layers, "kernels_per_step": (8 if w4a8 else 5) * layers, "weight_bytes_per_step": wbytes,
+    kps = (8 if w4a8 else 5) * layers
+    return {"layers": layers, "kernels_per_step": kps, "weight_bytes_per_step": wbytes,
             "weights": "NVFP4 (E2M1 + E4M3 per 16 k + fp32 tensor scale)" if nv else "int4, fp16 scales per 128 k",
             "activations": "int8 per token (quantised in the step)" if w4a8 else "fp16",
             "what": "per layer: qkv(h), o(h), gate_up(o), silu(gate)*up, down -> next h; one CUDA graph per step, "
@@ -573,11 +571,20 @@ def measure_w4a8(W, dev, peaks, timed, capture, l2, n_launches=100, keep=None):
             gq.replay()
             us_q = timed(gq.replay) / n_launches * 1e3
             del gq
+            # quantisation and GEMM in one call (two kernels, the GEMM with programmatic dependent launch)
+            W.quantize_gemm_w4a8(x, *copies[0], N, K, GROUP, out=act, y=y)
+            plan_qg = W.w4a16_last_dispatch()
+            gf = capture(lambda: [W.quantize_gemm_w4a8(x, *copies[i % R], N, K, GROUP, out=act, y=y)
+                                  for i in range(n_launches)])
+            gf.replay()
+            us_qg = timed(gf.replay) / n_launches * 1e3
+            del gf
             wb = weight_bytes(K, N)
             ab = M * K + 2 * M * N
             t_mem = (wb + ab) / (peaks["hbm_gbs"] * 1e9)
             t_tc = gemm_flops(M, K, N) / (peaks["bf16_tflops"] * 1e12)
-            rows.append(dict(matrix=name, M=M, K=K, N=N, us=us, us_quantize=us_q, weight_gbs=wb / (us * 1e-6) / 1e9,
+            rows.append(dict(matrix=name, M=M, K=K, N=N, us=us, us_quantize=us_q, us_quantize_gemm=us_qg,
+                             quantize_gemm_plan=plan_qg, weight_gbs=wb / (us * 1e-6) / 1e9,
                              tflops=gemm_flops(M, K, N) / (us * 1e-6) / 1e12,
                              roofline_frac=max(t_mem, t_tc) / (us * 1e-6), bound="hbm" if t_mem >= t_tc else "tensor",
                              plan=plan))
@@ -897,7 +904,8 @@ def main():
                       file=sys.stderr)
         if w4a8:
             for x in w4a8["rows"]:
-                print(f"w4a8 {x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} us (quantise {x['us_quantize']:5.2f} us) "
+                print(f"w4a8 {x['matrix']:8s} {x['M']:5d} {x['us']:9.2f} us (quantise {x['us_quantize']:5.2f} us, "
+                      f"quantise+GEMM call {x['us_quantize_gemm']:6.2f} us) "
                       f"{x['weight_gbs']:7.0f} GB/s {x['tflops']:8.1f} TFLOP/s {100 * x['roofline_frac']:6.1f}% "
                       f"{x['bound']}", file=sys.stderr)
         if w4a8 and w4a8.get("decode_step_chain"):

@@ -257,6 +257,14 @@ int w4a16_gemm_w4a8_ex(const int8_t* xq, const uint16_t* xq_f16, const float* sx
                        const void* scales_r, uint16_t* y, int M, int N, int K, int group, const w4a16_plan* plan,
                        void* stream);
 
+/* w4a16_quantize_x_int8 then w4a16_gemm_w4a8 in one call (two kernels on `stream`, the GEMM with
+ * programmatic dependent launch): writes xq, xq_f16 (may be NULL when the plan is the GEMV) and sx,
+ * which stay valid for other GEMMs of the same x, and y. Outputs overlap neither each other nor an
+ * input. Errors as the two calls. */
+int w4a16_quantize_gemm_w4a8(const uint16_t* x, int8_t* xq, uint16_t* xq_f16, float* sx, const void* qweight_r,
+                              const void* scales_r, uint16_t* y, int M, int N, int K, int group,
+                              const w4a16_plan* plan, void* stream);
+
 /* The automatic plan of w4a16_gemm_w4a8 for this shape (host only). */
 int w4a16_plan_for_w4a8(int M, int N, int K, int group, w4a16_plan* out);
 

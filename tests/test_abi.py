@@ -268,3 +268,18 @@ def test_w4a8_host_checks(W):
     assert W.w4a16_plan_for_w4a8(256, 34816, 5120).m_tile == 256
     with pytest.raises(W.W4A16Error):
         W.w4a16_plan_for_w4a8(9, 5120, 5120 + 64)  # K % 128 != 0: the tiles cannot, the GEMV takes M <= 8
+
+
+def test_quantize_gemm_w4a8_host_checks(W):
+    f = W.w4a16_quantize_gemm_w4a8
+    A = [FAKE, FAKE * 2, None, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6]  # x, xq, xq_f16, sx, qw_r, sc_r, y
+    def call(args, M=1, N=1024, K=1024, G=128):
+        return f(*args, M, N, K, G, None, None)
+    assert call([0] + A[1:]) == 1                        # null x
+    assert call(A, M=0) == 1
+    assert call(A, N=1000) == 2
+    assert call([FAKE + 2] + A[1:]) == 3                  # x misaligned
+    assert call(A[:3] + [FAKE * 3 + 1] + A[4:]) == 3      # sx misaligned
+    assert call(A[:1] + [FAKE + 256] + A[2:]) == 1        # xq overlaps x
+    assert call(A[:6] + [FAKE * 2 + 64]) == 1             # y overlaps xq
+    assert call(A[:2] + [FAKE * 3 - 64] + A[3:]) == 1     # xq_f16 overlaps sx

@@ -250,3 +250,119 @@ def test_debug_bounds_build_runs_clean(W, plan):
     assert D.w4a16_device_status(s) == 0
     assert np.array_equal(xq.cpu().numpy(), xq_ref)
     assert_parity(y_f64(y), y_ref, a_ref, "debug-bounds build")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 16])
+@pytest.mark.parametrize("split", [0, 1, 3, 16])
+def test_quantize_gemm_in_one_call(W, M, split):
+    # w4a16_quantize_gemm_w4a8: quantisation kernel + GEMM in one call; xq / sx bit-exact
+    K, N, G = 2048, 352, 128
+    if split and M > 8:
+        pytest.skip("explicit GEMV splits apply to M <= 8")
+    qw, sc, r = _weights(W, K, N, G, seed=1200 + M)
+    x = inputs.generate_x(M, K, seed=1201 + M)
+    x.view(np.float16)[0, :7] = np.array([0.5, 1.5, -2.5, 3.5, 0, 0, 0], np.float16) * (np.abs(
+        x.view(np.float16)[0]).max() / np.float16(127))
+    xq_ref, sx_ref = oracle.quantize_x_int8(x)
+    y_ref, a_ref = oracle.gemm_w4a8(xq_ref, sx_ref, qw, sc, G)
+    plan = dict(path=1, split_k=split) if split else None
+    y, (xq, xh, sx) = W.quantize_gemm_w4a8(x_to_dev(x), r[0], r[1], N, K, G, plan=plan)
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK
+    desc = W.w4a16_last_dispatch()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
+    assert np.array_equal(xh.cpu().numpy(), xq_ref.astype(np.float16))
+    assert_parity(y_f64(y), y_ref, a_ref, desc)
+
+
+@pytest.mark.parametrize("K", [5120, 17408])
+def test_quantize_gemm_in_one_call_full_size_and_zero_row(W, K):
+    # (the GEMV path needs no fp16 copy of the codes)
+    N, G, M = 5120, 128, 2
+    qw, sc, r = _weights(W, K, N, G, seed=1300 + K)
+    x = inputs.generate_x(M, K, seed=1301)
+    x.view(np.float16)[1] = 0
+    xq_ref, sx_ref = oracle.quantize_x_int8(x)
+    y_ref, a_ref = oracle.gemm_w4a8(xq_ref, sx_ref, qw, sc, G)
+    y, (xq, xh, sx) = W.quantize_gemm_w4a8(x_to_dev(x), r[0], r[1], N, K, G, with_f16=False)
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK and xh is None
+    assert "path=gemv" in W.w4a16_last_dispatch()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref) and sx.cpu().numpy()[1] == 0.0
+    assert np.all(y.float().cpu().numpy()[1] == 0.0)
+    assert_parity(y_f64(y), y_ref, a_ref, W.w4a16_last_dispatch())
+
+
+def test_quantize_gemm_reads_previous_gemm_output(W):
+    # W4A16 GEMM -> quantise-and-multiply -> W4A8 GEMM of the same codes, NaN-filled first
+    M, K1, N1, N2, N3, G = 2, 1024, 2048, 512, 256, 128
+    qw1, sc1, r1 = _weights(W, K1, N1, G, seed=1400)
+    qw2, sc2, r2 = _weights(W, N1, N2, G, seed=1401)
+    qw3, sc3, r3 = _weights(W, N1, N3, G, seed=1402)
+    x = inputs.generate_x(M, K1, seed=1403)
+    y1 = torch.full((M, N1), float("nan"), dtype=torch.float16, device="cuda")
+    out = (torch.full((M, N1), 55, dtype=torch.int8, device="cuda"), None,
+           torch.full((M,), float("nan"), dtype=torch.float32, device="cuda"))
+    y2 = torch.full((M, N2), float("nan"), dtype=torch.float16, device="cuda")
+    y3 = torch.full((M, N3), float("nan"), dtype=torch.float16, device="cuda")
+    torch.cuda.synchronize()
+    W.gemm(x_to_dev(x), *r1, N1, K1, G, y=y1)
+    W.quantize_gemm_w4a8(y1, *r2, N2, N1, G, out=out, y=y2)
+    W.gemm_w4a8(*out, *r3, N3, N1, G, y=y3)
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK
+    xq_ref, sx_ref = oracle.quantize_x_int8(y1.cpu().numpy().view(np.uint16))
+    assert np.array_equal(out[0].cpu().numpy(), xq_ref) and np.array_equal(out[2].cpu().numpy(), sx_ref)
+    for yk, qwk, sck in ((y2, qw2, sc2), (y3, qw3, sc3)):
+        y_ref, a_ref = oracle.gemm_w4a8(xq_ref, sx_ref, qwk, sck, G)
+        assert_parity(y_f64(yk), y_ref, a_ref, "chain")
+
+
+def test_quantize_gemm_debug_bounds(W):
+    D = W.load_debug_bounds()
+    M, K, N, G = 2, 1280, 352, 128
+    qw, sc, r = _weights(W, K, N, G, seed=1500)
+    x = inputs.generate_x(M, K, seed=1501)
+    xq_ref, sx_ref = oracle.quantize_x_int8(x)
+    y_ref, a_ref = oracle.gemm_w4a8(xq_ref, sx_ref, qw, sc, G)
+    s = torch.cuda.current_stream().cuda_stream
+    xd = x_to_dev(x)
+    xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    xh = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    sx = torch.empty(M, dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    p = W.Plan(path=1, split_k=3)
+    assert D.w4a16_quantize_gemm_w4a8(xd.data_ptr(), xq.data_ptr(), xh.data_ptr(), sx.data_ptr(), r[0].data_ptr(),
+                                      r[1].data_ptr(), y.data_ptr(), M, N, K, G, ctypes.byref(p), s) == 0
+    torch.cuda.synchronize()
+    assert D.w4a16_device_status(s) == 0
+    assert np.array_equal(xq.cpu().numpy(), xq_ref) and np.array_equal(xh.cpu().numpy(), xq_ref.astype(np.float16))
+    assert_parity(y_f64(y), y_ref, a_ref, "debug-bounds build")
+
+
+def test_quantize_near_half_integers(W):
+    # activations at and beside every (k + 1/2) * sx, for several row scales: the codes must equal the
+    # oracle's rne(fl32(x / sx)) wherever the quotient lies within rounding of a half-integer
+    rng = np.random.default_rng(1600)
+    rows = []
+    for amax in np.concatenate([[127.0, 1.0, 0.1], rng.uniform(0.01, 3000.0, 13)]).astype(np.float16):
+        sx = np.float32(np.float32(amax) / np.float32(127))
+        vals = [amax]
+        for k in range(-127, 127):
+            c = np.float16((k + 0.5) * float(sx))
+            vals += [c, np.nextafter(c, np.float16(np.inf)), np.nextafter(c, np.float16(-np.inf))]
+        v = np.array(vals, np.float16)
+        v = v[np.abs(v.astype(np.float32)) <= np.float32(amax)]
+        rows.append(v)
+    K = ((max(len(r) for r in rows) + 7) // 8) * 8
+    x = np.zeros((len(rows), K), np.float16)
+    for i, r in enumerate(rows):
+        x[i, :len(r)] = r
+    xq_ref, sx_ref = oracle.quantize_x_int8(x.view(np.uint16))
+    xq, xh, sx = W.quantize_x_int8(x_to_dev(x.view(np.uint16)))
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
+    bad = np.argwhere(xq.cpu().numpy() != xq_ref)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"

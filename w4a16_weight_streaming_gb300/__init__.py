@@ -40,6 +40,7 @@ EXPORTED = [
     "w4a16_silu_mul", "w4a16_debug_bounds", "w4a16_repacked_nvfp4_scales_bytes", "w4a16_repack_nvfp4",
     "w4a16_unrepack_nvfp4", "w4a16_gemm_nvfp4", "w4a16_gemm_nvfp4_ex", "w4a16_plan_for_nvfp4",
     "w4a16_quantize_x_int8", "w4a16_gemm_w4a8", "w4a16_gemm_w4a8_ex", "w4a16_plan_for_w4a8",
+    "w4a16_quantize_gemm_w4a8",
 ]
 
 
@@ -112,6 +113,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4a16_gemm_w4a8.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.w4a16_gemm_w4a8_ex.restype = I
     lib.w4a16_gemm_w4a8_ex.argtypes = [P, P, P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
+    lib.w4a16_quantize_gemm_w4a8.restype = I
+    lib.w4a16_quantize_gemm_w4a8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, ctypes.POINTER(Plan), P]
     lib.w4a16_plan_for_w4a8.restype = I
     lib.w4a16_plan_for_w4a8.argtypes = [I, I, I, I, ctypes.POINTER(Plan)]
     return lib
@@ -271,6 +274,12 @@ def w4a16_gemm_w4a8_ex(xq: int, xq_f16: int | None, sx: int, qweight_r: int, sca
                                   ctypes.byref(plan) if plan is not None else None, stream)
 
 
+def w4a16_quantize_gemm_w4a8(x: int, xq: int, xq_f16: int | None, sx: int, qweight_r: int, scales_r: int, y: int,
+                             M: int, N: int, K: int, group: int, plan: Plan | None, stream: int | None) -> int:
+    return lib.w4a16_quantize_gemm_w4a8(x, xq, xq_f16, sx, qweight_r, scales_r, y, M, N, K, group,
+                                        ctypes.byref(plan) if plan is not None else None, stream)
+
+
 def w4a16_plan_for_w4a8(M: int, N: int, K: int, group: int = 128) -> Plan:
     p = Plan()
     rc = lib.w4a16_plan_for_w4a8(M, N, K, group, ctypes.byref(p))
@@ -381,3 +390,24 @@ def gemm_w4a8(xq: torch.Tensor, xq_f16: torch.Tensor | None, sx: torch.Tensor, q
                               qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K, group, plan,
                               _stream_handle(stream)), "w4a16_gemm_w4a8")
     return y
+
+
+def quantize_gemm_w4a8(x: torch.Tensor, qweight_r: torch.Tensor, scales_r: torch.Tensor, N: int, K: int,
+                       group: int = 128, out=None, y: torch.Tensor | None = None, plan: Plan | dict | None = None,
+                       with_f16: bool = True, stream=None):
+    """(y, (xq, xq_f16, sx)): quantise x (float16 [M, K], CUDA) and multiply in one call
+    (w4a16_quantize_gemm_w4a8); the quantised activations are returned for other GEMMs of the same x."""
+    M = x.shape[0]
+    if out is None:
+        out = (torch.empty((M, K), dtype=torch.int8, device=x.device),
+               torch.empty((M, K), dtype=torch.float16, device=x.device) if with_f16 else None,
+               torch.empty(M, dtype=torch.float32, device=x.device))
+    xq, xh, sx = out
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if isinstance(plan, dict):
+        plan = Plan(**plan)
+    _check(w4a16_quantize_gemm_w4a8(x.data_ptr(), xq.data_ptr(), xh.data_ptr() if xh is not None else None,
+                                    sx.data_ptr(), qweight_r.data_ptr(), scales_r.data_ptr(), y.data_ptr(), M, N, K,
+                                    group, plan, _stream_handle(stream)), "w4a16_quantize_gemm_w4a8")
+    return y, out

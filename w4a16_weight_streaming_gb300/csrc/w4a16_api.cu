@@ -760,6 +760,44 @@ int w4a16_gemm_w4a8(const int8_t* xq, const uint16_t* xq_f16, const float* sx, c
     return w4a16_gemm_w4a8_ex(xq, xq_f16, sx, qweight_r, scales_r, y, M, N, K, group, nullptr, stream);
 }
 
+int w4a16_quantize_gemm_w4a8(const uint16_t* x, int8_t* xq, uint16_t* xq_f16, float* sx, const void* qweight_r,
+                              const void* scales_r, uint16_t* y, int M, int N, int K, int group,
+                              const w4a16_plan* plan, void* stream) {
+    if (!x || !xq || !sx || !qweight_r || !scales_r || !y || M <= 0) return W4A16_ERR_INVALID_ARG;
+    const int sh = check_matrix_shape(N, K, group);
+    if (sh != W4A16_OK) return sh;
+    if (M > (1 << 20)) return W4A16_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(xq) || (xq_f16 && !aligned16(xq_f16)) || (reinterpret_cast<uintptr_t>(sx) & 3u) ||
+        !aligned16(qweight_r) || !aligned16(scales_r) || !aligned16(y))
+        return W4A16_ERR_MISALIGNED;
+    const size_t xb = static_cast<size_t>(M) * K * 2, qxb = static_cast<size_t>(M) * K, sb = static_cast<size_t>(M) * 4;
+    const size_t yb = static_cast<size_t>(M) * N * 2, wb = static_cast<size_t>(N) * K / 2;
+    const size_t scb = static_cast<size_t>(K / group) * N * 2;
+    const void* outs[4] = {xq, xq_f16, sx, y};
+    const size_t out_bytes[4] = {qxb, xb, sb, yb};
+    for (int i = 0; i < 4; ++i) {  // the outputs overlap neither each other nor any input
+        if (!outs[i]) continue;
+        if (overlaps(outs[i], out_bytes[i], x, xb) || overlaps(outs[i], out_bytes[i], qweight_r, wb) ||
+            overlaps(outs[i], out_bytes[i], scales_r, scb) || is_host_pointer(outs[i]))
+            return W4A16_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (outs[j] && overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return W4A16_ERR_INVALID_ARG;
+    }
+    if (is_host_pointer(x) || is_host_pointer(qweight_r) || is_host_pointer(scales_r)) return W4A16_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (!device_info(&d)) return W4A16_ERR_CUDA;
+    Choice ch;
+    const int rc = resolve_plan(M, N, K, group, plan, d.sm_count, true, &ch, true);
+    if (rc != W4A16_OK) return rc;
+    if (ch.path == W4A16_PATH_TC && xq_f16 == nullptr) return W4A16_ERR_INVALID_ARG;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_quantize_x_int8(x, xq, xq_f16, sx, M, K, st, d.status) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A16_ERR_CUDA;
+    }
+    return launch_gemm(ch, xq_f16, qweight_r, scales_r, y, M, N, K, group, d, stream, false, 1.0f, xq, sx);
+}
+
 int w4a16_plan_for_w4a8(int M, int N, int K, int group, w4a16_plan* out) {
     if (!out) return W4A16_ERR_INVALID_ARG;
     if (M <= 0) return W4A16_ERR_INVALID_ARG;

@@ -5,10 +5,11 @@
 //   sx[m] = fl32(max_k |x[m][k]| / 127), xq[m][k] = rne(fl32(x[m][k] / sx[m])) in [-127, 127]
 //   (all 0 for a zero row), y[m][n] = sx[m] * sum_g s[g][n] * sum_{k in g} (q[k][n] - 8) * xq[m][k].
 //
-// quantize_x_int8_kernel: one CTA per activation row; both divisions are IEEE binary32 (div.rn)
-//   and the rounding is to nearest even (cvt.rni), so the integers are exactly those that any
-//   implementation of the same binary32 steps produces. It writes xq as int8 and, optionally, the
-//   same integers as fp16 (exact, |xq| <= 127) for the tensor-core tiles.
+// quantize_x_int8_kernel: one CTA per activation row. The scale is an IEEE binary32 division; each
+//   code is rne(fl32(x / sx)), reached through the reciprocal product with the IEEE division
+//   wherever the product lies near a half-integer (quantize1 gives the argument), so the integers
+//   are exactly those of the binary32 steps above. It writes xq as int8 and, optionally, the same
+//   integers as fp16 (exact, |xq| <= 127) for the tensor-core tiles.
 // gemv_w4a8_kernel (M <= 8): the CUDA-core split-K GEMV of gemv.cu with integer arithmetic. The
 //   unsigned nibbles of a weight word are split into two words of four bytes (one AND, one shift
 //   and AND) and multiplied with the int8 activations by dp4a (four products and their sum per
@@ -38,6 +39,20 @@ __device__ __forceinline__ float absmax8(const uint4 v) {
         m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
     }
     return m;
+}
+
+// One activation to its int8 code: rne(fl32(f / s)), clamped; 0 for a zero row (amax = 0). r is
+// fl32(1 / s). The quotient estimate qa = fl32(f * r) is within 2^-23 |f / s| <= 1.6e-5 of f / s
+// (two roundings of 2^-24 each), and fl32(f / s) within 2^-24 |f / s| <= 7.6e-6 of it (|f / s| <=
+// 127 + 2^-16), so the two differ by less than 2.3e-5: wherever qa is at least 1e-4 away from a
+// half-integer, both round to the same integer (and fl32(f / s) is not a tie). Only the remaining
+// cases take the exact IEEE division.
+__device__ __forceinline__ int quantize1(float f, float s, float r, bool nonzero) {
+    if (!nonzero) return 0;
+    const float qa = f * r;
+    const float frac = qa - floorf(qa);
+    const float q = fabsf(frac - 0.5f) < 1e-4f ? __fdiv_rn(f, s) : qa;
+    return min(127, max(-127, __float2int_rn(q)));
 }
 
 __global__ void __launch_bounds__(kQThreads) quantize_x_int8_kernel(const uint4* __restrict__ x, uint2* __restrict__ xq,
@@ -72,6 +87,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_x_int8_kernel(const uint4*
 #pragma unroll 8
     for (int w = 0; w < kQThreads / 32; ++w) amax = fmaxf(amax, wmax[w]);
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = __frcp_rn(s);
     if (threadIdx.x == 0 && in_bounds(m < M, status)) sx[m] = s;
 
     auto emit = [&](int v, const uint4 val) {
@@ -81,11 +97,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_x_int8_kernel(const uint4*
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            int a = 0, b = 0;
-            if (amax > 0.f) {
-                a = min(127, max(-127, __float2int_rn(__fdiv_rn(f.x, s))));
-                b = min(127, max(-127, __float2int_rn(__fdiv_rn(f.y, s))));
-            }
+            const int a = quantize1(f.x, s, rs, amax > 0.f), b = quantize1(f.y, s, rs, amax > 0.f);
             q8[i >> 1] |= ((static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8))
                           << (16 * (i & 1));
             const __half2 hq = __halves2half2(__int2half_rn(a), __int2half_rn(b));
@@ -170,10 +182,10 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) {
 __host__ __device__ constexpr int gemv_w4a8_min_ctas(int mr) { return mr <= 2 ? 8 : mr <= 4 ? 6 : 5; }
 
 template <int MR>
-__global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR)) gemv_w4a8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx,
-                                                             const uint4* __restrict__ wr,
-                                                             const uint16_t* __restrict__ sr, uint16_t* __restrict__ y,
-                                                             int N, int K, int G, int split, unsigned* status) {
+__global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
+    gemv_w4a8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx, const uint4* __restrict__ wr,
+                     const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int N, int K, int G, int split,
+                     unsigned* status) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int KB = K / 32;
     const int NG = K / G;
