@@ -15,8 +15,8 @@
 //   and AND) and multiplied with the int8 activations by dp4a (four products and their sum per
 //   instruction); the offset 8 is folded in as -8 * sum(xq) of the 32-k block, staged with x. Per
 //   32-k block the exact int32 sum is scaled by the block's group scale into an fp32 accumulator;
-//   y = fp16(sx * sum). Per weight at M = 1: ~0.4 instructions of unpacking and one quarter of a
-//   dp4a, against ~1.6 + 1 of the fp16 path.
+//   y = fp16(sx * sum). Per weight at M = 1 the inner loop spends ~0.4 instructions on unpacking
+//   and a quarter of a dp4a, against ~1.6 of dequantisation and one FMA on the fp16 path.
 // The tensor-core tiles (M > 8) are the W4A16 tile kernel fed with the fp16 copy of xq (the MMA
 // of fp16 operands is exact on integers) and a per-row output scale sx: sm_103a has no int8 MMA
 // (tcgen05 kind::i8 is not available on this target).
