@@ -246,7 +246,7 @@ int w4a16_quantize_x_int8(const uint16_t* x, int8_t* xq, uint16_t* xq_f16, float
 
 /* y[M,N] (fp16, device) for int8 activations (xq, xq_f16, sx as written by w4a16_quantize_x_int8)
  * and repacked int4 weights (w4a16_repack, group `group`). The automatic plan takes the integer
- * GEMV for M <= 2, for M <= 4 when its grid fits in one wave, and the tensor-core tiles otherwise
+ * GEMV for M <= 2, for M = 3 when its grid fits in one wave, and the tensor-core tiles otherwise
  * (w4a16_plan_for_w4a8 tells which); xq_f16 may be NULL when the plan is the GEMV
  * (W4A16_ERR_INVALID_ARG if the tiles would need it). Shapes and errors as w4a16_gemm. */
 int w4a16_gemm_w4a8(const int8_t* xq, const uint16_t* xq_f16, const float* sx, const void* qweight_r,

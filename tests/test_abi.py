@@ -254,13 +254,17 @@ def test_w4a8_host_checks(W):
     assert g(FAKE + 8, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 3
     assert g(FAKE, None, FAKE * 5 + 1, FAKE * 2, FAKE * 3, FAKE * 4, 1, 1024, 1024, 128, None) == 3
     assert g(FAKE, None, FAKE * 5, FAKE * 2, FAKE * 3, FAKE + 64, 1, 1024, 1024, 128, None) == 1  # y overlaps xq
-    # the automatic plan: the integer GEMV at M <= 2, at M <= 4 while its grid fits in one wave
+    # the automatic plan: the integer GEMV at M <= 2, at M = 3 while its grid fits in one wave
     for M in (1, 2):
-        assert W.w4a16_plan_for_w4a8(M, 5120, 5120).path == W.PATH_GEMV
-        assert W.w4a16_plan_for_w4a8(M, 34816, 5120).path == W.PATH_GEMV
-    for M in (3, 4):
-        assert W.w4a16_plan_for_w4a8(M, 5120, 5120).path == W.PATH_GEMV
-        assert W.w4a16_plan_for_w4a8(M, 34816, 5120).path == W.PATH_TC
+        for (N, K) in ((5120, 5120), (7168, 5120), (34816, 5120), (5120, 17408)):
+            assert W.w4a16_plan_for_w4a8(M, N, K).path == W.PATH_GEMV
+    assert W.w4a16_plan_for_w4a8(3, 5120, 17408).path == W.PATH_GEMV   # 40 tiles x split 16 = 640 CTAs
+    assert W.w4a16_plan_for_w4a8(3, 7168, 5120).path == W.PATH_TC      # 56 tiles x split 16 = 896 CTAs
+    for (N, K) in ((5120, 5120), (34816, 5120)):
+        assert W.w4a16_plan_for_w4a8(4, N, K).path == W.PATH_TC
+    # one wave: the split is the largest power of two whose grid fits (8 CTAs per SM at M <= 2)
+    assert W.w4a16_plan_for_w4a8(1, 34816, 5120).split_k == 4       # 272 tiles x 4 = 1088 <= 1216
+    assert W.w4a16_plan_for_w4a8(1, 5120, 17408).split_k == 16
     assert W.w4a16_plan_for_w4a8(5, 5120, 5120).path == W.PATH_TC
     assert W.w4a16_plan_for_w4a8(8, 5120, 5120 + 64, 64).path == W.PATH_GEMV  # K % 128 != 0: only the GEMV can
     p = W.w4a16_plan_for_w4a8(9, 5120, 5120)

@@ -398,6 +398,42 @@ __device__ __forceinline__ float ld_dsmem_f1(uint32_t addr) {
     return v;
 }
 
+// Sum over the cluster's first `split` CTAs (split <= 16) of the value at shared address `local`,
+// added in rank order 0, 1, ... Groups of four remote loads are issued before their adds, so their
+// latencies overlap instead of following one another (same sum, same order as a plain loop).
+__device__ __forceinline__ float cluster_sum_f1(uint32_t local, int split) {
+    float s = 0.f;
+    for (int p0 = 0; p0 < split; p0 += 4) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = p0 + u < split ? ld_dsmem_f1(map_peer(local, p0 + u)) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (p0 + u < split) s += v[u];
+    }
+    return s;
+}
+
+__device__ __forceinline__ float4 cluster_sum_f4(uint32_t local, int split) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < split; p0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            v[u] = p0 + u < split ? ld_dsmem_f4(map_peer(local, p0 + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (p0 + u < split) {
+                s.x += v[u].x;
+                s.y += v[u].y;
+                s.z += v[u].z;
+                s.w += v[u].w;
+            }
+        }
+    }
+    return s;
+}
+
 // ------------------------------------------------------------------------------------ dequant
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t bits) {
     uint32_t d;

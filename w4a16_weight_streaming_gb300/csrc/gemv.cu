@@ -216,8 +216,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
         if ((e % split) != rank) continue;
         const uint32_t local = smem_u32(part + e);
-        float s = 0.f;
-        for (int p = 0; p < split; ++p) s += ld_dsmem_f1(map_peer(local, p));
+        const float s = cluster_sum_f1(local, split);
         const int m = e / 32, l = e % 32;
         const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
         if (in_bounds(yi < static_cast<int64_t>(MR) * N, status)) y[yi] = __half_as_ushort(__float2half_rn(s * tensor_scale));

@@ -73,6 +73,7 @@ cudaError_t launch_quantize_x_int8(const uint16_t* x, int8_t* xq, uint16_t* xq_f
                                    cudaStream_t s, unsigned* status);
 // Integer (dp4a) split-K GEMV, M <= 8: y = fp16(sx[m] * sum_blocks s * sum (q - 8) xq).
 size_t gemv_w4a8_smem_bytes(int M, int K, int split);
+int gemv_w4a8_ctas_per_sm(int M);  // CTAs per SM its register bound guarantees
 cudaError_t launch_gemv_w4a8(const int8_t* xq, const float* sx, const uint32_t* qweight_r, const uint16_t* scales_r,
                              uint16_t* y, int M, int N, int K, int G, int split, const LaunchCtx& ctx);
 

@@ -469,14 +469,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         const int end = static_cast<int>((static_cast<int64_t>(rank + 1) * E4) / split);
         const uint32_t red_s = sbase + P.red_off;
         for (int e4 = beg + static_cast<int>(threadIdx.x); e4 < end; e4 += kThreads) {  // all warps
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = 0; p < split; ++p) {
-                const float4 v = ld_dsmem_f4(map_peer(red_s + 16u * e4, p));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
+            float4 acc = cluster_sum_f4(red_s + 16u * e4, split);
             acc.x *= tensor_scale;
             acc.y *= tensor_scale;
             acc.z *= tensor_scale;

@@ -126,6 +126,18 @@ int gemv_pick_split(int M, int N, int K, int sm_count) {
     return std::min(split, std::max(1, KB));
 }
 
+// Split along K for the integer GEMV (one CTA per 128-column tile and K-slice): the largest power of
+// two up to 16 whose grid still fits in one wave of resident CTAs, with at least two 32-k blocks per
+// rank. Measured on GB300 at M = 1: 5120 x 34816 (272 tiles) 18.4 us at split 4 (one wave), 22.4 at
+// 8 (1.8 waves); 17408 x 5120 (40 tiles) 16.0 us at 16, 22.1 at 8.
+int gemv_w4a8_pick_split(int M, int N, int K, int sm_count) {
+    const int64_t tiles = (N + 127) / 128;
+    const int64_t slots = static_cast<int64_t>(gemv_w4a8_ctas_per_sm(M)) * sm_count;
+    int split = 1;
+    while (split < 16 && 2 * split <= K / 64 && tiles * 2 * split <= slots) split *= 2;
+    return split;
+}
+
 constexpr size_t kGemvMaxSmem = 200 * 1024;  // the GEMV's dynamic shared memory limit
 
 bool group_fits(int KC, int G) { return KC >= G ? KC % G == 0 : G % KC == 0; }
@@ -304,14 +316,15 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
     int path = p.path;
     if (path == W4A16_PATH_AUTO && w4a8) {
         // int8 activations, measured on GB300 (the four dense-layer matrices): the integer GEMV is
-        // faster than the tiles at one and two rows on every matrix (5120 x 34816 at M = 2: 22.7
-        // against 33.9 us); at three and four rows only while its grid fits in one wave (the
-        // 5120-column matrices); from five rows the tiles. The tiles need whole 128-k stages.
+        // faster than the tiles at one and two rows on every matrix (5120 x 34816 at M = 2: 21.0
+        // against 34.0 us); at three rows only while its grid fits in one wave at 5 CTAs per SM
+        // (17408 x 5120: 19.2 against 21.6 us; 5120 x 7168, with 896 CTAs, loses); from four rows
+        // the tiles. The tiles need whole 128-k stages.
         const bool tc_ok = K % 128 == 0 && group_fits(128, G);
         if (M <= 2) {
             path = W4A16_PATH_GEMV;
-        } else if (M <= 4) {
-            const int64_t ctas = static_cast<int64_t>(N / 32) * gemv_pick_split(M, N, K, sm_count);
+        } else if (M == 3) {
+            const int64_t ctas = static_cast<int64_t>((N + 127) / 128) * gemv_w4a8_pick_split(M, N, K, sm_count);
             path = ctas <= 5 * static_cast<int64_t>(sm_count) ? W4A16_PATH_GEMV : W4A16_PATH_TC;
         } else {
             path = W4A16_PATH_TC;
@@ -337,7 +350,9 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
     out->path = path;
     if (path == W4A16_PATH_GEMV) {
         if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED_SHAPE;
-        int split = p.split_k > 0 ? p.split_k : gemv_pick_split(M, N, K, sm_count);
+        int split = p.split_k > 0 ? p.split_k
+                    : w4a8 ? gemv_w4a8_pick_split(M, N, K, sm_count)
+                           : gemv_pick_split(M, N, K, sm_count);
         if (split < 1 || split > 16 || split > K / 32) return W4A16_ERR_UNSUPPORTED_SHAPE;
         const size_t smem = w4a8 ? gemv_w4a8_smem_bytes(M, K, split) : gemv_smem_bytes(M, N, K, split);
         if (smem > kGemvMaxSmem) return W4A16_ERR_UNSUPPORTED_SHAPE;
@@ -459,8 +474,9 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
         else
             e = launch_gemv(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N,
                             K, group, ch.gemv_split, ctx);
+        const long long ctas = static_cast<long long>(ch.gemv_split) * (sx != nullptr ? (N + 127) / 128 : N / 32);
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128%s", M, N,
-                 K, group, ch.gemv_split, static_cast<long long>(ch.gemv_split) * (N / 32), fmt);
+                 K, group, ch.gemv_split, ctas, fmt);
     } else {
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);

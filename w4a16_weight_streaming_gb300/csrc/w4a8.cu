@@ -10,7 +10,8 @@
 //   wherever the product lies near a half-integer (quantize1 gives the argument), so the integers
 //   are exactly those of the binary32 steps above. It writes xq as int8 and, optionally, the same
 //   integers as fp16 (exact, |xq| <= 127) for the tensor-core tiles.
-// gemv_w4a8_kernel (M <= 8): the CUDA-core split-K GEMV of gemv.cu with integer arithmetic. The
+// gemv_w4a8_kernel (M <= 8): a CUDA-core split-K GEMV with integer arithmetic (one CTA per
+//   128-column tile and K-slice, one warp per 32-column slice of it). The
 //   unsigned nibbles of a weight word are split into two words of four bytes (one AND, one shift
 //   and AND) and multiplied with the int8 activations by dp4a (four products and their sum per
 //   instruction); the offset 8 is folded in as -8 * sum(xq) of the 32-k block, staged with x. Per
@@ -181,6 +182,11 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) {
 // one CTA fewer per SM can add a whole wave (8 per SM = at most 64 registers per thread).
 __host__ __device__ constexpr int gemv_w4a8_min_ctas(int mr) { return mr <= 2 ? 8 : mr <= 4 ? 6 : 5; }
 
+// One CTA = one 128-column weight tile and one K-slice: warp w owns the tile's column slice w and
+// runs the whole K-slice, so the four warps read each 2 KB row of the tile (32 k of 128 columns)
+// together. (With the four column slices in four CTAs, each row was fetched in 512-byte parts at
+// different times: measured 20 % slower once the weights in flight exceed ~2 GB, as in a decode
+// step.) The K-slices of a tile form a cluster summed through DSMEM in rank order.
 template <int MR>
 __global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
     gemv_w4a8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx, const uint4* __restrict__ wr,
@@ -190,10 +196,12 @@ __global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
     const int KB = K / 32;
     const int NG = K / G;
     const int rank = static_cast<int>(blockIdx.x) % split;
-    const int t = static_cast<int>(blockIdx.x) / split;  // 32-column slice
-    const int tile = t / 4;
-    const int wt = min(128, N - 128 * tile);
-    const int cofs = 32 * (t % 4);
+    const int tile = static_cast<int>(blockIdx.x) / split;
+    const int wt = min(128, N - 128 * tile);  // columns of this tile (32, 64, 96 or 128)
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int col = 32 * warp + lane;         // column within the tile
+    const bool valid = 32 * warp < wt;        // (warps past a ragged last tile only take part in the syncs)
     const int kb_begin = static_cast<int>((static_cast<int64_t>(rank) * KB) / split);
     const int kb_end = static_cast<int>((static_cast<int64_t>(rank + 1) * KB) / split);
     const int nblk = kb_end - kb_begin;
@@ -201,13 +209,10 @@ __global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
 
     uint4* xw = reinterpret_cast<uint4*>(smem);                                              // [MR][nblk_max][2]
     int* ofs = reinterpret_cast<int*>(smem + static_cast<size_t>(MR) * nblk_max * 32);        // [MR][nblk_max]
-    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(MR) * nblk_max * 36);    // [kWarps][MR][32]
-    float* part = red + kWarps * MR * 32;                                                     // [MR][32]
+    float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(MR) * nblk_max * 36);   // [MR][128]
 
-    const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + cofs + lane;
-    const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + cofs + lane;
+    const uint4* wcol = wr + static_cast<int64_t>(tile) * 128 * KB + col;
+    const uint16_t* scol = sr + static_cast<int64_t>(tile) * 128 * NG + col;
 
     const int gb = G / 32;
     const int gshift = (gb & (gb - 1)) == 0 ? __ffs(gb) - 1 : -1;
@@ -227,14 +232,14 @@ __global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
 
     // Programmatic dependent launch: the warp's first batch of weights and scales is loaded while
     // the previous grid on the stream (typically the quantisation of x) finishes; xq only after it.
-    int kb = kb_begin + warp;
-    const bool first = kb + kWarps * (kUnroll - 1) < kb_end;
+    int kb = kb_begin;
+    const bool first = valid && kb + kUnroll - 1 < kb_end;
     uint4 v0[kUnroll];
     float s0[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-        v0[u] = first ? load_w(kb + kWarps * u) : make_uint4(0u, 0u, 0u, 0u);
-        s0[u] = first ? load_s(kb + kWarps * u) : 0.f;
+        v0[u] = first ? load_w(kb + u) : make_uint4(0u, 0u, 0u, 0u);
+        s0[u] = first ? load_s(kb + u) : 0.f;
     }
     griddep_wait();
 
@@ -270,68 +275,58 @@ __global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
     float acc[MR];
 #pragma unroll
     for (int m = 0; m < MR; ++m) acc[m] = 0.f;
-
-    if (first) {
+    if (valid) {
+        if (first) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int jb = kb + kWarps * u - kb_begin;
-            w4a8_block<MR>(v0[u], s0[u], xw + 2 * jb, ofs + jb, nblk_max, acc);
+            for (int u = 0; u < kUnroll; ++u) {
+                const int jb = kb + u - kb_begin;
+                w4a8_block<MR>(v0[u], s0[u], xw + 2 * jb, ofs + jb, nblk_max, acc);
+            }
+            kb += kUnroll;
         }
-        kb += kWarps * kUnroll;
-    }
-    for (; kb + kWarps * (kUnroll - 1) < kb_end; kb += kWarps * kUnroll) {
-        uint4 v[kUnroll];
-        float sb[kUnroll];
+        for (; kb + kUnroll - 1 < kb_end; kb += kUnroll) {
+            uint4 v[kUnroll];
+            float sb[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            v[u] = load_w(kb + kWarps * u);
-            sb[u] = load_s(kb + kWarps * u);
-        }
+            for (int u = 0; u < kUnroll; ++u) {
+                v[u] = load_w(kb + u);
+                sb[u] = load_s(kb + u);
+            }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int jb = kb + kWarps * u - kb_begin;
-            w4a8_block<MR>(v[u], sb[u], xw + 2 * jb, ofs + jb, nblk_max, acc);
+            for (int u = 0; u < kUnroll; ++u) {
+                const int jb = kb + u - kb_begin;
+                w4a8_block<MR>(v[u], sb[u], xw + 2 * jb, ofs + jb, nblk_max, acc);
+            }
         }
-    }
-    for (; kb < kb_end; kb += kWarps) {
-        const int jb = kb - kb_begin;
-        w4a8_block<MR>(load_w(kb), load_s(kb), xw + 2 * jb, ofs + jb, nblk_max, acc);
+        for (; kb < kb_end; ++kb) {
+            const int jb = kb - kb_begin;
+            w4a8_block<MR>(load_w(kb), load_s(kb), xw + 2 * jb, ofs + jb, nblk_max, acc);
+        }
     }
 
     griddep_launch_dependents();
-#pragma unroll
-    for (int m = 0; m < MR; ++m) red[(warp * MR + m) * 32 + lane] = acc[m];
-    __syncthreads();
-
     auto row_scale = [&](int m) { return in_bounds(m < MR, status) ? sx[m] : 0.f; };
     if (split == 1) {
-        for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
-            const int m = e / 32, l = e % 32;
-            float s = 0.f;
+        if (valid) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) s += red[(w * MR + m) * 32 + l];
-            const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
-            if (in_bounds(yi < static_cast<int64_t>(MR) * N, status))
-                y[yi] = __half_as_ushort(__float2half_rn(s * row_scale(m)));
+            for (int m = 0; m < MR; ++m) {
+                const int64_t yi = static_cast<int64_t>(m) * N + 128 * tile + col;
+                if (in_bounds(yi < static_cast<int64_t>(MR) * N, status))
+                    y[yi] = __half_as_ushort(__float2half_rn(acc[m] * row_scale(m)));
+            }
         }
         return;
     }
-    for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
-        const int m = e / 32, l = e % 32;
-        float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[(w * MR + m) * 32 + l];
-        part[e] = s;
-    }
+    for (int m = 0; m < MR; ++m) part[m * 128 + col] = acc[m];
     cluster_sync_all();
-    for (int e = threadIdx.x; e < MR * 32; e += kThreads) {
+    for (int e = threadIdx.x; e < MR * 128; e += kThreads) {
         if ((e % split) != rank) continue;
         const uint32_t local = smem_u32(part + e);
-        float s = 0.f;
-        for (int p = 0; p < split; ++p) s += ld_dsmem_f1(map_peer(local, p));
-        const int m = e / 32, l = e % 32;
-        const int64_t yi = static_cast<int64_t>(m) * N + 32 * t + l;
-        if (in_bounds(yi < static_cast<int64_t>(MR) * N, status))
+        const float s = cluster_sum_f1(local, split);
+        const int m = e / 128, c = e % 128;
+        const int64_t yi = static_cast<int64_t>(m) * N + 128 * tile + c;
+        if (c < wt && in_bounds(yi < static_cast<int64_t>(MR) * N, status))
             y[yi] = __half_as_ushort(__float2half_rn(s * row_scale(m)));
     }
     cluster_sync_all();
@@ -348,7 +343,7 @@ cudaError_t launch_gemv_w4a8_m(const int8_t* xq, const float* sx, const uint32_t
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(split) * static_cast<unsigned>(N / 32), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(split) * static_cast<unsigned>((N + 127) / 128), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx.stream;
@@ -387,9 +382,11 @@ cudaError_t launch_quantize_x_int8(const uint16_t* x, int8_t* xq, uint16_t* xq_f
                               reinterpret_cast<uint2*>(xq), reinterpret_cast<uint4*>(xq_f16), sx, M, K, status);
 }
 
+int gemv_w4a8_ctas_per_sm(int M) { return gemv_w4a8_min_ctas(M); }
+
 size_t gemv_w4a8_smem_bytes(int M, int K, int split) {
     const size_t nblk_max = static_cast<size_t>((K / 32 + split - 1) / split);
-    return static_cast<size_t>(M) * nblk_max * 36 + static_cast<size_t>(kWarps + 1) * M * 32 * 4;
+    return static_cast<size_t>(M) * nblk_max * 36 + static_cast<size_t>(M) * 128 * 4;
 }
 
 cudaError_t launch_gemv_w4a8(const int8_t* xq, const float* sx, const uint32_t* qweight_r, const uint16_t* scales_r,
