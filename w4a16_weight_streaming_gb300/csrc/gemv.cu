@@ -181,10 +181,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
             gemv_block<MR, FP4>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
         }
     }
-    for (; kb < sl.kb_end; kb += kWarps) {
-        const uint4 v = load_w(kb);
-        const uint32_t sb = load_s(kb);
-        gemv_block<MR, FP4>(v, sb, xs + (kb - sl.kb_begin) * 32, sl.klen, acc);
+    if (kb < sl.kb_end) {  // the last (< kUnroll) blocks: their loads issued together as well
+        uint4 v[kUnroll];
+        uint32_t sb[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = kb + kWarps * u;
+            v[u] = b < sl.kb_end ? load_w(b) : make_uint4(0u, 0u, 0u, 0u);
+            sb[u] = b < sl.kb_end ? load_s(b) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = kb + kWarps * u;
+            if (b < sl.kb_end) gemv_block<MR, FP4>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
+        }
     }
 
     griddep_launch_dependents();

@@ -298,9 +298,18 @@ __global__ void __launch_bounds__(kThreads, gemv_w4a8_min_ctas(MR))
                 w4a8_block<MR>(v[u], sb[u], xw + 2 * jb, ofs + jb, nblk_max, acc);
             }
         }
-        for (; kb < kb_end; ++kb) {
-            const int jb = kb - kb_begin;
-            w4a8_block<MR>(load_w(kb), load_s(kb), xw + 2 * jb, ofs + jb, nblk_max, acc);
+        if (kb < kb_end) {  // the last (< kUnroll) blocks: their loads issued together as well
+            uint4 v[kUnroll];
+            float sb[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                v[u] = kb + u < kb_end ? load_w(kb + u) : make_uint4(0u, 0u, 0u, 0u);
+                sb[u] = kb + u < kb_end ? load_s(kb + u) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                if (kb + u < kb_end) w4a8_block<MR>(v[u], sb[u], xw + 2 * (kb + u - kb_begin), ofs + (kb + u - kb_begin),
+                                                    nblk_max, acc);
         }
     }
 
