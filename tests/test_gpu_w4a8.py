@@ -67,7 +67,7 @@ def _quant_rows(M, K, seed):
     return x
 
 
-@pytest.mark.parametrize("M,K", [(5, 1000), (6, 5120), (3, 17408), (2, 40960)])
+@pytest.mark.parametrize("M,K", [(5, 1000), (6, 5120), (3, 17408), (2, 40960), (1, 17408), (70, 5120)])
 def test_quantize_matches_oracle_bit_for_bit(W, M, K):
     x = _quant_rows(M, K, seed=K)
     xq_ref, sx_ref = oracle.quantize_x_int8(x.view(np.uint16))
