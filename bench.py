@@ -2,24 +2,24 @@
 """Benchmark of the W4A16 weight-streaming GEMM on GB300 (one JSON line on stdout).
 
 Default workload: the dense-layer sweep. The four matrices of one dense layer (K x N = 5120 x 7168
-fused qkv, 5120 x 5120 o, 5120 x 34816 fused gate+up, 17408 x 5120 down; group 128) at every
-M in {1, 2, 4, ..., 1024}. One step = one pass of the hot path over all 44 (M, matrix) GEMMs, in
-layer order (for each M: qkv, o, gate+up, down), each y = x . dequant(W) through the C ABI.
-`value` = weight bytes streamed per step / step time (effective weight-stream GB/s of the whole
-sweep); `tflops` likewise; `rows` gives every (matrix, M) launch on its own: mean us (plain CUDA
-graph), median / p10 / p90 us (per-launch event pairs), weight GB/s, TFLOP/s, roofline fraction,
-bound and plan.
+fused qkv, 5120 x 5120 o, 5120 x 34816 fused gate+up, 17408 x 5120 down; group 128) at every M in
+{1, 2, 4, ..., 1024}. One step = one pass of the hot path over all 44 (M, matrix) GEMMs, in layer
+order (for each M: qkv, o, gate+up, down), each y = x . dequant(W) through the C ABI. `value` =
+weight bytes streamed per step / step time (effective weight-stream GB/s of the whole sweep);
+`tflops` likewise; `rows` gives every (matrix, M) launch on its own: mean us (plain CUDA graph),
+median / p10 / p90 us (per-launch event pairs), weight GB/s, TFLOP/s, roofline fraction, bound and
+plan.
 
 Timing: W untimed warm-up steps; the K timed steps are K replays of a CUDA graph of one step,
-bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on the launching
-stream. L2: every weight matrix exists in R device copies and consecutive uses of one copy are at
-least 4 x L2 bytes of other weights apart, so no launch finds its weights in L2. `e2e` repeats
-steps through w4a16_gemm_host with host buffers (x copied in from pinned host memory, y copied
-back, every GEMM of the step). More objects, outside the timed step: `decode_step_chain` (64
-dense layers in one CUDA graph per decode step, at B = 1 .. 64 streams), `nvfp4` (the same four
-matrices with NVFP4 weights at M = 1, 16, 256, and their chain) and `w4a8` (the same int4 weights
-with int8 activations at M = 1, 8, 16, 256, the quantisation timed beside each row, and their chain
-with the quantisation inside the step).
+bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on the launching stream.
+L2: every weight matrix exists in R device copies and consecutive uses of one copy are at least 4 x
+L2 bytes of other weights apart, so no launch finds its weights in L2. `e2e` repeats steps through
+w4a16_gemm_host with host buffers (x copied in from pinned host memory, y copied back, every GEMM of
+the step, the independent GEMMs spread over three streams). More objects, outside the timed step:
+`decode_step_chain` (64 dense layers in one CUDA graph per decode step, at B = 1 .. 64 streams),
+`nvfp4` (the same four matrices with NVFP4 weights at M = 1, 16, 256, and their chain) and `w4a8`
+(the same int4 weights with int8 activations at M = 1, 8, 16, 256, the quantisation timed beside
+each row, and their chain with the quantisation inside the step).
 
 --workload picks one of the single configurations instead (decode, verify, batched, head, ...):
 the same line for that configuration. --impl reference times the CPU oracle (fp64, oracle/) on a
@@ -471,6 +471,7 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
 
 
 NVFP4_M = [1, 16, 256]
+E2E_STREAMS = 3  # streams the end-to-end step spreads its independent GEMMs over
 
 
 def nvfp4_weight_bytes(K: int, N: int) -> int:
@@ -819,28 +820,37 @@ def main():
     t_roof_step = sum(max(*roofline_seconds(x["M"], x["K"], x["N"], peaks)) for x in rows)
 
     # ---- end to end through the C ABI with host buffers: per GEMM, w4a16_gemm_host queues the copy of
-    # x from pinned host memory, the GEMM and the copy of y back to pinned host memory
+    # x from pinned host memory, the GEMM and the copy of y back to pinned host memory. The step's
+    # GEMMs are independent, so they go round-robin to E2E_STREAMS streams (one call each, as a user
+    # would issue them): one GEMM's copies overlap another's kernel. The streams join the timing
+    # stream before and after every step.
     h2d = sum(it["xd"].numel() * 2 for it in items)
     d2h = sum(it["yd"].numel() * 2 for it in items)
-    stream = torch.cuda.current_stream().cuda_stream
+    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
     calls = []
-    for it in items:
+    for i, it in enumerate(items):
         qr, sr = mats[it["name"]]["copies"][it["copy"]]
         calls.append((it["x_host"].data_ptr(), it["xd"].data_ptr(), qr.data_ptr(), sr.data_ptr(),
-                      it["yd"].data_ptr(), it["y_host"].data_ptr(), it["M"], it["N"], it["K"], GROUP, stream))
+                      it["yd"].data_ptr(), it["y_host"].data_ptr(), it["M"], it["N"], it["K"], GROUP,
+                      e2e_streams[i % E2E_STREAMS].cuda_stream))
 
     def e2e_step():
+        cur = torch.cuda.current_stream()
+        for s in e2e_streams:
+            s.wait_stream(cur)
         for c in calls:
             rc = W.w4a16_gemm_host(*c)
             if rc != W.OK:
                 raise RuntimeError(f"w4a16_gemm_host: {W.status_string(rc)}")
+        for s in e2e_streams:
+            cur.wait_stream(s)
 
     e2e_step()
     torch.cuda.synchronize()
     ne = max(1, args.e2e_steps)
     e2e_ms = dist_max(dist, timed(e2e_step, ne), dev) / ne
     e2e = {"value": world * step_wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": ne}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": ne, "streams": E2E_STREAMS}
     st = W.w4a16_device_status()
     if st != W.OK:
         raise RuntimeError(f"device status after the end-to-end steps: {W.status_string(st)}")
