@@ -9,7 +9,9 @@
   2^-10 (|y| + sum_k |x w|), plus the oracle's own rounding of its intermediate, plus the
   difference of the stage's inputs carried through the stage as independent errors (6 sigma, with
   the previous stage's bound as sigma). The layer is the dense-layer shape scaled down (hidden 2048,
-  qkv 2560, MLP 4096) so that the oracle holds |w|^2 in memory."""
+  qkv 2560, MLP 4096) so that the oracle holds |w|^2 in memory.
+* The same two layers with int8 activations (W4A8), every stage against the oracle applied to the
+  stage's own GPU inputs."""
 from __future__ import annotations
 
 import numpy as np
@@ -134,3 +136,40 @@ def test_two_layer_chain(W, layers, M):
             assert not bad.any(), (f"layer {layer} {stage}: {int(bad.sum())} of {err.size} outside, "
                                    f"worst err/bound {float(np.max(err / bound)):.3f}")
         hb, e_h = ref["down"]
+
+
+@pytest.mark.parametrize("M", [1, 2, 16])
+def test_two_layer_chain_int8_activations(W, layers, M):
+    # The same two layers with int8 activations (W4A8): every GEMM input quantised per token in the
+    # call of its first GEMM, all on one stream with programmatic dependent launch. Each stage is
+    # checked against the oracle applied to that stage's own GPU inputs: the codes and scales bit
+    # for bit, every GEMM output at the per-GEMM bound, the activation at its bound.
+    x0 = inputs.generate_x(M, H, seed=700 + M)
+    h = x_to_dev(x0)
+    outs = []
+    for mats in layers:
+        qkv, qh = W.quantize_gemm_w4a8(h, *mats["qkv"]["r"], QKV, H, G)
+        o = W.gemm_w4a8(*qh, *mats["o"]["r"], H, H, G)
+        gu, qo = W.quantize_gemm_w4a8(o, *mats["gu"]["r"], 2 * INTER, H, G)
+        act = W.silu_mul(gu)
+        h_next, qa = W.quantize_gemm_w4a8(act, *mats["down"]["r"], H, INTER, G)
+        outs.append(dict(h=h, qh=qh, qkv=qkv, o=o, qo=qo, gu=gu, act=act, qa=qa, down=h_next))
+        h = h_next
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK
+    for layer, (mats, st) in enumerate(zip(layers, outs)):
+        for (src, q, gemms) in (("h", "qh", (("qkv", "qkv"), ("o", "o"))), ("o", "qo", (("gu", "gu"),)),
+                                ("act", "qa", (("down", "down"),))):
+            xq_ref, sx_ref = oracle.quantize_x_int8(_bits(st[src]))
+            xq, _, sx = st[q]
+            assert np.array_equal(xq.cpu().numpy(), xq_ref), f"layer {layer}: codes of {src}"
+            assert np.array_equal(sx.cpu().numpy(), sx_ref), f"layer {layer}: scales of {src}"
+            for (mname, out) in gemms:
+                y_ref, a_ref = oracle.gemm_w4a8(xq_ref, sx_ref, mats[mname]["qw"], mats[mname]["sc"], G)
+                got = _f64(_bits(st[out]))
+                bound = 2.0 ** -10 * (np.abs(y_ref) + a_ref)
+                bad = ~(np.abs(got - y_ref) <= bound)
+                assert not bad.any(), f"layer {layer} {out}: {int(bad.sum())} outside"
+        act_ref, _ = oracle.silu_mul(_bits(st["gu"]))
+        got = _f64(_bits(st["act"]))
+        assert np.all(np.abs(got - act_ref) <= (2.0 ** -11 + 2.0 ** -20) * np.abs(act_ref) + 2.0 ** -25)
