@@ -85,7 +85,8 @@ def roofline_seconds(M: int, K: int, N: int, peaks: dict) -> tuple[float, float]
 # ncu capture (summaries under profiles/), with the SHA-256 prefix of the kernel sources it was
 # taken from: a figure is reported only while those sources are unchanged.
 MEASURED_TRAFFIC: dict[str, tuple[int, tuple[str, ...], str, str]] = {
-    "path=tc M=1024 N=34816 K=5120 ": (119_372_032, ("tc_gemm.cu", "common.cuh"), "c8003cb870078998",
+    # both launches of the GEMM: the whole waves of unsplit tiles and the K-split tail
+    "path=tc M=1024 N=34816 K=5120 ": (128_406_016, ("tc_gemm.cu", "common.cuh"), "f49a808f026474c8",
                                        "profiles/tc_gemm_mt256_m1024_5120x34816_traffic.md"),
 }
 
@@ -952,7 +953,8 @@ def main():
                 "layer_step": layer, "rows": rows, "cold_launch_us": cold, "decode_step_chain": chain,
                 "nvfp4": nvfp4, "w4a8": w4a8,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * len(items), "clocks": clocks,
+                "gpu_launches": args.steps * sum(2 if "tail_items=" in r["plan"] else 1 for r in rows),
+                "clocks": clocks,
                 "peaks": {k: v for k, v in peaks.items()}}
         print(json.dumps(line), flush=True)
     if dist is not None:

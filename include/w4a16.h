@@ -71,6 +71,11 @@ typedef struct {
     int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
     int clusters;    /* reserved, must be 0 */
     int dequant_warps; /* TC: 16, or 8 (m_tile <= 64, k_chunk 128: half-size CTAs, two per SM) */
+    int tail_split;  /* TC, with split_k 1 (or 0): when the work items (128 output columns x m_tile
+                        rows) do not fill whole waves of resident CTAs, the items of the last,
+                        partial wave run as a second launch on the same stream, each split this many
+                        ways along K (2..16). 0: none in an explicit plan, the dispatcher's choice in
+                        an automatic one (all fields 0); other values: W4A16_ERR_INVALID_ARG. */
 } w4a16_plan;
 
 /* Library version: major*10000 + minor*100 + patch. */

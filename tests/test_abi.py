@@ -182,13 +182,13 @@ def test_boundary_shapes_get_plans(W):
         W.w4a16_plan_for(1, 5120, (1 << 22) + 128, 128)
 
 
-def _plan_in_subprocess(env_value):
+def _plan_in_subprocess(env_value, shape=(1, 5120, 5120, 128), fields=("path", "split_k", "m_tile")):
     import subprocess
     import sys
 
     code = ("import w4a16_weight_streaming_gb300 as W\n"
             "try:\n"
-            "    p = W.w4a16_plan_for(1, 5120, 5120, 128); print(p.path, p.split_k, p.m_tile)\n"
+            f"    p = W.w4a16_plan_for{tuple(shape)}; print(*[getattr(p, f) for f in {tuple(fields)}])\n"
             "except W.W4A16Error as e:\n"
             "    print('error', e.code)\n")
     env = dict(os.environ)
@@ -205,6 +205,38 @@ def test_plan_override_from_environment(W):
     assert _plan_in_subprocess("path=2,bogus=1") == ["error", "1"]    # malformed: refused loudly
     assert _plan_in_subprocess("path=2,split_k=x") == ["error", "1"]
     assert _plan_in_subprocess("path=1,split_k=40") == ["error", "2"]  # valid syntax, invalid plan
+
+
+def test_partial_wave_tail_plans(W):
+    # Work items of 128 columns x 256 rows that overfill whole waves (one CTA per SM, 152 SMs
+    # without a device): the automatic plan runs the last, partial wave's items as a second launch,
+    # each split along K, when the cost model rates it cheaper than one launch.
+    for N, K in ((5120, 5120), (7168, 5120), (34816, 5120), (5120, 17408)):
+        p = W.w4a16_plan_for(1024, N, K, 128)
+        assert p.path == W.PATH_TC and p.m_tile == 256 and p.split_k == 1 and 2 <= p.tail_split <= 16, (N, K)
+        assert p.tail_split <= K // p.k_chunk
+    assert W.w4a16_plan_for(1000, 5088, 5120, 128).tail_split > 0  # ragged rows and last column tile
+    assert W.w4a16_plan_for(512, 34816, 5120, 128).tail_split == 0  # 88 left over: no one-wave tail
+    assert W.w4a16_plan_for(256, 5120, 5120, 128).tail_split == 0  # 40 items: one partial wave, split_k
+    assert W.w4a16_plan_for(16, 34816, 5120, 128).tail_split == 0  # small tiles: not this rule
+    assert W.w4a16_plan_for(1, 34816, 5120, 128).tail_split == 0  # the GEMV
+    assert W.w4a16_plan_for_nvfp4(1024, 5120, 5120).tail_split > 0
+    assert W.w4a16_plan_for_w4a8(1024, 5120, 5120).tail_split > 0
+
+
+def test_tail_split_in_explicit_plans(W):
+    shape, f = (1024, 5120, 5120, 128), ("path", "split_k", "tail_split")
+    assert _plan_in_subprocess("path=2,m_tile=256,split_k=1,tail_split=3", shape, f) == ["2", "1", "3"]
+    assert _plan_in_subprocess("path=2,tail_split=8", shape, f) == ["2", "1", "8"]
+    assert _plan_in_subprocess("path=2,m_tile=256,split_k=2", shape, f) == ["2", "2", "0"]  # explicit: none unless asked
+    assert _plan_in_subprocess("path=2,tail_split=1", shape, f) == ["error", "1"]
+    assert _plan_in_subprocess("path=2,tail_split=17", shape, f) == ["error", "1"]
+    assert _plan_in_subprocess("path=2,tail_split=-2", shape, f) == ["error", "1"]
+    assert _plan_in_subprocess("path=2,split_k=2,tail_split=4", shape, f) == ["error", "1"]
+    # one partial wave only (40 items): nothing to split off, the plan stays one unsplit launch
+    assert _plan_in_subprocess("path=2,m_tile=256,tail_split=4", (256, 5120, 5120, 128), f) == ["2", "1", "0"]
+    # a tail split above the stage count of K
+    assert _plan_in_subprocess("path=2,tail_split=16", (1024, 5120, 1024, 128), f) == ["error", "2"]
 
 
 def test_wait_timeout_setting(W):

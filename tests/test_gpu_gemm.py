@@ -313,3 +313,85 @@ def test_half_size_tiles(W, mt, ni):
             y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
             assert "dequant_warps=8" in W.w4a16_last_dispatch()
             assert_parity(y_f64(y), y_ref, abs_ref, W.w4a16_last_dispatch())
+
+
+# ------------------------------------------------------------------------------ partial last wave
+# Work items of 128 columns x 256 rows that overfill whole waves of one CTA per SM: the items of the
+# last, partial wave run as a second launch whose clusters split each of them along K.
+TAIL_SAMPLED = [(1024, 5120, 5120), (1000, 5120, 5088), (1024, 17408, 5120), (1024, 5120, 7168), (1024, 5120, 34816)]
+
+
+def _tail_samples(M, N, rng):
+    """Every column of the last two column tiles on rows of every row tile, plus random elements."""
+    cols = np.arange(max(0, N - 256), N)
+    rows = np.array(sorted({0, 1, 255, 256, 511, 512, 767, 768, min(M - 1, 900), M - 1} & set(range(M))))
+    ms = np.concatenate([np.repeat(rows, len(cols)), rng.integers(0, M, 2000)])
+    ns = np.concatenate([np.tile(cols, len(rows)), rng.integers(0, N, 2000)])
+    return ms, ns
+
+
+@pytest.mark.parametrize("M,K,N", TAIL_SAMPLED)
+def test_partial_wave_tail_sampled(W, M, K, N):
+    """Automatic plans of the layer shapes at M = 1000-1024 (a tail in each; the first with ragged
+    rows and a 96-column last tile)."""
+    G = inputs.GROUP
+    d = inputs.generate(M, K, N, G, seed=M + K + N)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    y = y_f64(run_gemm(W, x, qw_r, sc_r, N, K, G))
+    what = W.w4a16_last_dispatch()
+    assert "tail_items=" in what, what
+    assert np.all(np.isfinite(y))
+    ms, ns = _tail_samples(M, N, np.random.default_rng(M + N))
+    y_ref, abs_ref = oracle.gemm_sampled(d["x"], d["qweight"], d["scales"], G, ms, ns)
+    assert_parity(y[ms, ns], y_ref, abs_ref, what)
+
+
+@pytest.mark.parametrize("M,K,N,tails", [(200, 256, 19552, (2,)), (300, 1024, 10112, (2, 3, 8)),
+                                         (129, 512, 19584, (4,))])
+def test_partial_wave_tail_every_element(W, M, K, N, tails):
+    """Explicit tail plans on shapes the oracle multiplies in full: 153 or 158 work items (one or
+    six in the tail), ragged rows, a 96-column last tile, tail splits 2-8 up to K's stage count."""
+    G = inputs.GROUP
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=M + N)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    for t in tails:
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=256, split_k=1, tail_split=t))
+        what = W.w4a16_last_dispatch()
+        assert f"tail_split={t}" in what, what
+        assert_parity(y_f64(y), y_ref, abs_ref, what)
+        # the same product in one unsplit launch: bit-identical on the column tiles before the tail
+        y1 = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=256, split_k=1))
+        mtiles, items = -(-M // 256), -(-N // 128) * -(-M // 256)
+        first_tail_col = 128 * ((items - int(what.split("tail_items=")[1].split()[0])) // mtiles)
+        assert torch.equal(y[:, :first_tail_col], y1[:, :first_tail_col]), what
+
+
+def test_partial_wave_tail_nvfp4_and_int8_activations(W):
+    """The other weight and activation formats through the same two-launch plan (M = 1024,
+    5120 x 5120), sampled on the tail's columns and at random."""
+    M, K, N = 1024, 5120, 5120
+    rng = np.random.default_rng(77)
+    ms, ns = _tail_samples(M, N, rng)
+    qw, s8, g = inputs.generate_nvfp4_weights(K, N, seed=78)
+    x = inputs.generate_x(M, K, seed=79)
+    r = W.repack_nvfp4(torch.from_numpy(qw).cuda(), torch.from_numpy(s8).cuda())
+    y = W.gemm_nvfp4(x_to_dev(x), r[0], r[1], g, N, K)
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK
+    what = W.w4a16_last_dispatch()
+    assert "tail_items=" in what and "weights=nvfp4" in what, what
+    y_ref, abs_ref = oracle.gemm_nvfp4_sampled(x, qw, s8, g, ms, ns)
+    assert_parity(y_f64(y)[ms, ns], y_ref, abs_ref, what)
+
+    G = inputs.GROUP
+    qw, sc = inputs.generate_weights(K, N, G, seed=80)
+    r = W.repack(torch.from_numpy(qw).cuda(), torch.from_numpy(sc.view(np.int16)).cuda(), G)
+    act = W.quantize_x_int8(x_to_dev(x))
+    y = W.gemm_w4a8(*act, r[0], r[1], N, K, G)
+    torch.cuda.synchronize()
+    assert W.w4a16_device_status() == W.OK
+    what = W.w4a16_last_dispatch()
+    assert "tail_items=" in what and "activations=int8" in what, what
+    xq, sx = oracle.quantize_x_int8(x)
+    y_ref, abs_ref = oracle.gemm_w4a8_sampled(xq, sx, qw, sc, G, ms, ns)
+    assert_parity(y_f64(y)[ms, ns], y_ref, abs_ref, what)

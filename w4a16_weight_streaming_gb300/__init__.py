@@ -50,7 +50,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("m_tile", ctypes.c_int),
                 ("k_chunk", ctypes.c_int), ("stages", ctypes.c_int), ("tmem_stages", ctypes.c_int),
                 ("mma_issuers", ctypes.c_int), ("clusters", ctypes.c_int),
-                ("dequant_warps", ctypes.c_int)]
+                ("dequant_warps", ctypes.c_int), ("tail_split", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -56,6 +56,10 @@ struct TcConfig {
     int tmem_stages;  // TMEM A ring depth, 2..8
     int issuers;      // MMA-issuing threads (1, 2 or 4), each with its own accumulator
     int dequant_warps;  // 16, or 8 (small tiles that fit two CTAs per SM)
+    // Work items (column tile x row tile) of the last, partial wave of a split-1 launch, run as a
+    // second launch whose clusters split each item `tail_split` ways along K (0: no second launch).
+    int tail_items = 0;
+    int tail_split = 0;
 };
 bool tc_instantiated(int m_tile, int k_chunk, int issuers, int dequant_warps);
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G);

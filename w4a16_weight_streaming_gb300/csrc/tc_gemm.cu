@@ -40,6 +40,10 @@
 // 128 x MT output tile; after the mainloop each CTA writes its fp32 partial tile to shared
 // memory and the cluster sums them through distributed shared memory in rank order, each CTA
 // finishing 1/split of the tile. No global scratch memory is used.
+//
+// Partial last wave: a GEMM whose work items (column tile x row tile) overfill whole waves of
+// resident CTAs can run as two launches of this kernel on the same stream, the whole waves unsplit
+// and the remaining items split along K (kernel argument item0 = the launch's first item).
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -138,7 +142,7 @@ template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW, bool FP4>
 __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
-                   int split, int s_stages, int a_stages, int x_3d, float tensor_scale,
+                   int split, int item0, int s_stages, int a_stages, int x_3d, float tensor_scale,
                    const float* __restrict__ row_scale, unsigned* status, uint64_t timeout_ns) {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
@@ -199,12 +203,13 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(a_stages * kACols);
 
-    // grid.x = column tiles x row tiles x split: one cluster of `split` consecutive CTAs per (column
-    // tile, row tile), the row tile varying fastest, so that the CTAs streaming the same weight
-    // tile for different rows of x run side by side and all but the first find it in L2
+    // grid.x = work items x split: one cluster of `split` consecutive CTAs per work item (column
+    // tile, row tile) item0, item0 + 1, ..., the row tile varying fastest, so that the CTAs
+    // streaming the same weight tile for different rows of x run side by side and all but the
+    // first find it in L2
     const int mtiles = (M + MT - 1) / MT;
     const int rank = static_cast<int>(blockIdx.x) % split;
-    const int rest = static_cast<int>(blockIdx.x) / split;
+    const int rest = item0 + static_cast<int>(blockIdx.x) / split;
     const int tile = rest / mtiles;
     const int n0 = tile * kTileN;
     const int wt = min(kTileN, N - n0);  // columns of this tile (32, 64, 96 or 128)
@@ -533,12 +538,10 @@ cudaError_t prepare_kernel(Kern kern, size_t smem, int split) {
 }
 
 template <int MT, int KC, int NI, bool GI, int DW>
-cudaLaunchConfig_t make_config(const TcConfig& c, int M, int N, size_t smem, cudaStream_t stream,
+cudaLaunchConfig_t make_config(const TcConfig& c, int items, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(c.split) * static_cast<unsigned>((N + kTileN - 1) / kTileN) *
-                           static_cast<unsigned>((M + MT - 1) / MT),
-                       1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(c.split) * static_cast<unsigned>(items), 1, 1);
     cfg.blockDim = dim3(threads_for(GI, NI, DW), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -562,14 +565,25 @@ template <int MT, int KC, int NI, bool GI, int DW>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
                         uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
     auto kern = ctx.nvfp4 ? tc_gemm_kernel<MT, KC, NI, GI, DW, true> : tc_gemm_kernel<MT, KC, NI, GI, DW, false>;
-    const size_t smem = launch_smem(MT, KC, G, c);
-    cudaError_t e = prepare_kernel(kern, smem, c.split);
-    if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(c, M, N, smem, ctx.stream, attr);
-    return cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
-                              c.split, c.stages, c.tmem_stages, three_d ? 1 : 0, ctx.tensor_scale, ctx.row_scale,
-                              ctx.status, ctx.timeout_ns);
+    const int items = ((N + kTileN - 1) / kTileN) * ((M + MT - 1) / MT);
+    const int tail = c.tail_items;
+    // the work items of the full waves, then those of the last partial wave, split further along K
+    for (int part = 0; part < 2; ++part) {
+        TcConfig cp = c;
+        if (part == 1) cp.split = c.tail_split;
+        const int n = part == 0 ? items - tail : tail;
+        if (n <= 0) continue;
+        const size_t smem = launch_smem(MT, KC, G, cp);
+        cudaError_t e = prepare_kernel(kern, smem, cp.split);
+        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(cp, n, smem, ctx.stream, attr);
+        e = cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
+                               cp.split, part == 0 ? 0 : items - tail, cp.stages, cp.tmem_stages, three_d ? 1 : 0,
+                               ctx.tensor_scale, ctx.row_scale, ctx.status, ctx.timeout_ns);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.
@@ -674,6 +688,15 @@ bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
     if (c.k_chunk >= G && c.k_chunk % G != 0) return false;
     const SmemPlan P = make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.split);
     if (P.total + 1024 > 232448) return false;
+    if (c.tail_items < 0) return false;
+    if (c.tail_items > 0) {  // a second launch: split 1 before it, 2..16 in it
+        const int64_t items = static_cast<int64_t>((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
+        if (c.split != 1 || c.tail_items >= items) return false;
+        if (c.tail_split < 2 || c.tail_split > 16 || c.tail_split > K / c.k_chunk) return false;
+        if (static_cast<int64_t>(c.tail_split) * c.tail_items > 0x7fffffffLL) return false;
+        if (make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.tail_split).total + 1024 > 232448)
+            return false;
+    }
     return true;
 }
 

@@ -164,6 +164,18 @@ int default_tmem_stages(int m_tile, int k_chunk, int issuers) {
 // Split along K that minimises (waves) x (stages of work per CTA + fixed cost) + a small cost per
 // cluster rank. Waves use the device's cluster occupancy for each split (clusters must fit inside
 // one GPC, so large clusters leave SMs idle); without a device, the SM count.
+// CTAs of config c resident at once: the driver's cluster occupancy, or without a device an
+// estimate from TMEM columns and shared memory per SM.
+int resident_slots(const TcConfig& c, int G, int sm_count, bool have_device) {
+    int slots = have_device ? tc_resident_ctas(c, G) : 0;
+    if (slots <= 0) {
+        const int per_sm =
+            std::max(1, std::min(512 / tc_tmem_cols(c), static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024))));
+        slots = (sm_count * per_sm / c.split) * c.split;
+    }
+    return slots;
+}
+
 int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, bool have_device) {
     const int tiles = ((N + 127) / 128) * ((M + base.m_tile - 1) / base.m_tile);
     const int C = K / base.k_chunk;
@@ -173,12 +185,7 @@ int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, b
         if (static_cast<int64_t>(tiles) * s > 0x7fffffffLL) break;  // the grid's x extent
         TcConfig c = base;
         c.split = s;
-        int slots = have_device ? tc_resident_ctas(c, G) : 0;
-        if (slots <= 0) {
-            const int per_sm = std::max(1, std::min(512 / tc_tmem_cols(c),
-                                                    static_cast<int>(233472 / (tc_smem_bytes(c, G) + 1024))));
-            slots = (sm_count * per_sm / s) * s;
-        }
+        const int slots = resident_slots(c, G, sm_count, have_device);
         if (slots <= 0) continue;
         const int ctas = tiles * s;
         const int waves = (ctas + slots - 1) / slots;
@@ -194,6 +201,53 @@ int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, b
         }
     }
     return split;
+}
+
+// Work items (column tile x row tile) of the last, partial wave when config c runs unsplit; 0 when
+// the items fill whole waves or fit in one.
+int partial_wave_items(const TcConfig& c, int M, int N, int G, int sm_count, bool have_device) {
+    TcConfig c1 = c;
+    c1.split = 1;
+    c1.tail_items = c1.tail_split = 0;
+    const int items = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
+    const int slots = resident_slots(c1, G, sm_count, have_device);
+    return slots <= 0 || items <= slots ? 0 : items % slots;
+}
+
+// Whole waves of unsplit work items, then a second launch for the items of the last, partial wave,
+// each split along K so that together they fill one wave: taken when pick_split's cost model (128-
+// and 256-row tiles) rates it below the single launch. Measured on GB300 at M = 1024: 5120 x 5120
+// 79.2 -> 56.6 us, 17408 x 5120 194.7 -> 144.5 us, 5120 x 7168 79.9 -> 67.7 us, 5120 x 34816
+// 323.7 -> 304 us; the model's splits were within 3 % of the best forced one.
+void pick_tail(TcConfig& c, int M, int N, int K, int G, int sm_count, bool have_device) {
+    const int r = partial_wave_items(c, M, N, G, sm_count, have_device);
+    if (r <= 0) return;
+    const int items = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
+    const int C = K / c.k_chunk;
+    TcConfig c1 = c;
+    c1.split = 1;
+    const int slots1 = resident_slots(c1, G, sm_count, have_device);
+    const int full_waves = items / slots1;
+    const int slots = resident_slots(c, G, sm_count, have_device);
+    if (slots <= 0) return;
+    const int waves = static_cast<int>((static_cast<int64_t>(items) * c.split + slots - 1) / slots);
+    double best = static_cast<double>(waves) * ((C + c.split - 1) / c.split + 17.0 + c.split);
+    int tail_split = 0;
+    for (int s = 2; s <= 16 && s <= C; ++s) {
+        TcConfig ct = c1;
+        ct.split = s;
+        if (r * s > resident_slots(ct, G, sm_count, have_device)) continue;  // the tail in one wave
+        const double cost = full_waves * (C + 18.0) + ((C + s - 1) / s + 17.0 + s);
+        if (cost < best - 1e-9) {
+            best = cost;
+            tail_split = s;
+        }
+    }
+    if (tail_split > 0) {
+        c.split = 1;
+        c.tail_items = r;
+        c.tail_split = tail_split;
+    }
 }
 
 TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) {
@@ -219,6 +273,7 @@ TcConfig tc_default(int M, int N, int K, int G, int sm_count, bool have_device) 
     c.tmem_stages = default_tmem_stages(c.m_tile, c.k_chunk, c.issuers);
     c.stages = fill_stages(c, G, 225 * 1024, 8);
     c.split = pick_split(c, M, N, K, G, sm_count, have_device);
+    if (c.m_tile >= 128) pick_tail(c, M, N, K, G, sm_count, have_device);
     return c;
 }
 
@@ -264,6 +319,7 @@ const EnvPlan& env_plan() {
                          : key == "mma_issuers"   ? &r.plan.mma_issuers
                          : key == "clusters"      ? &r.plan.clusters
                          : key == "dequant_warps" ? &r.plan.dequant_warps
+                         : key == "tail_split"    ? &r.plan.tail_split
                                                   : nullptr;
             if (!field || n < 0 || n > 4096 || (stop && *stop != '\0')) {
                 r.valid = false;
@@ -282,7 +338,8 @@ int resolve_plan(int M, int N, int K, int G, const w4a16_plan* plan, int sm_coun
                  bool w4a8 = false) {
     bool automatic = plan == nullptr || (plan->path == 0 && plan->split_k == 0 && plan->m_tile == 0 &&
                                          plan->k_chunk == 0 && plan->stages == 0 && plan->tmem_stages == 0 &&
-                                         plan->mma_issuers == 0 && plan->clusters == 0 && plan->dequant_warps == 0);
+                                         plan->mma_issuers == 0 && plan->clusters == 0 && plan->dequant_warps == 0 &&
+                                         plan->tail_split == 0);
     if (automatic && env_plan().present) {
         if (!env_plan().valid) return W4A16_ERR_INVALID_ARG;
         plan = &env_plan().plan;
@@ -385,6 +442,13 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
             c.stages = p.stages > 0 ? p.stages : fill_stages(c, G, 225 * 1024, 8);
         }
         c.split = p.split_k > 0 ? p.split_k : std::min(pick_split(c, M, N, K, G, sm_count, have_device), K / c.k_chunk);
+        c.tail_items = c.tail_split = 0;
+    }
+    if (p.tail_split != 0) {  // the last partial wave's items as a second launch, split tail_split ways
+        if (p.tail_split < 2 || p.tail_split > 16 || p.split_k > 1) return W4A16_ERR_INVALID_ARG;
+        c.split = 1;
+        c.tail_items = partial_wave_items(c, M, N, G, sm_count, have_device);
+        c.tail_split = c.tail_items > 0 ? p.tail_split : 0;
     }
     if (!tc_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     out->tc = c;
@@ -478,15 +542,21 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128%s", M, N,
                  K, group, ch.gemv_split, ctas, fmt);
     } else {
+        char tail[80] = "";
+        if (ch.tc.tail_items > 0)
+            snprintf(tail, sizeof(tail), " tail_items=%d tail_split=%d tail_grid=(%lld,1,1)", ch.tc.tail_items,
+                     ch.tc.tail_split, static_cast<long long>(ch.tc.tail_items) * ch.tc.tail_split);
         e = launch_tc(x, static_cast<const uint32_t*>(qweight_r), static_cast<const uint16_t*>(scales_r), y, M, N, K,
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
                  "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "dequant_warps=%d split_k=%d grid=(%lld,1,1) tmem_cols=%d smem=%zu%s",
+                 "dequant_warps=%d split_k=%d grid=(%lld,1,1)%s tmem_cols=%d smem=%zu%s",
                  M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
                  ch.tc.dequant_warps, ch.tc.split,
-                 static_cast<long long>(ch.tc.split) * ((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile),
-                 tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), fmt);
+                 static_cast<long long>(ch.tc.split) *
+                     (static_cast<long long>((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile) -
+                      ch.tc.tail_items),
+                 tail, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), fmt);
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -504,7 +574,7 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
 
 extern "C" {
 
-int w4a16_version(void) { return 200; }
+int w4a16_version(void) { return 300; }
 
 int w4a16_debug_bounds(void) {
 #ifdef W4A16_DEBUG_BOUNDS
@@ -597,6 +667,7 @@ static int plan_for_group(int M, int N, int K, int group, w4a16_plan* out, bool 
     out->path = ch.path;
     out->clusters = 0;
     out->dequant_warps = 0;
+    out->tail_split = ch.path == W4A16_PATH_TC ? ch.tc.tail_split : 0;
     if (ch.path == W4A16_PATH_GEMV) {
         out->split_k = ch.gemv_split;
         out->m_tile = out->k_chunk = out->stages = out->tmem_stages = out->mma_issuers = 0;
