@@ -83,3 +83,30 @@ def test_repack_round_trip_and_activation_run_clean(W, D):
     assert _status(D) == W.OK
     assert torch.equal(qw2, qw) and torch.equal(sc2, sc)
     assert torch.equal(act.view(torch.int16), W.silu_mul(gu).view(torch.int16))
+
+
+@pytest.mark.parametrize("plan", [dict(path=2, m_tile=256, split_k=1), dict(path=2, m_tile=256, split_k=1, tail_split=2),
+                                  dict(path=2, m_tile=128, split_k=1)], ids=["persistent", "tail", "persistent128"])
+def test_persistent_grid_and_tail_run_clean(W, D, plan):
+    """153 work items of 128 columns (the last 96 wide): a persistent grid of one CTA per SM, or
+    152 unsplit items and a K-split tail, through the index-checking build."""
+    M, K, N, G = 200, 256, 19552, 128
+    d = inputs.generate(M, K, N, G, seed=720)
+    y_ref, abs_ref = oracle.gemm(d["x"], d["qweight"], d["scales"], G)
+    x, qw, sc = to_dev(d)
+    qw_r = torch.empty(N * K // 8, dtype=torch.int32, device="cuda")
+    sc_r = torch.empty((K // G) * N, dtype=torch.int16, device="cuda")
+    assert D.w4a16_repack(qw.data_ptr(), sc.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), N, K, G, _stream()) == 0
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    p = W.Plan(**plan)
+    assert D.w4a16_gemm_ex(x.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), y.data_ptr(), M, N, K, G,
+                           ctypes.byref(p), _stream()) == 0
+    torch.cuda.synchronize()
+    assert _status(D) == W.OK
+    what = ctypes.create_string_buffer(512)
+    D.w4a16_last_dispatch(what, 512)
+    assert (b"tail_split=2" in what.value) == ("tail_split" in plan), what.value
+    assert_parity(y_f64(y), y_ref, abs_ref, f"debug-bounds build {plan}")
+    y_norm = W.gemm(x, *W.repack(qw, sc, G), N, K, G, plan=plan)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_norm.view(torch.int16))

@@ -395,3 +395,30 @@ def test_partial_wave_tail_nvfp4_and_int8_activations(W):
     xq, sx = oracle.quantize_x_int8(x)
     y_ref, abs_ref = oracle.gemm_w4a8_sampled(xq, sx, qw, sc, G, ms, ns)
     assert_parity(y_f64(y)[ms, ns], y_ref, abs_ref, what)
+
+
+# ------------------------------------------------------------------------------ persistent grids
+# An unsplit launch of the 128- or 256-row tile with more work items than resident CTAs (one per
+# SM) runs one CTA per slot, each taking every slots-th item, its ring and barrier phases running on
+# from one item to the next.
+PERSISTENT = [
+    (256, 256, 20480, dict(path=2, m_tile=256, split_k=1)),                 # 160 items: 8 CTAs take two
+    (130, 512, 40960, dict(path=2, m_tile=256, split_k=1)),                 # 320 items, ragged rows
+    (200, 256, 19552, dict(path=2, m_tile=256, split_k=1)),                 # 153 items, the last 96 wide
+    (128, 256, 20480, dict(path=2, m_tile=128, split_k=1)),                 # the 128-row tile
+    (256, 512, 39680, dict(path=2, m_tile=256, split_k=1, tail_split=4)),   # 2 persistent waves + a tail
+]
+
+
+@pytest.mark.parametrize("M,K,N,plan", PERSISTENT, ids=lambda v: str(v) if not isinstance(v, dict) else "")
+def test_persistent_grid_every_element(W, M, K, N, plan):
+    G = inputs.GROUP
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=M + 3 * N)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+    what = W.w4a16_last_dispatch()
+    assert " persistent" in what, what
+    assert_parity(y_f64(y), y_ref, abs_ref, what)
+    # deterministic: the same plan again gives the same bits
+    y2 = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), what

@@ -60,6 +60,9 @@ struct TcConfig {
     // second launch whose clusters split each item `tail_split` ways along K (0: no second launch).
     int tail_items = 0;
     int tail_split = 0;
+    // > 0: a launch of unsplit CTAs with more work items than this runs this many CTAs, each taking
+    // every persist_ctas-th item (persistent grid); 0: one CTA (cluster) per item
+    int persist_ctas = 0;
 };
 bool tc_instantiated(int m_tile, int k_chunk, int issuers, int dequant_warps);
 bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G);

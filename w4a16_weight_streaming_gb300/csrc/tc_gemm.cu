@@ -41,9 +41,14 @@
 // memory and the cluster sums them through distributed shared memory in rank order, each CTA
 // finishing 1/split of the tile. No global scratch memory is used.
 //
-// Partial last wave: a GEMM whose work items (column tile x row tile) overfill whole waves of
-// resident CTAs can run as two launches of this kernel on the same stream, the whole waves unsplit
-// and the remaining items split along K (kernel argument item0 = the launch's first item).
+// Work items: a launch covers the work items (column tile x row tile) [item0, item_end). A GEMM whose
+// items overfill whole waves of resident CTAs can run as two launches on the same stream: the whole
+// waves unsplit, then the remaining items split along K. An unsplit launch of the 128- or 256-row
+// tile with more items than resident CTAs runs persistent (template PERSIST): one CTA per slot,
+// each taking every slots-th item, its TMA ring and barrier phases running on from one item to the
+// next, so that the copies for the next item overlap the last MMAs and the epilogue of the current
+// one; the dequantisation warps meet at a barrier after each epilogue before the next item's MMAs
+// overwrite the accumulator.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -89,7 +94,7 @@ __host__ __device__ inline SmemPlan make_plan(int MT, int KC, int s_stages, int 
     }
     p.bar_off = (end + 7u) & ~7u;
     p.misc_off = p.bar_off + (2 * s_stages + 2 * a_stages + 1) * 8;
-    p.total = p.misc_off + 16;
+    p.total = p.misc_off + 20;
     return p;
 }
 
@@ -138,11 +143,11 @@ __device__ __forceinline__ bool group_sync_and(int id, int nthreads, bool pred) 
 // per 32-k block) instead of int4 with offset 8. tensor_scale multiplies every fp32 sum before
 // the fp16 rounding (1 for int4); row_scale, when not null, then multiplies the sums of output row
 // m by row_scale[m] (the int8 activations' per-token scale).
-template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW, bool FP4>
+template <int MT, int KC, int NA, bool GROUP_ISSUE, int DW, bool FP4, bool PERSIST>
 __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint4* __restrict__ wr,
                    const uint16_t* __restrict__ sr, uint16_t* __restrict__ y, int M, int N, int K, int G,
-                   int split, int item0, int s_stages, int a_stages, int x_3d, float tensor_scale,
+                   int split, int item0, int item_end, int s_stages, int a_stages, int x_3d, float tensor_scale,
                    const float* __restrict__ row_scale, unsigned* status, uint64_t timeout_ns) {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(KC == 128 || KC == 256, "stage K must be 128 or 256");
@@ -190,6 +195,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         }
         mbar_init(dfull_bar, NA);
         *abort_flag = 0;
+        *reinterpret_cast<volatile int*>(smem + P.misc_off + 16) = 0;
         fence_barrier_init();
     }
     if (warp == kProducerWarp) {
@@ -203,75 +209,148 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(a_stages * kACols);
 
-    // grid.x = work items x split: one cluster of `split` consecutive CTAs per work item (column
-    // tile, row tile) item0, item0 + 1, ..., the row tile varying fastest, so that the CTAs
-    // streaming the same weight tile for different rows of x run side by side and all but the
-    // first find it in L2
+    // Work items (column tile, row tile) in [item0, item_end), the row tile varying fastest: cluster
+    // cl of the launch (`split` consecutive CTAs) takes items item0 + cl, item0 + cl + ncl, ... One
+    // item per cluster when the grid covers them all; several, back to back, for a persistent grid
+    // of unsplit CTAs, whose copies for the next item then overlap the current item's last MMAs and
+    // epilogue. Consecutive items run side by side, so the CTAs that stream one weight tile for
+    // different rows of x all but the first find it in L2.
     const int mtiles = (M + MT - 1) / MT;
     const int rank = static_cast<int>(blockIdx.x) % split;
-    const int rest = item0 + static_cast<int>(blockIdx.x) / split;
-    const int tile = rest / mtiles;
-    const int n0 = tile * kTileN;
-    const int wt = min(kTileN, N - n0);  // columns of this tile (32, 64, 96 or 128)
-    const int m0 = (rest % mtiles) * MT;
+    const int cl = static_cast<int>(blockIdx.x) / split;
+    const int ncl = static_cast<int>(gridDim.x) / split;
+    const int first_item = item0 + cl;
     const int KB = K / 32;
     const int NG = K / G;
     const int ngs = groups_per_stage(KC, G);
     const int C = K / KC;
     const int c_begin = static_cast<int>((static_cast<int64_t>(rank) * C) / split);
     const int c_end = static_cast<int>((static_cast<int64_t>(rank + 1) * C) / split);
-    const int niter = c_end - c_begin;
-    const uint4* w_tile = wr + static_cast<int64_t>(tile) * kTileN * KB;       // [K/32][wt] vectors
-    const uint16_t* s_tile = sr + static_cast<int64_t>(tile) * kTileN * NG;    // [K/G][wt]
+    const int niter = c_end - c_begin;  // stages per item, the same for every item of this CTA
+    struct Item {
+        int tile, n0, wt, m0;  // wt: columns of the tile (32, 64, 96 or 128)
+    };
+    auto item_at = [&](int rest) {
+        Item it;
+        it.tile = rest / mtiles;
+        it.n0 = it.tile * kTileN;
+        it.wt = min(kTileN, N - it.n0);
+        it.m0 = (rest % mtiles) * MT;
+        return it;
+    };
+    // items whose accumulator the issuers committed (dfull phases), for the drain at exit
+    volatile int* items_committed = reinterpret_cast<volatile int*>(smem + P.misc_off + 16);
+    const Item it1 = item_at(first_item);  // the first (with split > 1 the only) item of this cluster
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            const uint32_t wbytes = static_cast<uint32_t>(kKB * wt * 16);
-            const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
-            const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
             // (debug-bounds build: every copy's source range inside its buffer; a copy that is not
             // issued leaves its stage incomplete, so the kernel also reports the wait's timeout)
             const int64_t w_bytes_all = static_cast<int64_t>(N) * K / 2, s_bytes_all = static_cast<int64_t>(NG) * N * 2;
-            auto issue_w = [&](int i) {  // weights and scales of stage use i (no dependence on x)
-                const int s = i % s_stages;
-                const int k0 = (c_begin + i) * KC;
-                const uint32_t fb = full_bar(s);
-                const uint4* wsrc = w_tile + static_cast<int64_t>(k0 / 32) * wt;
-                const uint16_t* ssrc = s_tile + static_cast<int64_t>(k0 / G) * wt;
-                mbar_arrive_expect_tx(fb, bytes);
-                if (in_bounds((wsrc - wr) * 16 + wbytes <= w_bytes_all, status))
-                    bulk_g2s(sbase + P.w_off + s * P.w_stage, wsrc, wbytes, fb, pol);
-                if (in_bounds((ssrc - sr) * 2 + sbytes <= s_bytes_all, status))
-                    bulk_g2s(sbase + P.s_off + s * P.s_stage, ssrc, sbytes, fb, pol);
-            };
-            auto issue_x = [&](int i) {
-                const int s = i % s_stages;
-                const int k0 = (c_begin + i) * KC;
-                in_bounds(k0 + KC <= K && m0 < M, status);  // rows >= M of the box are zero-filled by the copy
-                const uint32_t xs = sbase + P.x_off + s * P.x_stage;
-                if (x_3d) {
-                    tma_load_x_3d(xs, &tmap_x, k0, m0, full_bar(s));
-                } else {
+            int issued = 0;  // stage uses of the ring issued, over all items of this CTA
+            if constexpr (!PERSIST) {  // one work item (this straight form measured faster than the loop)
+                const uint4* w_tile = wr + static_cast<int64_t>(it1.tile) * kTileN * KB;     // [K/32][wt] vectors
+                const uint16_t* s_tile = sr + static_cast<int64_t>(it1.tile) * kTileN * NG;  // [K/G][wt]
+                const int wt = it1.wt, m0 = it1.m0;
+                const uint32_t wbytes = static_cast<uint32_t>(kKB * wt * 16);
+                const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
+                const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
+                auto issue_w = [&](int i) {  // weights and scales of stage use i (no dependence on x)
+                    const int s = i % s_stages;
+                    const int k0 = (c_begin + i) * KC;
+                    const uint32_t fb = full_bar(s);
+                    const uint4* wsrc = w_tile + static_cast<int64_t>(k0 / 32) * wt;
+                    const uint16_t* ssrc = s_tile + static_cast<int64_t>(k0 / G) * wt;
+                    mbar_arrive_expect_tx(fb, bytes);
+                    if (in_bounds((wsrc - wr) * 16 + wbytes <= w_bytes_all, status))
+                        bulk_g2s(sbase + P.w_off + s * P.w_stage, wsrc, wbytes, fb, pol);
+                    if (in_bounds((ssrc - sr) * 2 + sbytes <= s_bytes_all, status))
+                        bulk_g2s(sbase + P.s_off + s * P.s_stage, ssrc, sbytes, fb, pol);
+                };
+                auto issue_x = [&](int i) {
+                    const int s = i % s_stages;
+                    const int k0 = (c_begin + i) * KC;
+                    in_bounds(k0 + KC <= K && m0 < M, status);  // rows >= M of the box are zero-filled by the copy
+                    const uint32_t xs = sbase + P.x_off + s * P.x_stage;
+                    if (x_3d) {
+                        tma_load_x_3d(xs, &tmap_x, k0, m0, full_bar(s));
+                    } else {
 #pragma unroll
-                    for (int a = 0; a < KC / 64; ++a)
-                        tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, full_bar(s));
+                        for (int a = 0; a < KC / 64; ++a)
+                            tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, full_bar(s));
+                    }
+                };
+                // Programmatic dependent launch: the first ring fill of weights goes out before the
+                // previous grid on the stream has finished; x (possibly its output) only after.
+                const int pre = niter < s_stages ? niter : s_stages;
+                for (int i = 0; i < pre; ++i) issue_w(i);
+                griddep_wait();
+                for (int i = 0; i < pre; ++i) issue_x(i);
+                issued = pre;
+                for (int i = pre; i < niter; ++i) {
+                    // far ahead of the consumers: a suspending wait costs no issue slots and no latency here
+                    const uint32_t ph = static_cast<uint32_t>(i / s_stages) & 1u;  // parity of this use of the stage
+                    if (!mbar_wait(empty_bar(i % s_stages), ph ^ 1u, abort_flag, timeout_ns, status)) break;
+                    issue_w(i);
+                    issue_x(i);
+                    issued = i + 1;
                 }
-            };
-            // Programmatic dependent launch: the first ring fill of weights goes out before the
-            // previous grid on the stream has finished; x (possibly its output) only after.
-            const int pre = niter < s_stages ? niter : s_stages;
-            for (int i = 0; i < pre; ++i) issue_w(i);
-            griddep_wait();
-            for (int i = 0; i < pre; ++i) issue_x(i);
-            int issued = pre;
-            for (int i = pre; i < niter; ++i) {
-                // far ahead of the consumers: a suspending wait costs no issue slots and no latency here
-                const uint32_t ph = static_cast<uint32_t>(i / s_stages) & 1u;  // parity of this use of the stage
-                if (!mbar_wait(empty_bar(i % s_stages), ph ^ 1u, abort_flag, timeout_ns, status)) break;
-                issue_w(i);
-                issue_x(i);
-                issued = i + 1;
+            } else {  // every item of this CTA, the ring continuing from one item to the next
+                bool go_on = true;
+                for (int rest = first_item;; rest += ncl) {
+                    const Item it = item_at(rest);
+                    const uint4* w_tile = wr + static_cast<int64_t>(it.tile) * kTileN * KB;     // [K/32][wt] vectors
+                    const uint16_t* s_tile = sr + static_cast<int64_t>(it.tile) * kTileN * NG;  // [K/G][wt]
+                    const uint32_t wbytes = static_cast<uint32_t>(kKB * it.wt * 16);
+                    const uint32_t sbytes = static_cast<uint32_t>(ngs * it.wt * 2);
+                    const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
+                    auto issue_w = [&](int i, int u) {  // weights and scales of stage i, ring use u (no x)
+                        const int s = u % s_stages;
+                        const int k0 = (c_begin + i) * KC;
+                        const uint32_t fb = full_bar(s);
+                        const uint4* wsrc = w_tile + static_cast<int64_t>(k0 / 32) * it.wt;
+                        const uint16_t* ssrc = s_tile + static_cast<int64_t>(k0 / G) * it.wt;
+                        mbar_arrive_expect_tx(fb, bytes);
+                        if (in_bounds((wsrc - wr) * 16 + wbytes <= w_bytes_all, status))
+                            bulk_g2s(sbase + P.w_off + s * P.w_stage, wsrc, wbytes, fb, pol);
+                        if (in_bounds((ssrc - sr) * 2 + sbytes <= s_bytes_all, status))
+                            bulk_g2s(sbase + P.s_off + s * P.s_stage, ssrc, sbytes, fb, pol);
+                    };
+                    auto issue_x = [&](int i, int u) {
+                        const int s = u % s_stages;
+                        const int k0 = (c_begin + i) * KC;
+                        in_bounds(k0 + KC <= K && it.m0 < M, status);  // rows >= M of the box are zero-filled
+                        const uint32_t xs = sbase + P.x_off + s * P.x_stage;
+                        if (x_3d) {
+                            tma_load_x_3d(xs, &tmap_x, k0, it.m0, full_bar(s));
+                        } else {
+#pragma unroll
+                            for (int a = 0; a < KC / 64; ++a)
+                                tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, it.m0, full_bar(s));
+                        }
+                    };
+                    int i = 0;
+                    if (rest == first_item) {  // the first ring fill, as above
+                        const int pre = niter < s_stages ? niter : s_stages;
+                        for (int k = 0; k < pre; ++k) issue_w(k, k);
+                        griddep_wait();
+                        for (int k = 0; k < pre; ++k) issue_x(k, k);
+                        issued = i = pre;
+                    }
+                    for (; i < niter; ++i) {
+                        const int u = issued;
+                        const uint32_t ph = static_cast<uint32_t>(u / s_stages) & 1u;  // parity of this use of the slot
+                        if (u >= s_stages && !mbar_wait(empty_bar(u % s_stages), ph ^ 1u, abort_flag, timeout_ns, status)) {
+                            go_on = false;
+                            break;
+                        }
+                        issue_w(i, u);
+                        issue_x(i, u);
+                        ++issued;
+                    }
+                    if (!PERSIST || !go_on || rest + ncl >= item_end) break;
+                }
             }
             griddep_launch_dependents();
             // Let the copies still in flight land before shared memory can be released.
@@ -293,39 +372,52 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         volatile int* go = reinterpret_cast<volatile int*>(smem + P.misc_off + 8);
         int s = 0, a = 0;
         uint32_t sph = 0, aph = 0;
-        for (int i = 0; i < niter; ++i) {
-            if (j == 0 && lane == 0)
-                go[i & 1] = (mbar_spin(afull_bar(a), aph, abort_flag, timeout_ns, status) &&
-                             mbar_spin(full_bar(s), sph, abort_flag, timeout_ns, status))
-                                ? 1
-                                : 0;
-            if (NA > 1) asm volatile("bar.sync 5, %0;" ::"n"(32 * NA) : "memory");
-            else __syncwarp();
-            if (go[i & 1] == 0) break;
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
-                const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
-#pragma unroll
-                for (int t = 0; t < kGroupSteps; ++t) {
-                    const int ks = j + t * NA;  // interleaved k-steps keep the issuers evenly busy
-                    const uint32_t koff = static_cast<uint32_t>(((ks / 4) * MT * 128 + (ks % 4) * 32) >> 4);
-                    umma_f16_ts(d_j, a_tmem + ks * 8, dstage + koff, idesc, (i > 0) || (t > 0));
+        int u = 0;  // stage uses consumed, over all items
+        int n_done = 0;
+        bool go_on = true;
+        for (int rest = first_item;; rest += ncl) {
+            for (int i = 0; i < niter; ++i, ++u) {
+                const int gu = PERSIST ? u : i;  // this stage's use of the ring, over all items
+                if (j == 0 && lane == 0)
+                    go[gu & 1] = (mbar_spin(afull_bar(a), aph, abort_flag, timeout_ns, status) &&
+                                 mbar_spin(full_bar(s), sph, abort_flag, timeout_ns, status))
+                                    ? 1
+                                    : 0;
+                if (NA > 1) asm volatile("bar.sync 5, %0;" ::"n"(32 * NA) : "memory");
+                else __syncwarp();
+                if (go[gu & 1] == 0) {
+                    go_on = false;
+                    break;
                 }
-                umma_commit(empty_bar(s));
-                umma_commit(aempty_bar(a));
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
+                    const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
+#pragma unroll
+                    for (int t = 0; t < kGroupSteps; ++t) {
+                        const int ks = j + t * NA;  // interleaved k-steps keep the issuers evenly busy
+                        const uint32_t koff = static_cast<uint32_t>(((ks / 4) * MT * 128 + (ks % 4) * 32) >> 4);
+                        umma_f16_ts(d_j, a_tmem + ks * 8, dstage + koff, idesc, (i > 0) || (t > 0));
+                    }
+                    umma_commit(empty_bar(s));
+                    umma_commit(aempty_bar(a));
+                }
+                __syncwarp();
+                if (++s == s_stages) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+                if (++a == a_stages) {
+                    a = 0;
+                    aph ^= 1u;
+                }
             }
+            if (lane == 0) umma_commit(dfull_bar);
+            ++n_done;
             __syncwarp();
-            if (++s == s_stages) {
-                s = 0;
-                sph ^= 1u;
-            }
-            if (++a == a_stages) {
-                a = 0;
-                aph ^= 1u;
-            }
+            if (!PERSIST || !go_on || rest + ncl >= item_end) break;
         }
-        if (lane == 0) umma_commit(dfull_bar);
+        if (j == 0 && lane == 0) *items_committed = n_done;
         __syncwarp();
     } else {
         // ---------------- dequantisation warps (and, grouped scheme, per group one MMA issuer)
@@ -333,14 +425,11 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         const int part = warp >> 2;
         const int grp = warp / kGroupWarps;               // accumulator group
         const bool issuer = (warp % kGroupWarps) == 0;    // first warp of the group issues its MMAs
-        const bool valid = 32 * q < wt;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         // scale row (within a stage's scale block) of each of this warp's 32-k blocks
         int srow[kPartKB];
 #pragma unroll
         for (int u = 0; u < kPartKB; ++u) srow[u] = KC >= G ? (32 * (part * kPartKB + u)) / G : 0;
-        // shared addresses of this lane's first vector / scale in stage 0 (explicit shared loads)
-        const uint32_t wst0 = sbase + P.w_off + 16u * static_cast<uint32_t>(32 * q + lane + part * kPartKB * wt);
         const uint32_t sst0 = sbase + P.s_off + 2u * static_cast<uint32_t>(32 * q + lane);
         const uint32_t a_base = tmem + lane_base + static_cast<uint32_t>(part * kPartKB * 16);
         // MMA operands of this group: k-steps grp*kGroupSteps .. +kGroupSteps of each stage
@@ -350,122 +439,140 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         const uint32_t stage_step = P.x_stage >> 4;
         int s = 0, a = 0;
         uint32_t sph = 0, aph = 0;
-        for (int i = 0; i < niter; ++i) {
-            bool ok = warp_wait_fast(full_bar(s), sph, abort_flag, timeout_ns, status);
-            if (ok && i >= a_stages) ok = warp_wait_fast(aempty_bar(a), aph ^ 1u, abort_flag, timeout_ns, status);
-            if (ok && valid) {
-                const uint32_t wst = wst0 + static_cast<uint32_t>(s) * P.w_stage;
-                const uint32_t sst = sst0 + static_cast<uint32_t>(s) * P.s_stage;
-                uint32_t regs[kPartKB * 16];
-                uint4 v[kPartKB];
-                uint32_t sb[kPartKB], sb2[kPartKB];
+        int u = 0;      // stage uses consumed, over all items
+        int jdone = 0;  // items entered (each commits the accumulator once)
+        for (int rest = first_item;; rest += ncl) {
+            const Item it = item_at(rest);
+            const int wt = it.wt, n0 = it.n0, m0 = it.m0;
+            const bool valid = 32 * q < wt;
+            // shared address of this lane's first vector in stage 0 (explicit shared loads)
+            const uint32_t wst0 = sbase + P.w_off + 16u * static_cast<uint32_t>(32 * q + lane + part * kPartKB * wt);
+            for (int i = 0; i < niter; ++i, ++u) {
+                bool ok = warp_wait_fast(full_bar(s), sph, abort_flag, timeout_ns, status);
+                if (ok && (PERSIST ? u : i) >= a_stages)
+                    ok = warp_wait_fast(aempty_bar(a), aph ^ 1u, abort_flag, timeout_ns, status);
+                if (ok && valid) {
+                    const uint32_t wst = wst0 + static_cast<uint32_t>(s) * P.w_stage;
+                    const uint32_t sst = sst0 + static_cast<uint32_t>(s) * P.s_stage;
+                    uint32_t regs[kPartKB * 16];
+                    uint4 v[kPartKB];
+                    uint32_t sb[kPartKB], sb2[kPartKB];
 #pragma unroll
-                for (int u = 0; u < kPartKB; ++u) {
-                    v[u] = lds128(wst + 16u * static_cast<uint32_t>(u * wt));
-                    sb[u] = lds16(sst + 2u * static_cast<uint32_t>(srow[u] * wt));
-                    // NVFP4: the block's second 16-k half has the next scale row
-                    sb2[u] = FP4 ? lds16(sst + 2u * static_cast<uint32_t>((srow[u] + 1) * wt)) : sb[u];
-                }
-#pragma unroll
-                for (int u = 0; u < kPartKB; ++u) {
-                    const uint32_t s2 = sb[u] | (sb[u] << 16);
-                    if (FP4) {
-                        const uint32_t s2b = sb2[u] | (sb2[u] << 16);
-                        dequant8_nvfp4(v[u].x, s2, &regs[u * 16 + 0]);
-                        dequant8_nvfp4(v[u].y, s2, &regs[u * 16 + 4]);
-                        dequant8_nvfp4(v[u].z, s2b, &regs[u * 16 + 8]);
-                        dequant8_nvfp4(v[u].w, s2b, &regs[u * 16 + 12]);
-                    } else {
-                        dequant8(v[u].x, s2, &regs[u * 16 + 0]);
-                        dequant8(v[u].y, s2, &regs[u * 16 + 4]);
-                        dequant8(v[u].z, s2, &regs[u * 16 + 8]);
-                        dequant8(v[u].w, s2, &regs[u * 16 + 12]);
+                    for (int u = 0; u < kPartKB; ++u) {
+                        v[u] = lds128(wst + 16u * static_cast<uint32_t>(u * wt));
+                        sb[u] = lds16(sst + 2u * static_cast<uint32_t>(srow[u] * wt));
+                        // NVFP4: the block's second 16-k half has the next scale row
+                        sb2[u] = FP4 ? lds16(sst + 2u * static_cast<uint32_t>((srow[u] + 1) * wt)) : sb[u];
                     }
-                }
-                tmem_st<kPartKB * 16>(a_base + static_cast<uint32_t>(a * kACols), regs);
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            if (!GROUP_ISSUE) {
-                __syncwarp();
-                if (!ok) break;
-                if (lane == 0) mbar_arrive(afull_bar(a));
-            } else {
-            // the group's A pieces for this stage are in TMEM (or some warp gave up a wait)
-            if (!group_sync_and(1 + grp, 32 * kGroupWarps, ok)) break;
-            if (issuer && lane == 0) {
-                tc_fence_after();
-                const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
-                const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
 #pragma unroll
-                for (int t = 0; t < kGroupSteps; ++t) {
-                    const int ks = grp * kGroupSteps + t;  // k-step of 16 within the stage
-                    const uint32_t koff = static_cast<uint32_t>(((ks / 4) * MT * 128 + (ks % 4) * 32) >> 4);
-                    umma_f16_ts(d_g, a_tmem + ks * 8, dstage + koff, idesc, (i > 0) || (t > 0));
-                }
-                umma_commit(empty_bar(s));
-                umma_commit(aempty_bar(a));
-            }
-            }
-            __syncwarp();
-            if (++s == s_stages) {
-                s = 0;
-                sph ^= 1u;
-            }
-            if (++a == a_stages) {
-                a = 0;
-                aph ^= 1u;
-            }
-        }
-        if (GROUP_ISSUE && issuer && lane == 0) umma_commit(dfull_bar);
-        __syncwarp();
-
-        // ---------------- epilogue: TMEM -> registers -> y (or the split-K partial tile)
-        griddep_wait();  // y may still be read or written by the previous grid on the stream
-        const bool have_d = warp_wait(dfull_bar, 0, abort_flag, timeout_ns, status);
-        tc_fence_after();
-        if (have_d) {
-            constexpr int kPartCols = MT / kParts;  // accumulator columns (activation rows) per K part
-            constexpr int kCols = kPartCols < 8 ? kPartCols : 8;  // columns per TMEM load
-            const int mbase = part * kPartCols;
-            float* red = reinterpret_cast<float*>(smem + P.red_off);
-            const int n = n0 + 32 * q + lane;
-#pragma unroll 1
-            for (int c = 0; c < kPartCols; c += kCols) {
-                uint32_t r[kCols];
-                tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int g = 1; g < NA; ++g) {  // fixed order: D_0 + D_1 + ...
-                    uint32_t r2[kCols];
-                    tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + g * MT + mbase + c), r2);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int t = 0; t < kCols; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + __uint_as_float(r2[t]));
-                }
-                if (split == 1) {
-                    if (valid) {
-#pragma unroll
-                        for (int j = 0; j < kCols; ++j) {
-                            const int m = m0 + mbase + c + j;
-                            if (m < M && in_bounds(static_cast<int64_t>(m) * N + n < static_cast<int64_t>(M) * N, status)) {
-                                float v = __uint_as_float(r[j]) * tensor_scale;
-                                if (row_scale != nullptr) v *= row_scale[m];
-                                y[static_cast<int64_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
-                            }
+                    for (int u = 0; u < kPartKB; ++u) {
+                        const uint32_t s2 = sb[u] | (sb[u] << 16);
+                        if (FP4) {
+                            const uint32_t s2b = sb2[u] | (sb2[u] << 16);
+                            dequant8_nvfp4(v[u].x, s2, &regs[u * 16 + 0]);
+                            dequant8_nvfp4(v[u].y, s2, &regs[u * 16 + 4]);
+                            dequant8_nvfp4(v[u].z, s2b, &regs[u * 16 + 8]);
+                            dequant8_nvfp4(v[u].w, s2b, &regs[u * 16 + 12]);
+                        } else {
+                            dequant8(v[u].x, s2, &regs[u * 16 + 0]);
+                            dequant8(v[u].y, s2, &regs[u * 16 + 4]);
+                            dequant8(v[u].z, s2, &regs[u * 16 + 8]);
+                            dequant8(v[u].w, s2, &regs[u * 16 + 12]);
                         }
                     }
+                    tmem_st<kPartKB * 16>(a_base + static_cast<uint32_t>(a * kACols), regs);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                if (!GROUP_ISSUE) {
+                    __syncwarp();
+                    if (!ok) break;
+                    if (lane == 0) mbar_arrive(afull_bar(a));
                 } else {
+                // the group's A pieces for this stage are in TMEM (or some warp gave up a wait)
+                if (!group_sync_and(1 + grp, 32 * kGroupWarps, ok)) break;
+                if (issuer && lane == 0) {
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem + static_cast<uint32_t>(a * kACols);
+                    const uint64_t dstage = desc0 + static_cast<uint64_t>(s * stage_step);
 #pragma unroll
-                    for (int j = 0; j < kCols; ++j)
-                        red[(mbase + c + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
+                    for (int t = 0; t < kGroupSteps; ++t) {
+                        const int ks = grp * kGroupSteps + t;  // k-step of 16 within the stage
+                        const uint32_t koff = static_cast<uint32_t>(((ks / 4) * MT * 128 + (ks % 4) * 32) >> 4);
+                        umma_f16_ts(d_g, a_tmem + ks * 8, dstage + koff, idesc, (i > 0) || (t > 0));
+                    }
+                    umma_commit(empty_bar(s));
+                    umma_commit(aempty_bar(a));
+                }
+                }
+                __syncwarp();
+                if (++s == s_stages) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+                if (++a == a_stages) {
+                    a = 0;
+                    aph ^= 1u;
                 }
             }
+            if (GROUP_ISSUE && issuer && lane == 0) umma_commit(dfull_bar);
+            __syncwarp();
+
+            // ---------------- epilogue: TMEM -> registers -> y (or the split-K partial tile)
+            griddep_wait();  // y may still be read or written by the previous grid on the stream
+            const bool have_d = warp_wait(dfull_bar, static_cast<uint32_t>(jdone) & 1u, abort_flag, timeout_ns, status);
+            tc_fence_after();
+            if (have_d) {
+                constexpr int kPartCols = MT / kParts;  // accumulator columns (activation rows) per K part
+                constexpr int kCols = kPartCols < 8 ? kPartCols : 8;  // columns per TMEM load
+                const int mbase = part * kPartCols;
+                float* red = reinterpret_cast<float*>(smem + P.red_off);
+                const int n = n0 + 32 * q + lane;
+#pragma unroll 1
+                for (int c = 0; c < kPartCols; c += kCols) {
+                    uint32_t r[kCols];
+                    tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + mbase + c), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int g = 1; g < NA; ++g) {  // fixed order: D_0 + D_1 + ...
+                        uint32_t r2[kCols];
+                        tmem_ld<kCols>(tmem + lane_base + static_cast<uint32_t>(a_stages * kACols + g * MT + mbase + c), r2);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < kCols; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + __uint_as_float(r2[t]));
+                    }
+                    if (split == 1) {
+                        if (valid) {
+#pragma unroll
+                            for (int j = 0; j < kCols; ++j) {
+                                const int m = m0 + mbase + c + j;
+                                if (m < M && in_bounds(static_cast<int64_t>(m) * N + n < static_cast<int64_t>(M) * N, status)) {
+                                    float v = __uint_as_float(r[j]) * tensor_scale;
+                                    if (row_scale != nullptr) v *= row_scale[m];
+                                    y[static_cast<int64_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
+                                }
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j)
+                            red[(mbase + c + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            ++jdone;
+            if (!PERSIST) break;
+            // every dequantisation warp has read the accumulator before an issuer starts the next
+            // item's MMAs into it; after an abort all leave together
+            if (!group_sync_and(6, 32 * kDequantWarps, *abort_flag == 0) || rest + ncl >= item_end) break;
         }
-        tc_fence_before();
+        if (GROUP_ISSUE && warp == 0 && lane == 0) *items_committed = jdone;
+        __syncwarp();
     }
 
-    if (split > 1) {
+    if (split > 1) {  // (one work item per cluster)
+        const int m0 = it1.m0, n0 = it1.n0, wt = it1.wt;
         __syncwarp();
         griddep_wait();  // every thread of the reduction writes y
         cluster_sync_all();
@@ -510,7 +617,8 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
         // still bounded, before shared memory and TMEM are released.
         if (lane == 0) {
             int drain_abort = 0;
-            mbar_wait(dfull_bar, 0, &drain_abort, timeout_ns, status);
+            const int n = *items_committed;  // the last committed phase: n - 1
+            if (n > 0) mbar_wait(dfull_bar, static_cast<uint32_t>(n - 1) & 1u, &drain_abort, timeout_ns, status);
         }
         __syncwarp();
         tc_fence_after();
@@ -561,10 +669,20 @@ cudaLaunchConfig_t make_config(const TcConfig& c, int items, size_t smem, cudaSt
     return cfg;
 }
 
+// The kernel for a launch: the persistent form (several work items per CTA) exists for the 128-
+// and 256-row tiles, whose one-CTA-per-SM grids span several waves at large M.
+template <int MT, int KC, int NI, bool GI, int DW>
+auto tc_kernel_for(bool fp4, bool persist) {
+    if constexpr (MT >= 128) {
+        if (persist)
+            return fp4 ? tc_gemm_kernel<MT, KC, NI, GI, DW, true, true> : tc_gemm_kernel<MT, KC, NI, GI, DW, false, true>;
+    }
+    return fp4 ? tc_gemm_kernel<MT, KC, NI, GI, DW, true, false> : tc_gemm_kernel<MT, KC, NI, GI, DW, false, false>;
+}
+
 template <int MT, int KC, int NI, bool GI, int DW>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* qweight_r, const uint16_t* scales_r,
                         uint16_t* y, int M, int N, int K, int G, const TcConfig& c, const LaunchCtx& ctx) {
-    auto kern = ctx.nvfp4 ? tc_gemm_kernel<MT, KC, NI, GI, DW, true> : tc_gemm_kernel<MT, KC, NI, GI, DW, false>;
     const int items = ((N + kTileN - 1) / kTileN) * ((M + MT - 1) / MT);
     const int tail = c.tail_items;
     // the work items of the full waves, then those of the last partial wave, split further along K
@@ -573,13 +691,17 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
         if (part == 1) cp.split = c.tail_split;
         const int n = part == 0 ? items - tail : tail;
         if (n <= 0) continue;
+        const int first = part == 0 ? 0 : items - tail;
+        const bool persist = MT >= 128 && cp.split == 1 && c.persist_ctas > 0 && n > c.persist_ctas;
+        const int clusters = persist ? c.persist_ctas : n;
+        auto kern = tc_kernel_for<MT, KC, NI, GI, DW>(ctx.nvfp4 != 0, persist);
         const size_t smem = launch_smem(MT, KC, G, cp);
         cudaError_t e = prepare_kernel(kern, smem, cp.split);
         if (e != cudaSuccess) return e;
         cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(cp, n, smem, ctx.stream, attr);
+        cudaLaunchConfig_t cfg = make_config<MT, KC, NI, GI, DW>(cp, clusters, smem, ctx.stream, attr);
         e = cudaLaunchKernelEx(&cfg, kern, tmap, reinterpret_cast<const uint4*>(qweight_r), scales_r, y, M, N, K, G,
-                               cp.split, part == 0 ? 0 : items - tail, cp.stages, cp.tmem_stages, three_d ? 1 : 0,
+                               cp.split, first, first + n, cp.stages, cp.tmem_stages, three_d ? 1 : 0,
                                ctx.tensor_scale, ctx.row_scale, ctx.status, ctx.timeout_ns);
         if (e != cudaSuccess) return e;
     }
@@ -589,7 +711,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, bool three_d, const uint32_t* q
 // CTAs of this config the device keeps resident at once (clusters x cluster size), or 0.
 template <int MT, int KC, int NI, bool GI, int DW>
 int resident_ctas_t(const TcConfig& c, int G) {
-    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW, false>;  // (the NVFP4 variant has the same resources)
+    auto kern = tc_gemm_kernel<MT, KC, NI, GI, DW, false, false>;  // (the other variants: the same resources)
     const size_t smem = launch_smem(MT, KC, G, c);
     if (prepare_kernel(kern, smem, c.split) != cudaSuccess) {
         cudaGetLastError();

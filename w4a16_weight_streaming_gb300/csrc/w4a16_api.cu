@@ -450,6 +450,12 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         c.tail_items = partial_wave_items(c, M, N, G, sm_count, have_device);
         c.tail_split = c.tail_items > 0 ? p.tail_split : 0;
     }
+    // Unsplit 128- and 256-row tiles (one CTA per SM) with more work items than resident CTAs: a
+    // persistent grid, one CTA per slot taking every slots-th item, so that each CTA's copies for
+    // its next item overlap the MMAs and epilogue of the current one instead of a new wave's ramp.
+    // Measured on GB300 (5120 x 34816): M = 256 80.2 -> 77.4 us, M = 512 160.0 -> 151.3 us, M = 1024
+    // 300 -> 282 us.
+    c.persist_ctas = c.m_tile >= 128 && c.split == 1 ? resident_slots(c, G, sm_count, have_device) : 0;
     if (!tc_config_valid(c, M, N, K, G)) return W4A16_ERR_UNSUPPORTED_SHAPE;
     out->tc = c;
     return W4A16_OK;
@@ -542,6 +548,9 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
         snprintf(desc, sizeof(desc), "path=gemv M=%d N=%d K=%d group=%d split_k=%d grid=(%lld,1,1) block=128%s", M, N,
                  K, group, ch.gemv_split, ctas, fmt);
     } else {
+        const long long items = static_cast<long long>((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile);
+        const long long main_items = items - ch.tc.tail_items;
+        const bool persistent = ch.tc.split == 1 && ch.tc.persist_ctas > 0 && main_items > ch.tc.persist_ctas;
         char tail[80] = "";
         if (ch.tc.tail_items > 0)
             snprintf(tail, sizeof(tail), " tail_items=%d tail_split=%d tail_grid=(%lld,1,1)", ch.tc.tail_items,
@@ -550,13 +559,11 @@ int launch_gemm(const Choice& ch, const uint16_t* x, const void* qweight_r, cons
                       group, ch.tc, ctx);
         snprintf(desc, sizeof(desc),
                  "path=tc M=%d N=%d K=%d group=%d m_tile=%d k_chunk=%d stages=%d tmem_stages=%d issuers=%d "
-                 "dequant_warps=%d split_k=%d grid=(%lld,1,1)%s tmem_cols=%d smem=%zu%s",
+                 "dequant_warps=%d split_k=%d grid=(%lld,1,1)%s%s tmem_cols=%d smem=%zu%s",
                  M, N, K, group, ch.tc.m_tile, ch.tc.k_chunk, ch.tc.stages, ch.tc.tmem_stages, ch.tc.issuers,
                  ch.tc.dequant_warps, ch.tc.split,
-                 static_cast<long long>(ch.tc.split) *
-                     (static_cast<long long>((N + 127) / 128) * ((M + ch.tc.m_tile - 1) / ch.tc.m_tile) -
-                      ch.tc.tail_items),
-                 tail, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), fmt);
+                 persistent ? static_cast<long long>(ch.tc.persist_ctas) : ch.tc.split * main_items,
+                 persistent ? " persistent" : "", tail, tc_tmem_cols(ch.tc), tc_smem_bytes(ch.tc, group), fmt);
     }
     {
         std::lock_guard<std::mutex> lock(g_mu);
