@@ -127,7 +127,9 @@ int w4a16_unrepack(const void* qweight_r, const void* scales_r, int32_t* qweight
  *   scales_r:  repacked scales from w4a16_repack, device
  *   y:         fp16 [M][N] row-major, device, written in full (every element)
  * The dispatcher picks the kernel family and launch plan from (M, N, K, group); w4a16_last_dispatch
- * reports what ran. Accuracy: every element is within 2^-10*|y_exact| + 2^-10*sum_k|x*w| of the
+ * reports what ran. A call is one kernel launch on `stream`, or two when the tile plan splits off the
+ * last, partial wave of work items (w4a16_plan.tail_split); unsplit 128- and 256-row tile launches
+ * with more work items than resident CTAs run one CTA per SM over several items. Accuracy: every element is within 2^-10*|y_exact| + 2^-10*sum_k|x*w| of the
  * exact result (fp32 accumulation chains are kept short enough for that bound).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA (launch refused).
  */
@@ -135,7 +137,8 @@ int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, u
                int group, void* stream);
 
 /* As w4a16_gemm with an explicit plan (NULL or zero fields = automatic). An invalid plan
- * (e.g. GEMV with M > 8, split_k larger than the K chunks) returns UNSUPPORTED_SHAPE. */
+ * (e.g. GEMV with M > 8, split_k larger than the K chunks) returns UNSUPPORTED_SHAPE; a tail_split
+ * outside {0, 2..16}, or with split_k > 1, INVALID_ARG. */
 int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                   int group, const w4a16_plan* plan, void* stream);
 
