@@ -15,7 +15,7 @@ bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on t
 L2: every weight matrix exists in R device copies and consecutive uses of one copy are at least 4 x
 L2 bytes of other weights apart, so no launch finds its weights in L2. `e2e` repeats steps through
 w4a16_gemm_host with host buffers (x copied in from pinned host memory, y copied back, every GEMM of
-the step, the independent GEMMs spread over three streams). More objects, outside the timed step:
+the step, the independent GEMMs spread over eight streams). More objects, outside the timed step:
 `decode_step_chain` (64 dense layers in one CUDA graph per decode step, at B = 1 .. 64 streams),
 `nvfp4` (the same four matrices with NVFP4 weights at M = 1, 16, 256, and their chain) and `w4a8`
 (the same int4 weights with int8 activations at M = 1, 8, 16, 256, the quantisation timed beside
@@ -472,7 +472,8 @@ def measure_layer_chain(W, dev, sources, peaks, timed, capture, layers=CHAIN_LAY
 
 
 NVFP4_M = [1, 16, 256]
-E2E_STREAMS = 3  # streams the end-to-end step spreads its independent GEMMs over
+E2E_STREAMS = 8  # streams the end-to-end step spreads its independent GEMMs over (measured: 3 -> 775,
+#                 4 -> 837, 6 -> 912, 8 -> 933 GB/s)
 
 
 def nvfp4_weight_bytes(K: int, N: int) -> int:
@@ -619,6 +620,8 @@ def main():
     ap.add_argument("--workload", choices=["sweep"] + sorted(WORKLOADS), default="sweep")
     ap.add_argument("--launches", type=int, default=200, help="per-row launches for median / p10 / p90")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-streams", type=int, default=E2E_STREAMS,
+                    help="streams the end-to-end step spreads its independent GEMMs over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--table", action="store_true", help="also print the per-row table to stderr")
@@ -827,13 +830,13 @@ def main():
     # stream before and after every step.
     h2d = sum(it["xd"].numel() * 2 for it in items)
     d2h = sum(it["yd"].numel() * 2 for it in items)
-    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
+    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(max(1, args.e2e_streams))]
     calls = []
     for i, it in enumerate(items):
         qr, sr = mats[it["name"]]["copies"][it["copy"]]
         calls.append((it["x_host"].data_ptr(), it["xd"].data_ptr(), qr.data_ptr(), sr.data_ptr(),
                       it["yd"].data_ptr(), it["y_host"].data_ptr(), it["M"], it["N"], it["K"], GROUP,
-                      e2e_streams[i % E2E_STREAMS].cuda_stream))
+                      e2e_streams[i % len(e2e_streams)].cuda_stream))
 
     def e2e_step():
         cur = torch.cuda.current_stream()
@@ -851,7 +854,7 @@ def main():
     ne = max(1, args.e2e_steps)
     e2e_ms = dist_max(dist, timed(e2e_step, ne), dev) / ne
     e2e = {"value": world * step_wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": ne, "streams": E2E_STREAMS}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": ne, "streams": len(e2e_streams)}
     st = W.w4a16_device_status()
     if st != W.OK:
         raise RuntimeError(f"device status after the end-to-end steps: {W.status_string(st)}")
