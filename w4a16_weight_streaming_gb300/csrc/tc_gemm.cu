@@ -31,7 +31,9 @@
 //     group's first warp issues the group's k-steps itself. (Measured on GB300: the 256-row tile is
 //     faster grouped, 81 against 86 us on 5120 x 34816 at M = 256; the 128-row tile is faster with
 //     dedicated issuers, 57 against 63 us at M = 128.)
-// Barriers: full[s] (TMA bytes landed) -> A in TMEM -> MMAs -> tcgen05.commit by each issuer ->
+// Barriers: full[s] (TMA bytes landed; with dedicated issuers the x tile completes its own xfull[s],
+// which only the issuers wait for, so that the dequantisation starts once the weights are in) ->
+// A in TMEM -> MMAs -> tcgen05.commit by each issuer ->
 // empty[s] (shared stage free; producer) and aempty[a] (TMEM A stage free; dequant warps). Every
 // mbarrier wait is bounded; grouped warps leave their loop only through a barrier reduction, so a
 // group leaves together.
@@ -69,7 +71,7 @@ struct SmemPlan {
     uint32_t w_off, w_stage;  // packed weights: s_stages x (128 * KC / 2)
     uint32_t s_off, s_stage;  // scales: s_stages x (ngs * 128 * 2)
     uint32_t red_off;         // split-K partial tile, MT * 128 * 4 (may overlap the x tiles)
-    uint32_t bar_off;         // 2 * s_stages + 2 * a_stages + 1 mbarriers
+    uint32_t bar_off;         // 3 * s_stages + 2 * a_stages + 1 mbarriers
     uint32_t misc_off;        // tmem address slot, abort flag, two issuer go flags
     uint32_t total;           // bytes from the 1024-aligned base
 };
@@ -93,7 +95,7 @@ __host__ __device__ inline SmemPlan make_plan(int MT, int KC, int s_stages, int 
         p.red_off = 0;
     }
     p.bar_off = (end + 7u) & ~7u;
-    p.misc_off = p.bar_off + (2 * s_stages + 2 * a_stages + 1) * 8;
+    p.misc_off = p.bar_off + (3 * s_stages + 2 * a_stages + 1) * 8;
     p.total = p.misc_off + 20;
     return p;
 }
@@ -177,6 +179,11 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a); };
     auto afull_bar = [&](int a) { return bar0 + 8u * (2 * s_stages + a_stages + a); };  // dedicated scheme
     const uint32_t dfull_bar = bar0 + 8u * (2 * s_stages + 2 * a_stages);
+    // The x tile's own barrier (dedicated issuers: the dequantisation warps wait only for the weights
+    // and scales, the issuers for x); the grouped scheme, whose issuing warp also dequantises, keeps
+    // one barrier for all three copies.
+    auto xfull_bar = [&](int s) { return GROUP_ISSUE ? full_bar(s) : bar0 + 8u * (2 * s_stages + 2 * a_stages + 1 + s); };
+    constexpr uint32_t kXBytes = static_cast<uint32_t>(MT * KC * 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.misc_off + 4);
 
@@ -186,7 +193,8 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < s_stages; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), 1);  // weights and scales (and, grouped scheme, x) landed
+            if (!GROUP_ISSUE) mbar_init(xfull_bar(s), 1);
             mbar_init(empty_bar(s), NA);  // one commit per accumulator group
         }
         for (int a = 0; a < a_stages; ++a) {
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                 const int wt = it1.wt, m0 = it1.m0;
                 const uint32_t wbytes = static_cast<uint32_t>(kKB * wt * 16);
                 const uint32_t sbytes = static_cast<uint32_t>(ngs * wt * 2);
-                const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
+                const uint32_t bytes = wbytes + sbytes + (GROUP_ISSUE ? kXBytes : 0u);
                 auto issue_w = [&](int i) {  // weights and scales of stage use i (no dependence on x)
                     const int s = i % s_stages;
                     const int k0 = (c_begin + i) * KC;
@@ -273,12 +281,13 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                     const int k0 = (c_begin + i) * KC;
                     in_bounds(k0 + KC <= K && m0 < M, status);  // rows >= M of the box are zero-filled by the copy
                     const uint32_t xs = sbase + P.x_off + s * P.x_stage;
+                    if (!GROUP_ISSUE) mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
                     if (x_3d) {
-                        tma_load_x_3d(xs, &tmap_x, k0, m0, full_bar(s));
+                        tma_load_x_3d(xs, &tmap_x, k0, m0, xfull_bar(s));
                     } else {
 #pragma unroll
                         for (int a = 0; a < KC / 64; ++a)
-                            tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, full_bar(s));
+                            tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, m0, xfull_bar(s));
                     }
                 };
                 // Programmatic dependent launch: the first ring fill of weights goes out before the
@@ -304,7 +313,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                     const uint16_t* s_tile = sr + static_cast<int64_t>(it.tile) * kTileN * NG;  // [K/G][wt]
                     const uint32_t wbytes = static_cast<uint32_t>(kKB * it.wt * 16);
                     const uint32_t sbytes = static_cast<uint32_t>(ngs * it.wt * 2);
-                    const uint32_t bytes = wbytes + sbytes + static_cast<uint32_t>(MT * KC * 2);
+                        const uint32_t bytes = wbytes + sbytes + (GROUP_ISSUE ? kXBytes : 0u);
                     auto issue_w = [&](int i, int u) {  // weights and scales of stage i, ring use u (no x)
                         const int s = u % s_stages;
                         const int k0 = (c_begin + i) * KC;
@@ -322,12 +331,13 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                         const int k0 = (c_begin + i) * KC;
                         in_bounds(k0 + KC <= K && it.m0 < M, status);  // rows >= M of the box are zero-filled
                         const uint32_t xs = sbase + P.x_off + s * P.x_stage;
+                        if (!GROUP_ISSUE) mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
                         if (x_3d) {
-                            tma_load_x_3d(xs, &tmap_x, k0, it.m0, full_bar(s));
+                            tma_load_x_3d(xs, &tmap_x, k0, it.m0, xfull_bar(s));
                         } else {
 #pragma unroll
                             for (int a = 0; a < KC / 64; ++a)
-                                tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, it.m0, full_bar(s));
+                                tma_load_2d(xs + a * MT * 128, &tmap_x, k0 + 64 * a, it.m0, xfull_bar(s));
                         }
                     };
                     int i = 0;
@@ -355,9 +365,13 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
             griddep_launch_dependents();
             // Let the copies still in flight land before shared memory can be released.
             int dummy_abort = 0;
-            for (int i = issued > s_stages ? issued - s_stages : 0; i < issued; ++i)  // (only after the loop)
+            for (int i = issued > s_stages ? issued - s_stages : 0; i < issued; ++i) {  // (only after the loop)
                 mbar_wait(full_bar(i % s_stages), static_cast<uint32_t>(i / s_stages) & 1u, &dummy_abort, timeout_ns,
                           status);
+                if (!GROUP_ISSUE)
+                    mbar_wait(xfull_bar(i % s_stages), static_cast<uint32_t>(i / s_stages) & 1u, &dummy_abort,
+                              timeout_ns, status);
+            }
         }
         __syncwarp();
     } else if (!GROUP_ISSUE && warp >= kIssuerWarp0) {
@@ -380,7 +394,7 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
                 const int gu = PERSIST ? u : i;  // this stage's use of the ring, over all items
                 if (j == 0 && lane == 0)
                     go[gu & 1] = (mbar_spin(afull_bar(a), aph, abort_flag, timeout_ns, status) &&
-                                 mbar_spin(full_bar(s), sph, abort_flag, timeout_ns, status))
+                                 mbar_spin(xfull_bar(s), sph, abort_flag, timeout_ns, status))
                                     ? 1
                                     : 0;
                 if (NA > 1) asm volatile("bar.sync 5, %0;" ::"n"(32 * NA) : "memory");
