@@ -110,3 +110,25 @@ def test_persistent_grid_and_tail_run_clean(W, D, plan):
     y_norm = W.gemm(x, *W.repack(qw, sc, G), N, K, G, plan=plan)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y_norm.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,split", [(1, 1), (2, 3)])
+def test_gemv_batch_depth_runs_clean(W, D, M, split):
+    """The GEMV with 8 blocks in flight per warp (one or two rows) through the index-checking build."""
+    K, N, G = 1280, 352, 128
+    d = inputs.generate(M, K, N, G, seed=730 + M)
+    y_ref, abs_ref = oracle.gemm(d["x"], d["qweight"], d["scales"], G)
+    x, qw, sc = to_dev(d)
+    qw_r = torch.empty(N * K // 8, dtype=torch.int32, device="cuda")
+    sc_r = torch.empty((K // G) * N, dtype=torch.int16, device="cuda")
+    assert D.w4a16_repack(qw.data_ptr(), sc.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), N, K, G, _stream()) == 0
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    p = W.Plan(path=1, split_k=split)
+    assert D.w4a16_gemm_ex(x.data_ptr(), qw_r.data_ptr(), sc_r.data_ptr(), y.data_ptr(), M, N, K, G,
+                           ctypes.byref(p), _stream()) == 0
+    torch.cuda.synchronize()
+    assert _status(D) == W.OK
+    what = ctypes.create_string_buffer(512)
+    D.w4a16_last_dispatch(what, 512)
+    assert b"unroll=8" in what.value, what.value
+    assert_parity(y_f64(y), y_ref, abs_ref, f"debug-bounds build GEMV M={M} split {split}")

@@ -422,3 +422,28 @@ def test_persistent_grid_every_element(W, M, K, N, plan):
     # deterministic: the same plan again gives the same bits
     y2 = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), what
+
+
+# ------------------------------------------------------------------------------ GEMV batch depth
+# At one and two rows the GEMV keeps 8 blocks of 32 k in flight per warp (instead of 4) when its
+# grid fits in one wave of that larger-register kernel.
+@pytest.mark.parametrize("M,K,N,G,plan,deep", [
+    (1, 5120, 5120, 128, None, True), (2, 5120, 5120, 128, None, True), (1, 17408, 5120, 128, None, True),
+    (1, 5120, 7168, 128, None, False),                                 # 896 CTAs: two waves, stays at 4
+    (1, 1088, 5120, 64, dict(path=1, split_k=1), True), (2, 1088, 5120, 32, dict(path=1, split_k=3), True),
+    (1, 5120, 5120, 128, dict(path=1, split_k=16), False),             # 2560 CTAs
+])
+def test_gemv_batch_depth_every_element(W, M, K, N, G, plan, deep):
+    d, y_ref, abs_ref = _case(M, K, N, G, seed=M + K + N)
+    x, qw_r, sc_r = _repacked(W, d, G)
+    y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
+    what = W.w4a16_last_dispatch()
+    assert what.startswith("path=gemv") and ("unroll=8" in what) == deep, what
+    assert_parity(y_f64(y), y_ref, abs_ref, what)
+    if deep:  # one-hot rows stay exact through the deeper batches
+        xb = np.zeros((M, K), np.uint16)
+        for m in range(M):
+            xb[m, (37 * m + 5) % K] = 0x3C00
+        y1 = run_gemm(W, x_to_dev(xb), qw_r, sc_r, N, K, G, plan=plan)
+        yo, _ = oracle.gemm(xb, d["qweight"], d["scales"], G)
+        assert np.array_equal(y1.cpu().numpy().view(np.uint16), yo.astype(np.float16).view(np.uint16)), what

@@ -182,3 +182,16 @@ def test_debug_bounds_build_runs_clean(W, plan):
     torch.cuda.synchronize()
     assert D.w4a16_device_status(s) == 0
     assert_parity(y_f64(y), y_ref, a_ref, "debug-bounds build")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_gemv_batch_depth(W, M):
+    """NVFP4 through the GEMV with 8 blocks in flight per warp (a one-wave grid at M <= 2)."""
+    K, N = 5120, 5120
+    qw, s8, g, x = _case(M, K, N, seed=950 + M)
+    r = _dev_weights(W, qw, s8)
+    y = _run(W, x, r, g, N, K)
+    what = W.w4a16_last_dispatch()
+    assert what.startswith("path=gemv") and "unroll=8" in what, what
+    y_ref, a_ref = oracle.gemm_nvfp4(x, qw, s8, g)
+    assert_parity(y_f64(y), y_ref, a_ref, what)

@@ -17,7 +17,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kUnroll = 4;  // 32-k blocks in flight per warp
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
     uint4 v;
@@ -122,7 +121,9 @@ __device__ __forceinline__ void gemv_block(const uint4 v, uint32_t sbits, const 
     }
 }
 
-template <int MR, bool FP4>
+// U: 32-k blocks in flight per warp: 4, or 8 at one and two rows when the grid fits in one wave of
+// the larger-register kernel (fewer load round trips for short K-slices).
+template <int MR, bool FP4, int U>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restrict__ x,
                                                         const uint4* __restrict__ wr,
                                                         const uint16_t* __restrict__ sr, uint16_t* __restrict__ y,
@@ -178,11 +179,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
     // Programmatic dependent launch: the warp's first batch of weights and scales is loaded while the
     // previous grid on the stream finishes; x (possibly its output) is read only after it completed.
     int kb = sl.kb_begin + warp;
-    const bool first = kb + kWarps * (kUnroll - 1) < sl.kb_end;
-    uint4 v0[kUnroll];
-    uint32_t s0[kUnroll];
+    const bool first = kb + kWarps * (U - 1) < sl.kb_end;
+    uint4 v0[U];
+    uint32_t s0[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         v0[u] = first ? load_w(kb + kWarps * u) : make_uint4(0u, 0u, 0u, 0u);
         s0[u] = first ? load_s(kb + kWarps * u) : 0u;
     }
@@ -211,38 +212,38 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 
     if (first) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int b = kb + kWarps * u;
             gemv_block<MR, FP4>(v0[u], s0[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
         }
-        kb += kWarps * kUnroll;
+        kb += kWarps * U;
     }
-    for (; kb + kWarps * (kUnroll - 1) < sl.kb_end; kb += kWarps * kUnroll) {
-        uint4 v[kUnroll];
-        uint32_t sb[kUnroll];
+    for (; kb + kWarps * (U - 1) < sl.kb_end; kb += kWarps * U) {
+        uint4 v[U];
+        uint32_t sb[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int b = kb + kWarps * u;
             v[u] = load_w(b);
             sb[u] = load_s(b);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int b = kb + kWarps * u;
             gemv_block<MR, FP4>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
         }
     }
-    if (kb < sl.kb_end) {  // the last (< kUnroll) blocks: their loads issued together as well
-        uint4 v[kUnroll];
-        uint32_t sb[kUnroll];
+    if (kb < sl.kb_end) {  // the last (< U) blocks: their loads issued together as well
+        uint4 v[U];
+        uint32_t sb[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int b = kb + kWarps * u;
             v[u] = b < sl.kb_end ? load_w(b) : make_uint4(0u, 0u, 0u, 0u);
             sb[u] = b < sl.kb_end ? load_s(b) : 0u;
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int b = kb + kWarps * u;
             if (b < sl.kb_end) gemv_block<MR, FP4>(v[u], sb[u], xs + (b - sl.kb_begin) * 32, sl.klen, acc);
         }
@@ -286,11 +287,19 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint16_t* __restri
 }
 
 template <int MR>
+auto gemv_kernel_for(bool fp4, int unroll) {
+    if constexpr (MR <= 2) {
+        if (unroll == 8) return fp4 ? gemv_kernel<MR, true, 8> : gemv_kernel<MR, false, 8>;
+    }
+    return fp4 ? gemv_kernel<MR, true, 4> : gemv_kernel<MR, false, 4>;
+}
+
+template <int MR>
 cudaError_t launch_gemv_m(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y,
-                          int N, int K, int G, int split, size_t smem, const LaunchCtx& ctx) {
+                          int N, int K, int G, int split, int unroll, size_t smem, const LaunchCtx& ctx) {
     const cudaStream_t s = ctx.stream;
     unsigned* status = ctx.status;
-    auto kern = ctx.nvfp4 ? gemv_kernel<MR, true> : gemv_kernel<MR, false>;
+    auto kern = gemv_kernel_for<MR>(ctx.nvfp4 != 0, unroll);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (split > 8) {
@@ -329,18 +338,41 @@ size_t gemv_smem_bytes(int M, int N, int K, int split) {
     return static_cast<size_t>(M) * klen_max * 2 + static_cast<size_t>(kWarps + 1) * M * 32 * 4;
 }
 
+// CTAs of the M-row GEMV with `unroll` blocks in flight that the device keeps resident at once
+// (both weight formats; the smaller of the two), 0 if the query fails.
+int gemv_resident_ctas(int M, int unroll, size_t smem, int sm_count) {
+    if (M != 1 && M != 2) return 0;
+    int best = -1;
+    for (int f = 0; f < 2; ++f) {
+        const void* kern = M == 1 ? reinterpret_cast<const void*>(gemv_kernel_for<1>(f != 0, unroll))
+                                  : reinterpret_cast<const void*>(gemv_kernel_for<2>(f != 0, unroll));
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        int blocks = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        best = best < 0 || blocks < best ? blocks : best;
+    }
+    return best < 0 ? 0 : best * sm_count;
+}
+
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
-                        int N, int K, int G, int split, const LaunchCtx& ctx) {
+                        int N, int K, int G, int split, int unroll, const LaunchCtx& ctx) {
     const size_t smem = gemv_smem_bytes(M, N, K, split);
     switch (M) {
-        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
-        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, smem, ctx);
+        case 1: return launch_gemv_m<1>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 2: return launch_gemv_m<2>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 3: return launch_gemv_m<3>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 4: return launch_gemv_m<4>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 5: return launch_gemv_m<5>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 6: return launch_gemv_m<6>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 7: return launch_gemv_m<7>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
+        case 8: return launch_gemv_m<8>(x, qweight_r, scales_r, y, N, K, G, split, unroll, smem, ctx);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -39,8 +39,11 @@ cudaError_t launch_unrepack_nvfp4(const uint32_t* qweight_r, const uint16_t* sca
 // ---- gemv.cu: CUDA-core split-K GEMV, M <= 8.
 constexpr int kGemvMaxM = 8;
 size_t gemv_smem_bytes(int M, int N, int K, int split);
+// unroll: 32-k blocks in flight per warp, 4 (any M) or 8 (M <= 2).
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qweight_r, const uint16_t* scales_r, uint16_t* y, int M,
-                        int N, int K, int G, int split, const LaunchCtx& ctx);
+                        int N, int K, int G, int split, int unroll, const LaunchCtx& ctx);
+// CTAs of the M-row GEMV (M <= 2) with `unroll` blocks in flight resident at once, 0 if unknown.
+int gemv_resident_ctas(int M, int unroll, size_t smem, int sm_count);
 
 // ---- tc_gemm.cu: the x operand's tensor map. x viewed as
 // [K/64 blocks][M rows][64 k]; one box = one stage tile [KC/64][MT][64] in the MMA's 128-byte-swizzle
