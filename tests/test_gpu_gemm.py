@@ -429,7 +429,9 @@ def test_persistent_grid_every_element(W, M, K, N, plan):
 # grid fits in one wave of that larger-register kernel.
 @pytest.mark.parametrize("M,K,N,G,plan,deep", [
     (1, 5120, 5120, 128, None, True), (2, 5120, 5120, 128, None, True), (1, 17408, 5120, 128, None, True),
-    (1, 5120, 7168, 128, None, False),                                 # 896 CTAs: two waves, stays at 4
+    (1, 5120, 7168, 128, None, True),                                  # split 4 -> 3: 672 CTAs, one wave
+    (2, 5120, 7168, 128, None, False),                                 # 896 CTAs: two waves, stays at 4
+    (1, 5120, 34816, 128, None, False),                                # 2176 CTAs
     (1, 1088, 5120, 64, dict(path=1, split_k=1), True), (2, 1088, 5120, 32, dict(path=1, split_k=3), True),
     (1, 5120, 5120, 128, dict(path=1, split_k=16), False),             # 2560 CTAs
 ])
@@ -439,6 +441,8 @@ def test_gemv_batch_depth_every_element(W, M, K, N, G, plan, deep):
     y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=plan)
     what = W.w4a16_last_dispatch()
     assert what.startswith("path=gemv") and ("unroll=8" in what) == deep, what
+    if plan is None and (M, N) == (1, 7168):
+        assert "split_k=3" in what, what
     assert_parity(y_f64(y), y_ref, abs_ref, what)
     if deep:  # one-hot rows stay exact through the deeper batches
         xb = np.zeros((M, K), np.uint16)

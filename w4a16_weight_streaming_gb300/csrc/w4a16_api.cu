@@ -421,10 +421,25 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         // K-slices take fewer load round trips. Measured on GB300 at M = 1: 5120 x 5120 (640 CTAs)
         // 7.78 -> 7.30 us, 17408 x 5120 (640) 17.33 -> 16.78 us, at M = 2 5120 x 5120 9.3 -> 8.9 us;
         // 5120 x 7168 (896 CTAs, two waves) 8.70 -> 11.29 us, which therefore keeps 4.
+        // At one row with an automatic split, a smaller split whose grid fits that wave is taken when
+        // there is one above 2 (5120 x 7168: split 4, 896 CTAs, 8.69 us -> split 3, 672 CTAs, 8.28 us).
         if (!w4a8 && M <= 2) {
-            const int64_t ctas = static_cast<int64_t>(split) * (N / 32);
+            const int64_t slices = N / 32;
             const int slots = have_device ? gemv_resident_ctas(M, 8, smem, sm_count) : 5 * sm_count;
-            if (slots > 0 && ctas <= slots) out->gemv_unroll = 8;
+            if (slots > 0 && split * slices <= slots) {
+                out->gemv_unroll = 8;
+            } else if (slots > 0 && M == 1 && p.split_k <= 0) {
+                for (int s = split - 1; s > 2; --s) {
+                    if (s * slices > slots) continue;
+                    const size_t smem_s = gemv_smem_bytes(M, N, K, s);
+                    const int slots_s = have_device ? gemv_resident_ctas(M, 8, smem_s, sm_count) : 5 * sm_count;
+                    if (smem_s <= kGemvMaxSmem && slots_s > 0 && s * slices <= slots_s) {
+                        out->gemv_split = s;
+                        out->gemv_unroll = 8;
+                    }
+                    break;
+                }
+            }
         }
         return W4A16_OK;
     }
