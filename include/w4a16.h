@@ -71,11 +71,12 @@ typedef struct {
     int mma_issuers; /* TC: threads issuing tensor-core MMAs, each with its own accumulator: 1, 2, 4 */
     int clusters;    /* reserved, must be 0 */
     int dequant_warps; /* TC: 16, or 8 (m_tile <= 64, k_chunk 128: half-size CTAs, two per SM) */
-    int tail_split;  /* TC, with split_k 1 (or 0): when the work items (128 output columns x m_tile
-                        rows) do not fill whole waves of resident CTAs, the items of the last,
-                        partial wave run as a second launch on the same stream, each split this many
-                        ways along K (2..16). 0: none in an explicit plan, the dispatcher's choice in
-                        an automatic one (all fields 0); other values: W4A16_ERR_INVALID_ARG. */
+    int tail_split;  /* TC: when the work items (128 output columns x m_tile rows), split_k CTAs
+                        each (0 taken as 1), do not fill whole waves of resident CTAs, the items of
+                        the last, partial wave run as a second launch on the same stream, each split
+                        this many ways along K (2..16). 0: none in an explicit plan, the dispatcher's
+                        choice in an automatic one (all fields 0); other values:
+                        W4A16_ERR_INVALID_ARG. */
 } w4a16_plan;
 
 /* Library version: major*10000 + minor*100 + patch. */
@@ -138,7 +139,7 @@ int w4a16_gemm(const uint16_t* x, const void* qweight_r, const void* scales_r, u
 
 /* As w4a16_gemm with an explicit plan (NULL or zero fields = automatic). An invalid plan
  * (e.g. GEMV with M > 8, split_k larger than the K chunks) returns UNSUPPORTED_SHAPE; a tail_split
- * outside {0, 2..16}, or with split_k > 1, INVALID_ARG. */
+ * outside {0, 2..16}, INVALID_ARG. */
 int w4a16_gemm_ex(const uint16_t* x, const void* qweight_r, const void* scales_r, uint16_t* y, int M, int N, int K,
                   int group, const w4a16_plan* plan, void* stream);
 

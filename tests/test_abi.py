@@ -216,6 +216,8 @@ def test_partial_wave_tail_plans(W):
         assert p.path == W.PATH_TC and p.m_tile == 256 and p.split_k == 1 and 2 <= p.tail_split <= 16, (N, K)
         assert p.tail_split <= K // p.k_chunk
     assert W.w4a16_plan_for(1000, 5088, 5120, 128).tail_split > 0  # ragged rows and last column tile
+    p = W.w4a16_plan_for(512, 5120, 17408, 128)  # 80 items: split whole waves are for explicit plans only
+    assert (p.split_k, p.tail_split) == (3, 0), (p.split_k, p.tail_split)
     assert W.w4a16_plan_for(512, 34816, 5120, 128).tail_split == 0  # 88 left over: no one-wave tail
     assert W.w4a16_plan_for(256, 5120, 5120, 128).tail_split == 0  # 40 items: one partial wave, split_k
     assert W.w4a16_plan_for(16, 34816, 5120, 128).tail_split == 0  # small tiles: not this rule
@@ -232,7 +234,7 @@ def test_tail_split_in_explicit_plans(W):
     assert _plan_in_subprocess("path=2,tail_split=1", shape, f) == ["error", "1"]
     assert _plan_in_subprocess("path=2,tail_split=17", shape, f) == ["error", "1"]
     assert _plan_in_subprocess("path=2,tail_split=-2", shape, f) == ["error", "1"]
-    assert _plan_in_subprocess("path=2,split_k=2,tail_split=4", shape, f) == ["error", "1"]
+    assert _plan_in_subprocess("path=2,split_k=2,tail_split=4", shape, f) == ["2", "2", "4"]  # 76 items a wave
     # one partial wave only (40 items): nothing to split off, the plan stays one unsplit launch
     assert _plan_in_subprocess("path=2,m_tile=256,tail_split=4", (256, 5120, 5120, 128), f) == ["2", "1", "0"]
     # a tail split above the stage count of K

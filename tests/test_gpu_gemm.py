@@ -346,21 +346,22 @@ def test_partial_wave_tail_sampled(W, M, K, N):
     assert_parity(y[ms, ns], y_ref, abs_ref, what)
 
 
-@pytest.mark.parametrize("M,K,N,tails", [(200, 256, 19552, (2,)), (300, 1024, 10112, (2, 3, 8)),
-                                         (129, 512, 19584, (4,))])
-def test_partial_wave_tail_every_element(W, M, K, N, tails):
+@pytest.mark.parametrize("M,K,N,split,tails", [(200, 256, 19552, 1, (2,)), (300, 1024, 10112, 1, (2, 3, 8)),
+                                               (129, 512, 19584, 1, (4,)), (200, 512, 19552, 2, (4,))])
+def test_partial_wave_tail_every_element(W, M, K, N, split, tails):
     """Explicit tail plans on shapes the oracle multiplies in full: 153 or 158 work items (one or
-    six in the tail), ragged rows, a 96-column last tile, tail splits 2-8 up to K's stage count."""
+    six in the tail), ragged rows, a 96-column last tile, tail splits 2-8 up to K's stage count, the
+    whole waves unsplit or split 2 ways."""
     G = inputs.GROUP
     d, y_ref, abs_ref = _case(M, K, N, G, seed=M + N)
     x, qw_r, sc_r = _repacked(W, d, G)
     for t in tails:
-        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=256, split_k=1, tail_split=t))
+        y = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=256, split_k=split, tail_split=t))
         what = W.w4a16_last_dispatch()
-        assert f"tail_split={t}" in what, what
+        assert f"split_k={split} " in what and f"tail_split={t}" in what, what
         assert_parity(y_f64(y), y_ref, abs_ref, what)
-        # the same product in one unsplit launch: bit-identical on the column tiles before the tail
-        y1 = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=256, split_k=1))
+        # the same product in one launch: bit-identical on the column tiles before the tail
+        y1 = run_gemm(W, x, qw_r, sc_r, N, K, G, plan=dict(path=2, m_tile=256, split_k=split))
         mtiles, items = -(-M // 256), -(-N // 128) * -(-M // 256)
         first_tail_col = 128 * ((items - int(what.split("tail_items=")[1].split()[0])) // mtiles)
         assert torch.equal(y[:, :first_tail_col], y1[:, :first_tail_col]), what

@@ -825,9 +825,9 @@ bool tc_config_valid(const TcConfig& c, int M, int N, int K, int G) {
     const SmemPlan P = make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.split);
     if (P.total + 1024 > 232448) return false;
     if (c.tail_items < 0) return false;
-    if (c.tail_items > 0) {  // a second launch: split 1 before it, 2..16 in it
+    if (c.tail_items > 0) {  // a second launch for the last partial wave's items, split 2..16 ways
         const int64_t items = static_cast<int64_t>((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
-        if (c.split != 1 || c.tail_items >= items) return false;
+        if (c.tail_items >= items) return false;
         if (c.tail_split < 2 || c.tail_split > 16 || c.tail_split > K / c.k_chunk) return false;
         if (static_cast<int64_t>(c.tail_split) * c.tail_items > 0x7fffffffLL) return false;
         if (make_plan(c.m_tile, c.k_chunk, c.stages, c.tmem_stages, G, c.tail_split).total + 1024 > 232448)

@@ -207,12 +207,11 @@ int pick_split(const TcConfig& base, int M, int N, int K, int G, int sm_count, b
 // Work items (column tile x row tile) of the last, partial wave when config c runs unsplit; 0 when
 // the items fill whole waves or fit in one.
 int partial_wave_items(const TcConfig& c, int M, int N, int G, int sm_count, bool have_device) {
-    TcConfig c1 = c;
-    c1.split = 1;
-    c1.tail_items = c1.tail_split = 0;
+    TcConfig cw = c;  // the whole waves run at c.split (clusters of c.split CTAs per item)
+    cw.tail_items = cw.tail_split = 0;
     const int items = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
-    const int slots = resident_slots(c1, G, sm_count, have_device);
-    return slots <= 0 || items <= slots ? 0 : items % slots;
+    const int per_wave = resident_slots(cw, G, sm_count, have_device) / c.split;
+    return per_wave <= 0 || items <= per_wave ? 0 : items % per_wave;
 }
 
 // Whole waves of unsplit work items, then a second launch for the items of the last, partial wave,
@@ -221,32 +220,40 @@ int partial_wave_items(const TcConfig& c, int M, int N, int G, int sm_count, boo
 // 79.2 -> 56.6 us, 17408 x 5120 194.7 -> 144.5 us, 5120 x 7168 79.9 -> 67.7 us, 5120 x 34816
 // 323.7 -> 304 us; the model's splits were within 3 % of the best forced one.
 void pick_tail(TcConfig& c, int M, int N, int K, int G, int sm_count, bool have_device) {
-    const int r = partial_wave_items(c, M, N, G, sm_count, have_device);
-    if (r <= 0) return;
     const int items = ((N + 127) / 128) * ((M + c.m_tile - 1) / c.m_tile);
     const int C = K / c.k_chunk;
-    TcConfig c1 = c;
-    c1.split = 1;
-    const int slots1 = resident_slots(c1, G, sm_count, have_device);
-    const int full_waves = items / slots1;
     const int slots = resident_slots(c, G, sm_count, have_device);
     if (slots <= 0) return;
     const int waves = static_cast<int>((static_cast<int64_t>(items) * c.split + slots - 1) / slots);
     double best = static_cast<double>(waves) * ((C + c.split - 1) / c.split + 17.0 + c.split);
-    int tail_split = 0;
-    for (int s = 2; s <= 16 && s <= C; ++s) {
-        TcConfig ct = c1;
-        ct.split = s;
-        if (r * s > resident_slots(ct, G, sm_count, have_device)) continue;  // the tail in one wave
-        const double cost = full_waves * (C + 18.0) + ((C + s - 1) / s + 17.0 + s);
-        if (cost < best - 1e-9) {
-            best = cost;
-            tail_split = s;
+    int main_split = 0, tail_split = 0, tail_items = 0;
+    // The whole waves run unsplit. (Split whole waves, which explicit plans may ask for, were rated
+    // cheaper for 17408 x 5120 at M = 512, split 3 then a tail split 4: 95.0 -> 90.3 us alone, but the
+    // dense-layer sweep step measured 1.717 -> 1.743 ms: the full tail wave leaves the next GEMM no
+    // idle SMs to start on.)
+    for (int s1 = 1; s1 <= 1; ++s1) {
+        TcConfig cm = c;
+        cm.split = s1;
+        const int r = partial_wave_items(cm, M, N, G, sm_count, have_device);
+        if (r <= 0) continue;
+        const int full_waves = items / (resident_slots(cm, G, sm_count, have_device) / s1);
+        for (int s = s1 + 1; s <= 16 && s <= C; ++s) {
+            TcConfig ct = c;
+            ct.split = s;
+            if (r * s > resident_slots(ct, G, sm_count, have_device)) continue;  // the tail in one wave
+            const double cost =
+                full_waves * ((C + s1 - 1) / s1 + 17.0 + s1) + ((C + s - 1) / s + 17.0 + s);
+            if (cost < best - 1e-9) {
+                best = cost;
+                main_split = s1;
+                tail_split = s;
+                tail_items = r;
+            }
         }
     }
     if (tail_split > 0) {
-        c.split = 1;
-        c.tail_items = r;
+        c.split = main_split;
+        c.tail_items = tail_items;
         c.tail_split = tail_split;
     }
 }
@@ -472,8 +479,8 @@ int resolve_plan_uncached(int M, int N, int K, int G, const w4a16_plan* plan, in
         c.tail_items = c.tail_split = 0;
     }
     if (p.tail_split != 0) {  // the last partial wave's items as a second launch, split tail_split ways
-        if (p.tail_split < 2 || p.tail_split > 16 || p.split_k > 1) return W4A16_ERR_INVALID_ARG;
-        c.split = 1;
+        if (p.tail_split < 2 || p.tail_split > 16) return W4A16_ERR_INVALID_ARG;
+        c.split = p.split_k > 0 ? p.split_k : 1;
         c.tail_items = partial_wave_items(c, M, N, G, sm_count, have_device);
         c.tail_split = c.tail_items > 0 ? p.tail_split : 0;
     }
