@@ -162,6 +162,14 @@ def test_every_supported_shape_gets_a_plan(W):
             assert p.k_chunk in (128, 256) and K % p.k_chunk == 0
             assert p.split_k <= K // p.k_chunk
             assert 2 <= p.stages <= 16 and p.m_tile in (16, 32, 64, 128, 256)
+            # a K-split tail only behind unsplit whole waves of the 128- and 256-row tiles, and only
+            # when the work items overfill whole waves (152 one-CTA-per-SM slots without a device)
+            if p.tail_split:
+                items = -(-N // 128) * -(-M // p.m_tile)
+                assert p.m_tile >= 128 and p.split_k == 1 and 2 <= p.tail_split <= min(16, K // p.k_chunk)
+                assert items > 152 and items % 152, (M, N, K, G, items)
+        else:
+            assert p.tail_split == 0
 
 
 def test_boundary_shapes_get_plans(W):
