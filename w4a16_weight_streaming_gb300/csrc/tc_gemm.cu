@@ -72,7 +72,7 @@ struct SmemPlan {
     uint32_t s_off, s_stage;  // scales: s_stages x (ngs * 128 * 2)
     uint32_t red_off;         // split-K partial tile, MT * 128 * 4 (may overlap the x tiles)
     uint32_t bar_off;         // 3 * s_stages + 2 * a_stages + 1 mbarriers
-    uint32_t misc_off;        // tmem address slot, abort flag, two issuer go flags
+    uint32_t misc_off;        // tmem address slot, abort flag, two issuer go flags, items committed
     uint32_t total;           // bytes from the 1024-aligned base
 };
 
@@ -182,7 +182,9 @@ __global__ void __launch_bounds__(threads_for(GROUP_ISSUE, NA, DW), 1)
     // The x tile's own barrier (dedicated issuers: the dequantisation warps wait only for the weights
     // and scales, the issuers for x); the grouped scheme, whose issuing warp also dequantises, keeps
     // one barrier for all three copies.
-    auto xfull_bar = [&](int s) { return GROUP_ISSUE ? full_bar(s) : bar0 + 8u * (2 * s_stages + 2 * a_stages + 1 + s); };
+    auto xfull_bar = [&](int s) {
+        return GROUP_ISSUE ? full_bar(s) : bar0 + 8u * (2 * s_stages + 2 * a_stages + 1 + s);
+    };
     constexpr uint32_t kXBytes = static_cast<uint32_t>(MT * KC * 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.misc_off + 4);
